@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Throughput of causal shared-offset sparse attention, forward + backward.
+
+One step = forward and backward (dQ, dK, dV, dalpha/dtheta) of a 16-layer
+stack of interpolated shared-offset sparse attention over one batch:
+B = 32 sequences of T = 1024 tokens, 8 query / 2 KV heads, head dim 64,
+bf16 I/O, window W = 8, Fibonacci rungs (K = 15) scaled by the linear layer
+schedule alpha_l = 0.5 + l/15, RoPE theta 1e4.  Every layer has its own
+independently drawn Q, K, V, dO (N(0, 1), seeded), so each step streams
+16 distinct layers' tensors (2.6 GB, far above the 129 MB L2: no L2 flush is
+needed between steps).
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; N > 1 under
+torch.distributed.run (one rank per GPU, weak scaling: every rank runs its
+own batch; the per-layer dtheta values are summed across ranks with one
+all-reduce per step, as data-parallel training of theta would).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd sparse-attn tokens/s at T=1024 GQA bf16; HBM GB/s vs GB300 peak"
+B, T, HQ, HKV, D, LAYERS = 32, 1024, 8, 2, 64, 16
+FIB = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987]
+ROPE = 1e4
+SEED = 0
+# unique bytes per token per layer, bf16: Q, O, dO, dQ (Hq heads) + K, V, dK, dV (Hkv heads)
+UNIQUE_BYTES_PER_TOKEN = 2 * D * (4 * HQ + 4 * HKV)
+# FP32 SIMT peak: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.070 GHz max SM clock
+ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+# algorithmic flop per (query head, key) pair, per kernel; D = 64
+FLOP_PER_PAIR = {"fwd": 4 * D, "bwd_q": 6 * D, "bwd_kv": 8 * D}
+FLOP_PER_RUNG_PAIR_DALPHA = 4 * D  # bwd_kv: q.(k0 - k1) and dO.(v0 - v1)
+
+
+def alphas(schedule: str):
+    if schedule == "linear":
+        return [0.5 + l / (LAYERS - 1) for l in range(LAYERS)]
+    if schedule == "coprime":
+        lin = [0.5 + l / (LAYERS - 1) for l in range(LAYERS)]
+        return [lin[(7 * l) % LAYERS] for l in range(LAYERS)]
+    if schedule == "fixed":
+        return [1.0] * LAYERS
+    raise ValueError(schedule)
+
+
+def pair_counts(alpha: float, W: int):
+    """(query, key) pairs per (b, query head) and how many are rung pairs.
+
+    Counts the plain definition: window keys min(W, i) + 1 and a rung with
+    ceil(alpha f) = c and alpha f > W reaching queries i >= c."""
+    import math
+
+    win = sum(min(W, i) + 1 for i in range(T))
+    rung = 0
+    for f in FIB:
+        d = alpha * f
+        if d <= W:
+            continue
+        c = math.ceil(d)
+        rung += max(0, T - c)
+    return win + rung, rung
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def kernel_traffic(kind: str):
+    """Per-launch DRAM bytes of `kind` from the committed ncu summary, or None
+    when there is none or the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "static_offset_sparse_gb300", "csrc", vals.get("source", ""))
+    if not os.path.isfile(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != vals.get("source_sha256_16"):
+        return None
+    try:
+        return float(vals["bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Layer:
+    """One layer's device tensors and its prebuilt C-ABI descriptor."""
+
+    def __init__(self, sfa, lib, x, alpha, W, dev):
+        import ctypes as C
+        import torch
+
+        self.x = x
+        self.alpha = alpha
+        self.o = torch.empty_like(x["q"])
+        self.lse = torch.empty((B, HQ, T), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(x["q"])
+        self.dk = torch.empty_like(x["k"])
+        self.dv = torch.empty_like(x["v"])
+        self.dadt = torch.zeros((2,), dtype=torch.float64, device=dev)
+        self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha, base=FIB, rope_theta=ROPE)
+        self.nws = sfa.workspace_size(self.desc, True)
+        self.ws = torch.empty((self.nws,), dtype=torch.uint8, device=dev)
+        P = lambda t: C.c_void_p(t.data_ptr())  # noqa: E731
+        self.fargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse))
+        self.bargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse),
+                      P(x["do"]), P(self.dq), P(self.dk), P(self.dv), P(self.dadt), P(self.ws),
+                      self.nws)
+        self.lib = lib
+
+    def run(self, stream):
+        rc = self.lib.sfa_forward(*self.fargs, stream)
+        rc = rc or self.lib.sfa_backward(*self.bargs, stream)
+        if rc:
+            raise RuntimeError(f"libsfa status {rc}")
+
+
+def gpu_arm(args, rank, world, dev):
+    import ctypes as C
+    import torch
+    import torch.distributed as dist
+
+    import sfa_inputs as si
+    import static_offset_sparse_gb300 as sfa
+    from static_offset_sparse_gb300._lib import _lib
+
+    lib = _lib()
+    al = alphas(args.schedule)
+    layers = []
+    for l in range(LAYERS):
+        x = si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", si.mix_seed(SEED, 1000 + rank), dev, layer=l)
+        layers.append(Layer(sfa, lib, x, al[l], args.W, dev))
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+    dtheta = torch.zeros((LAYERS,), dtype=torch.float64, device=dev)
+
+    def step():
+        for L in layers:
+            L.run(sp)
+        if world > 1:
+            for l, L in enumerate(layers):
+                dtheta[l] = L.dadt[1]
+            dist.all_reduce(dtheta)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert sfa.get_device_status() == 0
+
+    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    sfa.timing_enable(True)
+    sfa.timing_read()  # drop anything recorded before the timed region
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    kt = sfa.timing_read()
+    sfa.timing_enable(False)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    launches = int(sum(c for _, c in kt.values()))
+
+    # roofline of the dominant kernel (largest summed device time)
+    dom = max(("fwd", "bwd_q", "bwd_kv"), key=lambda k: kt[k][0])
+    flops = 0.0
+    for L in layers:
+        pairs, rung_pairs = pair_counts(L.alpha, args.W)
+        f = pairs * FLOP_PER_PAIR[dom]
+        if dom == "bwd_kv":
+            f += rung_pairs * FLOP_PER_RUNG_PAIR_DALPHA
+        flops += f * B * HQ
+    per_launch_ms = kt[dom][0] / max(1, kt[dom][1])
+    flops_per_launch = flops / LAYERS
+    achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
+    traffic = kernel_traffic(dom)
+    roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 3),
+                "peak": round(ALU_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / ALU_PEAK_TFLOPS, 4), "traffic": traffic,
+                "peak_source": "FP32 SIMT: 152 SM x 128 lanes x 2 x 2.070 GHz",
+                "per_launch_ms": round(per_launch_ms, 4),
+                "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kt.items() if v[1]}}
+    return layers, ms, clk, launches, roofline
+
+
+def e2e_arm(layers, steps, world, dev):
+    """Same step through the C ABI with host buffers: every step copies each
+    layer's Q, K, V, dO from pinned host memory and reads dQ, dK, dV and
+    (dalpha, dtheta) back, inside the timed region."""
+    import ctypes as C
+    import torch
+    import torch.distributed as dist
+
+    host_in = [{n: t.to("cpu").pin_memory() for n, t in L.x.items()} for L in layers]
+    host_out = [{n: torch.empty(getattr(L, n).shape, dtype=getattr(L, n).dtype).pin_memory()
+                 for n in ("dq", "dk", "dv", "dadt")} for L in layers]
+    h2d = sum(t.numel() * t.element_size() for h in host_in for t in h.values())
+    d2h = sum(t.numel() * t.element_size() for h in host_out for t in h.values())
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+
+    def step():
+        for L, hi, ho in zip(layers, host_in, host_out):
+            for n, t in hi.items():
+                L.x[n].copy_(t, non_blocking=True)
+            L.run(sp)
+            for n, t in ho.items():
+                t.copy_(getattr(L, n), non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = (time.perf_counter() - t0) / steps
+    if world > 1:
+        t = torch.tensor([el], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": round(world * B * T / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(el * 1e3, 3), "steps": steps}
+
+
+def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
+    """One oracle fwd+bwd of `layer` for the first nb sequences (both KV heads)."""
+    import oracle as o
+    import sfa_inputs as si
+
+    a = alphas(schedule)[layer]
+    x = si.make_qkvdo(nb, T, HQ, HKV, D, "bf16", si.mix_seed(SEED, 1000), layer=layer)
+    slots = o.interp_slots(FIB, a, W)
+    t0 = time.perf_counter()
+    o.forward(x["q"], x["k"], x["v"], slots, ROPE)
+    o.backward(x["q"], x["k"], x["v"], x["do"], slots, ROPE, alpha=a)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(schedule: str, W: int, budget_s: float = 10.0):
+    """The oracle as it stands on this host: one layer (layer 7), one
+    sequence at a time until ~budget_s of CPU work; throughput scaled to the
+    16-layer step (tokens / (16 x seconds per layer))."""
+    spent, n = 0.0, 0
+    while spent < budget_s and n < 32:
+        spent += oracle_step_sample(schedule, W, 1, 7)
+        n += 1
+    tok_s = n * T / (spent * LAYERS)
+    return {"value": round(tok_s, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, layer 7 of 16 (alpha={alphas(schedule)[7]:.4f}), W={W}, "
+                      f"{n} sequence(s) x {T} tokens, fwd+bwd incl. dtheta, single thread; "
+                      f"{spent:.1f} s; scaled to 16 layers"}
+
+
+def reference_arm(args):
+    """--impl reference: the fp64 oracle timed on this host, each step one
+    sequence of one layer (bounded sample), scaled to the 16-layer step."""
+    for _ in range(args.warmup):
+        oracle_step_sample(args.schedule, args.W, 1, 7)
+    ts = [oracle_step_sample(args.schedule, args.W, 1, 7) for _ in range(args.steps)]
+    sec = sum(ts) / len(ts)
+    val = T / (sec * LAYERS)
+    cb = {"value": round(val, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+          "sample": f"fp64 numpy oracle, one {T}-token sequence of layer 7 per step, W={args.W}, "
+                    "fwd+bwd incl. dtheta, single thread; scaled to 16 layers"}
+    return {"metric": METRIC, "impl": "reference", "value": round(val, 3), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * LAYERS * 1e3 * (B * T) / T, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config(args), "cpu_baseline": cb,
+            "e2e": {"value": round(val, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def config(args):
+    return {"workload": f"interp {args.schedule} schedule, W={args.W}: B={B} T={T} Hq={HQ} Hkv={HKV} "
+                        f"D={D}, {LAYERS} layers, Fibonacci K=15, RoPE 1e4, fwd+bwd+dtheta",
+            "global_batch": B * args.gpus, "seq_len": T, "layers": LAYERS, "W": args.W,
+            "schedule": args.schedule, "parallelism": f"dp{args.gpus}",
+            "l2": "inputs exceed L2 (16 distinct layers, 2.6 GB per step); no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--W", type=int, default=8)
+    ap.add_argument("--schedule", default="linear", choices=["linear", "coprime", "fixed"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    import torch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    from static_offset_sparse_gb300._lib import LIB_PATH
+
+    if not os.path.exists(LIB_PATH):
+        raise SystemExit("libsfa.so is not built: run __graft_entry__.build() first")
+    layers, ms, clk, launches, roofline = gpu_arm(args, rank, world, dev)
+    value = world * B * T / (ms * 1e-3)
+    hbm = UNIQUE_BYTES_PER_TOKEN * B * T * LAYERS / (ms * 1e-3) / 1e9
+    peak = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peak = json.load(open(pk)).get("hbm_gbs")
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic: seeded N(0,1) Q, K, V, dO per layer", "config": config(args),
+           "roofline": roofline,
+           "hbm": {"unique_bytes_per_token_layer": UNIQUE_BYTES_PER_TOKEN,
+                   "achieved_gbs": round(hbm, 1), "peak_gbs": peak,
+                   "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if peak else "fallback 6800",
+                   "frac": round(hbm / (peak or 6800.0), 4)},
+           "gpu_launches": launches, "clocks": clk}
+    if not args.no_e2e:
+        out["e2e"] = e2e_arm(layers, min(args.steps, 5), world, dev)
+    if rank == 0 and world == 1:
+        out["cpu_baseline"] = cpu_baseline(args.schedule, args.W, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

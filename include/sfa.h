@@ -1,0 +1,191 @@
+/*
+ * sfa.h - C ABI of libsfa: causal shared-offset sparse attention on one
+ * NVIDIA GB300 (sm_103a), forward and backward.
+ *
+ * The operation ("Depth-Staggered Fibonacci Spacing for Sparse Attention",
+ * method section): query i attends the keys at distances 0..W (a dense local
+ * window, self included) and at rung distances d_k = alpha * f_k.  A rung
+ * whose distance is not an integer reads the key/value row at real position
+ * i - d_k by linear interpolation between rows floor(i - d_k) and
+ * floor(i - d_k) + 1, which gives alpha a gradient.  RoPE rotates Q and K at
+ * their own positions before the gather.  alpha = 0.5 + sigmoid(theta).
+ * Integer offset lists (Fibonacci at integer alpha, power-of-2, the
+ * Christoffel carry-word offsets of "Christoffel-Balanced Sparse Attention")
+ * run through the same kernels as exact one-row gathers.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are contiguous [B, H, T, D] with D fastest; D must be 64.
+ *    q, o, dO, dq: H = Hq.  k, v, dk, dv: H = Hkv.  Hq % Hkv == 0 and the
+ *    group size G = Hq / Hkv is a power of two <= 32; query head h reads KV
+ *    head h / G.  lse and delta are fp32 [B, Hq, T].
+ *  - All tensor pointers are device pointers, owned by the caller, 16-byte
+ *    aligned.  Host arrays (base offsets, distance lists, outputs of the
+ *    host builders) are read or written during the call and not retained.
+ *  - The library never allocates device memory inside a call; scratch comes
+ *    from the caller's workspace (see sfa_workspace_size).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device entry points only enqueue work and return; they do not
+ *    synchronise.  Asynchronous device-side errors are read with
+ *    sfa_get_device_status.
+ *  - Every function returns an sfa_status code.  On an argument error
+ *    nothing is launched and no output is touched.
+ *  - Gradients are of L = sum(O * dO) (no averaging).
+ */
+#ifndef SFA_H
+#define SFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SFA_OK = 0,
+  SFA_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad range */
+  SFA_ERR_UNSUPPORTED = 2, /* valid but not implemented (D != 64, G not a power of two, ...) */
+  SFA_ERR_CAPACITY = 3,    /* an output array or the workspace is too small */
+  SFA_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  SFA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (device status only) */
+  SFA_ERR_DEVICE_BOUNDS = 6 /* a device-side index check failed (device status only) */
+} sfa_status;
+
+typedef enum { SFA_F32 = 0, SFA_BF16 = 1 } sfa_dtype;
+
+typedef enum { SFA_SCHED_FIXED = 0, SFA_SCHED_LINEAR = 1, SFA_SCHED_COPRIME = 2 } sfa_schedule;
+
+/* Maximum number of rungs (interpolated path) or of distances outside the
+ * contiguous window prefix (integer path) in one call. */
+#define SFA_MAX_RUNGS 256
+
+/* One call's problem description. */
+typedef struct {
+  int32_t B, T, Hq, Hkv, D; /* D must be 64 */
+  int32_t dtype;            /* sfa_dtype of q, k, v, o, dO, dq, dk, dv */
+  /* interpolated path (sfa_forward / sfa_backward) */
+  int32_t W;                /* window: distances 0..W, W >= 0 */
+  double alpha;             /* rung scale, alpha > 0 (the method uses [0.5, 1.5]) */
+  const int32_t* base;      /* host: base offsets f_k (> 0), n_base entries */
+  int32_t n_base;
+  /* integer path (sfa_forward_int / sfa_backward_int) */
+  const int32_t* dist;      /* host: key distances (>= 0), window included; duplicates allowed */
+  int32_t n_dist;
+  /* RoPE: device table written by sfa_rope_table for at least T positions
+   * with D = 64, or NULL for no rotation. */
+  const float* rope;
+} sfa_desc;
+
+/* ---- host builders (no GPU needed) ---------------------------------- */
+
+/* First K terms of 1, 2, 3, 5, 8, ... (each the sum of the previous two),
+ * the Fibonacci base of "Depth-Staggered Fibonacci Spacing for Sparse
+ * Attention", method section.  1 <= K <= 40; out has K entries. */
+int sfa_offsets_fib(int32_t K, int32_t* out);
+
+/* 1, 2, 4, ..., 2^(K-1): the power-of-2 control base of the same page.
+ * 1 <= K <= 31. */
+int sfa_offsets_pow2(int32_t K, int32_t* out);
+
+/* Christoffel carry word c[j] = floor((j+1)m/k) - floor(jm/k), j < k, in
+ * 64-bit integer arithmetic ("Christoffel-Balanced Sparse Attention");
+ * writes the offsets {j : c[j] = 1} ascending, preceded by 0 when
+ * include_zero != 0.  0 < m <= k <= 2^30.  *n_out is always set to the
+ * count; if it exceeds cap, nothing is written and SFA_ERR_CAPACITY is
+ * returned. */
+int sfa_offsets_christoffel(int32_t m, int32_t k, int32_t include_zero, int32_t* out,
+                            int32_t cap, int32_t* n_out);
+
+/* Per-layer alpha ("Depth-Staggered ...", method section): FIXED alpha = 1;
+ * LINEAR alpha_l = 0.5 + l/(L-1); COPRIME: layer l takes the LINEAR value of
+ * index (S*l mod L), gcd(S, L) = 1.  out has L entries.  1 <= L <= 4096. */
+int sfa_alpha_schedule(int32_t L, int32_t kind, int32_t S, double* out);
+
+/* The rung table the interpolated path uses (exposed for testing):
+ * d = fl64(alpha * f) for each base entry; rungs with d <= W are dropped (they
+ * lie in the window); c = ceil(d), w = c - d (fp64, then fp32).  Output is
+ * sorted by c ascending; f_out holds the matching f.  *n_out always set;
+ * SFA_ERR_CAPACITY if it exceeds cap. */
+int sfa_rung_table(const int32_t* base, int32_t n_base, double alpha, int32_t W,
+                   int32_t* c_out, float* w_out, float* f_out, int32_t cap, int32_t* n_out);
+
+/* Sorted, de-duplicated integer distance set used by the integer path
+ * (exposed for testing).  *n_out always set; SFA_ERR_CAPACITY if > cap. */
+int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t cap,
+                      int32_t* n_out);
+
+const char* sfa_status_string(int status);
+
+/* ---- device entry points ------------------------------------------- */
+
+/* Bytes of the RoPE table for T positions (D = 64): T * 32 * 2 floats. */
+int sfa_rope_table_bytes(int32_t T, size_t* bytes);
+
+/* Fill `table` (device, sfa_rope_table_bytes(T)) with cos and sin of
+ * phi(t, j) = t * theta^(-2j/64), t < T, j < 32, evaluated in fp64 and
+ * stored fp32, laid out [T][32][2] = (cos, sin).  Rotation pairs are
+ * (j, j + 32) ("rotate half").  theta > 0. */
+int sfa_rope_table(int32_t T, double theta, float* table, void* stream);
+
+/* Workspace bytes needed by sfa_backward / sfa_backward_int for `d`
+ * (forward needs none).  Holds delta = rowsum(dO * O) and the per-block
+ * partial sums of dL/dalpha. */
+int sfa_workspace_size(const sfa_desc* d, int interp, size_t* bytes);
+
+/* Interpolated-path forward.  Writes o [B,Hq,T,64] (d->dtype) and lse
+ * (fp32 [B,Hq,T], natural log of the softmax denominator including the max
+ * shift).  Keys for query i: window distances 0..min(W, i) and every rung
+ * of sfa_rung_table with c_k <= i (a rung whose position precedes the
+ * sequence is absent, not zero-filled). */
+int sfa_forward(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
+                float* lse, void* stream);
+
+/* Interpolated-path backward.  Inputs are those of the forward plus its
+ * o and lse and the upstream gradient dO.  Writes dq, dk, dv (d->dtype) and,
+ * if dalpha_dtheta != NULL, two device doubles: dL/dalpha and
+ * dL/dtheta = dL/dalpha * (alpha - 0.5) * (1.5 - alpha).  At an integer
+ * rung distance the alpha-derivative is the one-sided one from below
+ * (the interpolation weight w = c - d with c held fixed).  ws must hold
+ * sfa_workspace_size(d, 1) bytes. */
+int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                 double* dalpha_dtheta, void* ws, size_t ws_bytes, void* stream);
+
+/* Integer-offset fast path ("Depth-Staggered ...", method section: integer
+ * offsets as an exact gather; "Christoffel-Balanced Sparse Attention": keys
+ * i - o kept when >= 0).  Keys for query i: i - s for every s in d->dist
+ * with s <= i.  Same outputs as sfa_forward / sfa_backward without the alpha
+ * gradient. */
+int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
+                    float* lse, void* stream);
+int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                     void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* Per-kernel timing for measurement tools.  While enabled, every kernel the
+ * library launches is bracketed by two CUDA events recorded on its own
+ * stream.  sfa_timing_read waits for the recorded events, writes for each
+ * kernel kind (index = sfa_kernel_kind) the summed milliseconds and the
+ * launch count into arrays of n entries, and forgets the records.  Enabling
+ * adds two event records per launch; nothing else changes. */
+typedef enum {
+  SFA_KERNEL_FWD = 0,
+  SFA_KERNEL_BWD_Q = 1,
+  SFA_KERNEL_BWD_KV = 2,
+  SFA_KERNEL_DALPHA = 3,
+  SFA_KERNEL_ROPE = 4,
+  SFA_KERNEL_KINDS = 5
+} sfa_kernel_kind;
+int sfa_timing_enable(int on);
+int sfa_timing_read(double* ms, int64_t* launches, int n);
+
+/* Synchronise `stream`, return in *out the device status word (an
+ * sfa_status recorded by a kernel's bounds check or bounded wait since the
+ * last call, SFA_OK if none) and clear it. */
+int sfa_get_device_status(void* stream, int32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFA_H */

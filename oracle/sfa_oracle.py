@@ -281,8 +281,12 @@ def forward(q, k, v, slots, rope_theta: float = 1e4, rows=None):
     return O, LSE
 
 
-def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = None):
+def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = None, rows=None):
     """Gradients of L = sum(O * dO) (no batch averaging).
+
+    ``rows`` optionally restricts the work to a list of (b, kv_head) pairs:
+    only their dq / dk / dv entries are computed (others stay 0) and dd,
+    dalpha, dtheta then sum over those pairs only.
 
     Returns a dict with dq, dk, dv (fp64, the inputs' shapes), dd (one entry
     per rung slot: dL/dd_k) and, when ``alpha`` is given, dalpha and dtheta.
@@ -315,42 +319,42 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
     dv = np.zeros_like(v)
     rung_ids = [a for a, sl in enumerate(slots) if sl["kind"] == "rung"]
     dd = np.zeros(len(rung_ids))
-    for b in range(B):
-        for g in range(Hkv):
-            Ks, Vs, ok = _slot_rows(k[b, g], v[b, g], slots, T)
-            dKs = np.zeros_like(Ks)
-            dVs = np.zeros_like(Vs)
-            for h in range(g * G, (g + 1) * G):
-                s = np.where(ok, np.einsum("td,ntd->nt", q[b, h], Ks) * scale, -np.inf)
-                m = s.max(axis=0)
-                e = np.exp(s - m)
-                P = e / e.sum(axis=0)
-                O = np.einsum("nt,ntd->td", P, Vs)
-                delta = np.einsum("td,td->t", do[b, h], O)
-                dP = np.einsum("td,ntd->nt", do[b, h], Vs)
-                dS = np.where(ok, P * (dP - delta), 0.0)
-                dq[b, h] = np.einsum("nt,ntd->td", dS, Ks) * scale
-                dKs += dS[:, :, None] * q[b, h][None] * scale
-                dVs += P[:, :, None] * do[b, h][None]
-            for a, sl in enumerate(slots):
-                if sl["kind"] == "win":
-                    s_ = sl["s"]
-                    if s_ >= T:
-                        continue
-                    dk[b, g, : T - s_] += dKs[a, s_:]
-                    dv[b, g, : T - s_] += dVs[a, s_:]
-                else:
-                    c, w = sl["c"], sl["w"]
-                    if c >= T:
-                        continue
-                    dk[b, g, : T - c] += (1.0 - w) * dKs[a, c:]
-                    dk[b, g, 1 : T - c + 1] += w * dKs[a, c:]
-                    dv[b, g, : T - c] += (1.0 - w) * dVs[a, c:]
-                    dv[b, g, 1 : T - c + 1] += w * dVs[a, c:]
-                    r = rung_ids.index(a)
-                    dK_row = k[b, g, : T - c] - k[b, g, 1 : T - c + 1]
-                    dV_row = v[b, g, : T - c] - v[b, g, 1 : T - c + 1]
-                    dd[r] += np.sum(dKs[a, c:] * dK_row) + np.sum(dVs[a, c:] * dV_row)
+    pairs = rows if rows is not None else [(b, g) for b in range(B) for g in range(Hkv)]
+    for b, g in pairs:
+        Ks, Vs, ok = _slot_rows(k[b, g], v[b, g], slots, T)
+        dKs = np.zeros_like(Ks)
+        dVs = np.zeros_like(Vs)
+        for h in range(g * G, (g + 1) * G):
+            s = np.where(ok, np.einsum("td,ntd->nt", q[b, h], Ks) * scale, -np.inf)
+            m = s.max(axis=0)
+            e = np.exp(s - m)
+            P = e / e.sum(axis=0)
+            O = np.einsum("nt,ntd->td", P, Vs)
+            delta = np.einsum("td,td->t", do[b, h], O)
+            dP = np.einsum("td,ntd->nt", do[b, h], Vs)
+            dS = np.where(ok, P * (dP - delta), 0.0)
+            dq[b, h] = np.einsum("nt,ntd->td", dS, Ks) * scale
+            dKs += dS[:, :, None] * q[b, h][None] * scale
+            dVs += P[:, :, None] * do[b, h][None]
+        for a, sl in enumerate(slots):
+            if sl["kind"] == "win":
+                s_ = sl["s"]
+                if s_ >= T:
+                    continue
+                dk[b, g, : T - s_] += dKs[a, s_:]
+                dv[b, g, : T - s_] += dVs[a, s_:]
+            else:
+                c, w = sl["c"], sl["w"]
+                if c >= T:
+                    continue
+                dk[b, g, : T - c] += (1.0 - w) * dKs[a, c:]
+                dk[b, g, 1 : T - c + 1] += w * dKs[a, c:]
+                dv[b, g, : T - c] += (1.0 - w) * dVs[a, c:]
+                dv[b, g, 1 : T - c + 1] += w * dVs[a, c:]
+                r = rung_ids.index(a)
+                dK_row = k[b, g, : T - c] - k[b, g, 1 : T - c + 1]
+                dV_row = v[b, g, : T - c] - v[b, g, 1 : T - c + 1]
+                dd[r] += np.sum(dKs[a, c:] * dK_row) + np.sum(dVs[a, c:] * dV_row)
     if rot:
         dq = rope_apply(dq, cs, sn, inverse=True)
         dk = rope_apply(dk, cs, sn, inverse=True)

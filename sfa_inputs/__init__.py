@@ -105,3 +105,64 @@ def make_qkvdo(B: int, T: int, Hq: int, Hkv: int, D: int, dtype: str,
     if with_do:
         out["do"] = make_tensor((B, Hq, T, D), dtype, seed, layer, TENSOR_IDS["do"])
     return out
+
+
+# ---------------------------------------------------------------- on device
+#
+# The same stream computed with torch integer ops on a device (used by the
+# benchmark, where host generation of gigabytes would dominate the run).  The
+# integer stream is bit-identical to ``splitmix64``; the fp64 Box-Muller may
+# differ from numpy's by an ulp of cos/sin/log, which the storage rounding
+# almost always absorbs.
+
+
+def _as_i64(x: int) -> int:
+    x &= 0xFFFFFFFFFFFFFFFF
+    return x - (1 << 64) if x >= (1 << 63) else x
+
+
+def _lsr(z, s: int):
+    """Logical right shift of int64 values (two's-complement bit pattern)."""
+    import torch
+
+    return (z >> s) & torch.tensor((1 << (64 - s)) - 1, dtype=torch.int64, device=z.device)
+
+
+def normal_device(seed: int, n: int, device, chunk: int = 1 << 24):
+    import torch
+
+    m = (n + 1) // 2
+    out = torch.empty(2 * m, dtype=torch.float64, device=device)
+    g, m1, m2 = _as_i64(0x9E3779B97F4A7C15), _as_i64(0xBF58476D1CE4E5B9), _as_i64(0x94D049BB133111EB)
+    s0 = _as_i64(seed)
+    for lo in range(0, 2 * m, chunk):
+        hi = min(2 * m, lo + chunk)
+        z = torch.arange(lo + 1, hi + 1, dtype=torch.int64, device=device) * g + s0
+        z = (z ^ _lsr(z, 30)) * m1
+        z = (z ^ _lsr(z, 27)) * m2
+        z = z ^ _lsr(z, 31)
+        u = _lsr(z, 11).to(torch.float64) * (1.0 / 9007199254740992.0)
+        r = torch.sqrt(-2.0 * torch.log1p(-u[0::2]))
+        t = 2.0 * torch.pi * u[1::2]
+        out[lo:hi:2] = r * torch.cos(t)
+        out[lo + 1 : hi : 2] = r * torch.sin(t)
+    return out[:n]
+
+
+def make_qkvdo_device(B, T, Hq, Hkv, D, dtype: str, seed: int, device, layer: int = 0,
+                      with_do: bool = True):
+    """``make_qkvdo`` generated directly on ``device``."""
+    import torch
+
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+
+    def one(shape, tid):
+        n = int(np.prod(shape))
+        x = normal_device(mix_seed(seed, layer, tid), n, device)
+        return x.to(torch.float32).to(tdt).reshape(shape)
+
+    out = {"q": one((B, Hq, T, D), TENSOR_IDS["q"]), "k": one((B, Hkv, T, D), TENSOR_IDS["k"]),
+           "v": one((B, Hkv, T, D), TENSOR_IDS["v"])}
+    if with_do:
+        out["do"] = one((B, Hq, T, D), TENSOR_IDS["do"])
+    return out

@@ -1,0 +1,223 @@
+// C ABI device entry points of libsfa: argument checks, the per-call key plan,
+// kernel launches and the device status word.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "sfa_internal.h"
+
+namespace sfa {
+
+int launch_rope_table(int T, double theta, float* table, void* stream);
+
+// Device status word: kernels record SFA_ERR_* codes here (bounded waits,
+// index checks); sfa_get_device_status reads and clears it.
+static __device__ int g_status;
+
+static int status_ptr(int** out) {
+  static std::mutex mu;
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SFA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return SFA_ERR_CUDA;
+    cache[dev] = static_cast<int*>(p);
+  }
+  *out = cache[dev];
+  return SFA_OK;
+}
+
+// ---- launch timing --------------------------------------------------------
+struct TimingRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+static std::mutex g_tmu;
+static std::vector<TimingRec> g_trec;
+static bool g_timing = false;
+
+int timing_start(int kind, void* stream) {
+  std::lock_guard<std::mutex> lock(g_tmu);
+  if (!g_timing) return -1;
+  TimingRec r{kind, nullptr, nullptr};
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return -1;
+  cudaEventRecord(r.a, (cudaStream_t)stream);
+  g_trec.push_back(r);
+  return (int)g_trec.size() - 1;
+}
+
+void timing_stop(int id, void* stream) {
+  if (id < 0) return;
+  std::lock_guard<std::mutex> lock(g_tmu);
+  if (id < (int)g_trec.size()) cudaEventRecord(g_trec[id].b, (cudaStream_t)stream);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int fill_args(const sfa_desc* d, AttnArgs* a) {
+  *a = AttnArgs{};
+  a->B = d->B;
+  a->T = d->T;
+  a->Hq = d->Hq;
+  a->Hkv = d->Hkv;
+  a->lgG = __builtin_ctz((unsigned)(d->Hq / d->Hkv));
+  a->rope = d->rope;
+  a->alpha = d->alpha;
+  if (d->rope && !aligned16(d->rope)) return SFA_ERR_INVALID_ARG;
+  return status_ptr(&a->status);
+}
+
+static int forward_common(const sfa_desc* d, int interp, const void* q, const void* k,
+                          const void* v, void* o, float* lse, void* stream) {
+  int rc = validate_shape(d);
+  if (rc != SFA_OK) return rc;
+  if (!q || !k || !v || !o || !lse) return SFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SFA_ERR_INVALID_ARG;
+  Plan p;
+  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
+  if (rc != SFA_OK) return rc;
+  AttnArgs a;
+  if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out_o = o;
+  a.out_lse = lse;
+  return launch_forward(a, p, d->dtype, stream);
+}
+
+static int backward_common(const sfa_desc* d, int interp, const void* q, const void* k,
+                           const void* v, const void* o, const float* lse, const void* dO,
+                           void* dq, void* dk, void* dv, double* dadt, void* ws,
+                           size_t ws_bytes, void* stream) {
+  int rc = validate_shape(d);
+  if (rc != SFA_OK) return rc;
+  if (d->Hq / d->Hkv > 16) return SFA_ERR_UNSUPPORTED;  // key-side smem budget
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !ws) return SFA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, dO, dq, dk, dv, ws};
+  for (const void* x : ptrs)
+    if (!aligned16(x)) return SFA_ERR_INVALID_ARG;
+  Plan p;
+  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
+  if (rc != SFA_OK) return rc;
+  const size_t need = backward_workspace_bytes(d, p);
+  if (ws_bytes < need) return SFA_ERR_CAPACITY;
+  AttnArgs a;
+  if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dO = dO;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  const int TK = 128 >> a.lgG;
+  const size_t nparts = (size_t)((d->T + TK - 1) / TK) * d->B * d->Hkv;
+  const size_t parts = (nparts * sizeof(double) + 255) & ~(size_t)255;
+  a.dalpha_part = static_cast<double*>(ws);
+  a.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + parts);
+  a.dalpha_out = interp ? dadt : nullptr;
+  return launch_backward(a, p, d->dtype, stream);
+}
+
+}  // namespace sfa
+
+using namespace sfa;
+
+extern "C" {
+
+int sfa_rope_table_bytes(int32_t T, size_t* bytes) {
+  if (T <= 0 || !bytes) return SFA_ERR_INVALID_ARG;
+  *bytes = (size_t)T * 32 * 2 * sizeof(float);
+  return SFA_OK;
+}
+
+int sfa_rope_table(int32_t T, double theta, float* table, void* stream) {
+  if (T <= 0 || T > (1 << 24) || !(theta > 0.0) || !table || !aligned16(table))
+    return SFA_ERR_INVALID_ARG;
+  return launch_rope_table(T, theta, table, stream);
+}
+
+int sfa_workspace_size(const sfa_desc* d, int interp, size_t* bytes) {
+  if (!bytes) return SFA_ERR_INVALID_ARG;
+  int rc = validate_shape(d);
+  if (rc != SFA_OK) return rc;
+  Plan p;
+  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
+  if (rc != SFA_OK) return rc;
+  *bytes = backward_workspace_bytes(d, p);
+  return SFA_OK;
+}
+
+int sfa_forward(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
+                float* lse, void* stream) {
+  return forward_common(d, 1, q, k, v, o, lse, stream);
+}
+
+int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
+                    float* lse, void* stream) {
+  return forward_common(d, 0, q, k, v, o, lse, stream);
+}
+
+int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                 double* dalpha_dtheta, void* ws, size_t ws_bytes, void* stream) {
+  return backward_common(d, 1, q, k, v, o, lse, dO, dq, dk, dv, dalpha_dtheta, ws, ws_bytes,
+                         stream);
+}
+
+int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void* v,
+                     const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                     void* dv, void* ws, size_t ws_bytes, void* stream) {
+  return backward_common(d, 0, q, k, v, o, lse, dO, dq, dk, dv, nullptr, ws, ws_bytes, stream);
+}
+
+int sfa_timing_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_tmu);
+  g_timing = on != 0;
+  return SFA_OK;
+}
+
+int sfa_timing_read(double* ms, int64_t* launches, int n) {
+  if (n < 0 || (n > 0 && (!ms || !launches))) return SFA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_tmu);
+  for (int x = 0; x < n; ++x) {
+    ms[x] = 0.0;
+    launches[x] = 0;
+  }
+  int rc = SFA_OK;
+  for (TimingRec& r : g_trec) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      rc = SFA_ERR_CUDA;
+    else if (r.kind >= 0 && r.kind < n) {
+      ms[r.kind] += t;
+      launches[r.kind] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_trec.clear();
+  return rc;
+}
+
+int sfa_get_device_status(void* stream, int32_t* out) {
+  if (!out) return SFA_ERR_INVALID_ARG;
+  int* p = nullptr;
+  int rc = status_ptr(&p);
+  if (rc != SFA_OK) return rc;
+  int v = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return SFA_ERR_CUDA;
+  *out = v;
+  return SFA_OK;
+}
+
+}  // extern "C"

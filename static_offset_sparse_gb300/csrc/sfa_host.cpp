@@ -1,0 +1,196 @@
+// Host-side builders of libsfa: offset lists, alpha schedules, rung tables and
+// argument validation.  Integer work is exact (64-bit); the rung distances are
+// fp64 products as the method defines them.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "sfa_internal.h"
+
+extern "C" {
+
+int sfa_offsets_fib(int32_t K, int32_t* out) {
+  // "Depth-Staggered Fibonacci Spacing for Sparse Attention", method section:
+  // base 1, 2, 3, 5, ... (15 terms reach 987).  Term 40 is 165580141 < 2^31.
+  if (K < 1 || K > 40 || !out) return SFA_ERR_INVALID_ARG;
+  int64_t a = 1, b = 2;
+  for (int32_t j = 0; j < K; ++j) {
+    out[j] = (int32_t)a;
+    int64_t n = a + b;
+    a = b;
+    b = n;
+  }
+  return SFA_OK;
+}
+
+int sfa_offsets_pow2(int32_t K, int32_t* out) {
+  // Same page, the reach-matched power-of-2 control base.
+  if (K < 1 || K > 31 || !out) return SFA_ERR_INVALID_ARG;
+  for (int32_t j = 0; j < K; ++j) out[j] = (int32_t)(1u << j);
+  return SFA_OK;
+}
+
+int sfa_offsets_christoffel(int32_t m, int32_t k, int32_t include_zero, int32_t* out,
+                            int32_t cap, int32_t* n_out) {
+  // "Christoffel-Balanced Sparse Attention": c[j] = floor((j+1)m/k) - floor(jm/k).
+  if (!n_out || m <= 0 || k <= 0 || m > k || k > (1 << 30)) return SFA_ERR_INVALID_ARG;
+  std::vector<int32_t> o;
+  o.reserve((size_t)m + 1);
+  const int64_t M = m, Kp = k;
+  for (int64_t j = 0; j < Kp; ++j) {
+    int64_t cj = ((j + 1) * M) / Kp - (j * M) / Kp;  // both operands >= 0: floor
+    if (cj == 1) o.push_back((int32_t)j);
+  }
+  if (include_zero && (o.empty() || o[0] != 0)) o.insert(o.begin(), 0);
+  *n_out = (int32_t)o.size();
+  if ((int64_t)o.size() > (int64_t)cap) return SFA_ERR_CAPACITY;
+  if (!out && !o.empty()) return SFA_ERR_INVALID_ARG;
+  std::copy(o.begin(), o.end(), out);
+  return SFA_OK;
+}
+
+int sfa_alpha_schedule(int32_t L, int32_t kind, int32_t S, double* out) {
+  // "Depth-Staggered ...", method section: fixed, linear ramp 0.5 .. 1.5, and
+  // the coprime reassignment l -> S l mod L of the linear values.
+  if (L < 1 || L > 4096 || !out) return SFA_ERR_INVALID_ARG;
+  if (kind == SFA_SCHED_FIXED) {
+    for (int32_t l = 0; l < L; ++l) out[l] = 1.0;
+    return SFA_OK;
+  }
+  auto lin = [L](int64_t l) { return L > 1 ? 0.5 + (double)l / (double)(L - 1) : 1.0; };
+  if (kind == SFA_SCHED_LINEAR) {
+    for (int32_t l = 0; l < L; ++l) out[l] = lin(l);
+    return SFA_OK;
+  }
+  if (kind == SFA_SCHED_COPRIME) {
+    if (S <= 0) return SFA_ERR_INVALID_ARG;
+    int64_t a = S, b = L;
+    while (b) {
+      int64_t t = a % b;
+      a = b;
+      b = t;
+    }
+    if (a != 1) return SFA_ERR_INVALID_ARG;
+    for (int32_t l = 0; l < L; ++l) out[l] = lin(((int64_t)S * l) % L);
+    return SFA_OK;
+  }
+  return SFA_ERR_INVALID_ARG;
+}
+
+int sfa_rung_table(const int32_t* base, int32_t n_base, double alpha, int32_t W,
+                   int32_t* c_out, float* w_out, float* f_out, int32_t cap, int32_t* n_out) {
+  if (!n_out || n_base < 0 || (n_base > 0 && !base) || W < -1) return SFA_ERR_INVALID_ARG;
+  if (!(alpha > 0.0) || !std::isfinite(alpha)) return SFA_ERR_INVALID_ARG;
+  struct R {
+    int64_t c;
+    double w;
+    int32_t f;
+  };
+  std::vector<R> rs;
+  for (int32_t j = 0; j < n_base; ++j) {
+    if (base[j] <= 0) return SFA_ERR_INVALID_ARG;
+    const double d = alpha * (double)base[j];  // fl64(alpha * f_k)
+    if (!(d <= 2147483647.0)) return SFA_ERR_INVALID_ARG;
+    if (d <= (double)W) continue;  // inside the window: the union keeps it once
+    const double c = std::ceil(d);
+    rs.push_back({(int64_t)c, c - d, base[j]});
+  }
+  std::stable_sort(rs.begin(), rs.end(), [](const R& a, const R& b) { return a.c < b.c; });
+  *n_out = (int32_t)rs.size();
+  if ((int64_t)rs.size() > (int64_t)cap) return SFA_ERR_CAPACITY;
+  for (size_t j = 0; j < rs.size(); ++j) {
+    if (c_out) c_out[j] = (int32_t)rs[j].c;
+    if (w_out) w_out[j] = (float)rs[j].w;
+    if (f_out) f_out[j] = (float)rs[j].f;
+  }
+  return SFA_OK;
+}
+
+int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t cap,
+                      int32_t* n_out) {
+  if (!n_out || n_dist < 0 || (n_dist > 0 && !dist)) return SFA_ERR_INVALID_ARG;
+  std::vector<int32_t> s(dist, dist + n_dist);
+  for (int32_t x : s)
+    if (x < 0) return SFA_ERR_INVALID_ARG;
+  std::sort(s.begin(), s.end());
+  s.erase(std::unique(s.begin(), s.end()), s.end());
+  *n_out = (int32_t)s.size();
+  if ((int64_t)s.size() > (int64_t)cap) return SFA_ERR_CAPACITY;
+  if (!out && !s.empty()) return SFA_ERR_INVALID_ARG;
+  std::copy(s.begin(), s.end(), out);
+  return SFA_OK;
+}
+
+const char* sfa_status_string(int s) {
+  switch (s) {
+    case SFA_OK: return "ok";
+    case SFA_ERR_INVALID_ARG: return "invalid argument";
+    case SFA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SFA_ERR_CAPACITY: return "output or workspace too small";
+    case SFA_ERR_CUDA: return "CUDA runtime error";
+    case SFA_ERR_TIMEOUT: return "device wait timed out";
+    case SFA_ERR_DEVICE_BOUNDS: return "device index check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
+
+namespace sfa {
+
+int validate_shape(const sfa_desc* d) {
+  if (!d) return SFA_ERR_INVALID_ARG;
+  if (d->B <= 0 || d->T <= 0 || d->Hq <= 0 || d->Hkv <= 0) return SFA_ERR_INVALID_ARG;
+  if (d->dtype != SFA_F32 && d->dtype != SFA_BF16) return SFA_ERR_INVALID_ARG;
+  if (d->D != kD) return SFA_ERR_UNSUPPORTED;
+  if (d->Hq % d->Hkv != 0) return SFA_ERR_UNSUPPORTED;
+  const int G = d->Hq / d->Hkv;
+  if (G > 32 || (G & (G - 1)) != 0) return SFA_ERR_UNSUPPORTED;
+  if (d->T > (1 << 24) || d->B > 65535 || (int64_t)d->B * d->Hkv > 65535)
+    return SFA_ERR_UNSUPPORTED;  // grid y = B * Hkv
+  return SFA_OK;
+}
+
+int build_interp_plan(const sfa_desc* d, Plan* p) {
+  if (d->W < 0) return SFA_ERR_INVALID_ARG;
+  int32_t n = 0;
+  int rc = sfa_rung_table(d->base, d->n_base, d->alpha, d->W, p->c, p->w, p->f, kMaxRungs, &n);
+  if (rc == SFA_ERR_CAPACITY) return SFA_ERR_UNSUPPORTED;
+  if (rc != SFA_OK) return rc;
+  p->W = d->W;
+  p->n = n;
+  p->interp = 1;
+  return SFA_OK;
+}
+
+int build_int_plan(const sfa_desc* d, Plan* p) {
+  if (d->n_dist <= 0 || !d->dist) return SFA_ERR_INVALID_ARG;
+  std::vector<int32_t> s((size_t)d->n_dist);
+  int32_t n = 0;
+  int rc = sfa_int_distances(d->dist, d->n_dist, s.data(), d->n_dist, &n);
+  if (rc != SFA_OK) return rc;
+  s.resize((size_t)n);
+  // Distance 0 (the query itself) must be present so that no query has an
+  // empty key set, as the window of the method guarantees.
+  if (s.empty() || s[0] != 0) return SFA_ERR_INVALID_ARG;
+  // The contiguous prefix 0..W runs as a window; the rest are exact rungs.
+  int32_t W = -1;
+  size_t j = 0;
+  while (j < s.size() && s[j] == W + 1) {
+    ++W;
+    ++j;
+  }
+  if (s.size() - j > (size_t)kMaxRungs) return SFA_ERR_UNSUPPORTED;
+  p->W = W;
+  p->n = (int32_t)(s.size() - j);
+  p->interp = 0;
+  for (int32_t r = 0; r < p->n; ++r) {
+    p->c[r] = s[j + r];
+    p->w[r] = 0.0f;
+    p->f[r] = 0.0f;
+  }
+  return SFA_OK;
+}
+
+}  // namespace sfa

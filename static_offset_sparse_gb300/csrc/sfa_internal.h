@@ -1,0 +1,73 @@
+// Internal declarations shared by the host code and the CUDA kernels of libsfa.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "sfa.h"
+
+namespace sfa {
+
+constexpr int kD = 64;          // head dimension (the only one supported)
+constexpr int kMaxRungs = SFA_MAX_RUNGS;
+
+// One call's key set, built on the host and passed to every kernel by value.
+// Distances 0..W (W = -1: no window) plus n rungs.  Rung r reads, for query i
+// with c[r] <= i, the row (1 - w[r]) * row[i - c[r]] + w[r] * row[i - c[r] + 1]
+// (w = 0: the exact row i - c[r]).  Rungs are sorted by c ascending and every
+// c[r] > W.  f[r] is the base offset (for dalpha = sum_k f_k dL/dd_k).
+struct Plan {
+  int32_t W;
+  int32_t n;
+  int32_t interp;  // 1: interpolated path (w may be nonzero, dalpha computed)
+  int32_t c[kMaxRungs];
+  float w[kMaxRungs];
+  float f[kMaxRungs];
+};
+
+// Pointers and sizes of one call, passed by value to every kernel.
+// Tensor element type is bf16 or fp32 (a template parameter of the kernels).
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;       // forward output (read by the backward)
+  const void* dO;
+  const float* lse;    // [B, Hq, T]
+  const void* rope;    // float2 [T][32] (cos, sin) or nullptr
+  void* out_o;
+  float* out_lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;        // workspace [B, Hq, T]
+  double* dalpha_part; // workspace, one per backward key-side CTA
+  double* dalpha_out;  // device [2]: dL/dalpha, dL/dtheta (or nullptr)
+  double alpha;
+  int32_t B, T, Hq, Hkv, lgG;  // G = 1 << lgG query heads per KV head
+  int* status;         // device status word
+};
+
+// Kernel launchers (stream is a cudaStream_t).
+int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
+int launch_backward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
+size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p);
+
+// Optional launch timing (sfa_api.cu): returns a record id or -1 when off.
+int timing_start(int kind, void* stream);
+void timing_stop(int id, void* stream);
+
+// Brackets one kernel launch with timing events (no-op while timing is off).
+struct LaunchTimer {
+  int id;
+  void* stream;
+  LaunchTimer(int kind, void* s) : id(timing_start(kind, s)), stream(s) {}
+  ~LaunchTimer() { timing_stop(id, stream); }
+};
+
+// Host helpers (sfa_host.cpp).
+int build_interp_plan(const sfa_desc* d, Plan* p);
+int build_int_plan(const sfa_desc* d, Plan* p);
+int validate_shape(const sfa_desc* d);
+
+}  // namespace sfa
