@@ -34,7 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fwd+bwd sparse-attn tokens/s at T=1024 GQA bf16; HBM GB/s vs GB300 peak"
-B, T, HQ, HKV, D, LAYERS = 32, 1024, 8, 2, 64, 16
+B, T, HQ, HKV, D = 32, 1024, 8, 2, 64
+LAYERS = 16  # --layers changes it for profiling captures of a smaller case
 FIB = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987]
 ROPE = 1e4
 SEED = 0
@@ -47,15 +48,23 @@ FLOP_PER_PAIR = {"fwd": 4 * D, "bwd_q": 6 * D, "bwd_kv": 8 * D}
 FLOP_PER_RUNG_PAIR_DALPHA = 4 * D  # bwd_kv: q.(k0 - k1) and dO.(v0 - v1)
 
 
+SCHED_L = 16  # the schedules are defined over the 16-layer stack
+
+
 def alphas(schedule: str):
     if schedule == "linear":
-        return [0.5 + l / (LAYERS - 1) for l in range(LAYERS)]
+        return [0.5 + l / (SCHED_L - 1) for l in range(SCHED_L)]
     if schedule == "coprime":
-        lin = [0.5 + l / (LAYERS - 1) for l in range(LAYERS)]
-        return [lin[(7 * l) % LAYERS] for l in range(LAYERS)]
+        lin = [0.5 + l / (SCHED_L - 1) for l in range(SCHED_L)]
+        return [lin[(7 * l) % SCHED_L] for l in range(SCHED_L)]
     if schedule == "fixed":
-        return [1.0] * LAYERS
+        return [1.0] * SCHED_L
     raise ValueError(schedule)
+
+
+def layer_ids():
+    """All 16 layers, or (profiling captures) LAYERS of them from layer 7 on."""
+    return list(range(SCHED_L)) if LAYERS == SCHED_L else [(7 + j) % SCHED_L for j in range(LAYERS)]
 
 
 def pair_counts(alpha: float, W: int):
@@ -196,7 +205,7 @@ def gpu_arm(args, rank, world, dev):
     lib = _lib()
     al = alphas(args.schedule)
     layers = []
-    for l in range(LAYERS):
+    for l in layer_ids():
         x = si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", si.mix_seed(SEED, 1000 + rank), dev, layer=l)
         layers.append(Layer(sfa, lib, x, al[l], args.W, dev))
     stream = torch.cuda.current_stream()
@@ -366,14 +375,17 @@ def config(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--W", type=int, default=8)
     ap.add_argument("--schedule", default="linear", choices=["linear", "coprime", "fixed"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
     args = ap.parse_args()
+    global LAYERS
+    LAYERS = args.layers
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -415,7 +427,7 @@ def main():
            "gpu_launches": launches, "clocks": clk}
     if not args.no_e2e:
         out["e2e"] = e2e_arm(layers, min(args.steps, 5), world, dev)
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
         out["cpu_baseline"] = cpu_baseline(args.schedule, args.W, args.cpu_budget)
     if rank == 0:
         print(json.dumps(out), flush=True)
