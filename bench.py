@@ -177,10 +177,11 @@ class Layer:
         self.dv = torch.empty_like(x["v"])
         self.dadt = torch.zeros((2,), dtype=torch.float64, device=dev)
         self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha, base=FIB, rope_theta=ROPE)
-        self.nws = sfa.workspace_size(self.desc, True)
+        self.nws = max(sfa.workspace_size(self.desc, True, True), sfa.workspace_size(self.desc, True, False))
         self.ws = torch.empty((self.nws,), dtype=torch.uint8, device=dev)
         P = lambda t: C.c_void_p(t.data_ptr())  # noqa: E731
-        self.fargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse))
+        self.fargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse),
+                      P(self.ws), self.nws)
         self.bargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse),
                       P(x["do"]), P(self.dq), P(self.dk), P(self.dv), P(self.dadt), P(self.ws),
                       self.nws)

@@ -127,18 +127,22 @@ int sfa_rope_table_bytes(int32_t T, size_t* bytes);
  * (j, j + 32) ("rotate half").  theta > 0. */
 int sfa_rope_table(int32_t T, double theta, float* table, void* stream);
 
-/* Workspace bytes needed by sfa_backward / sfa_backward_int for `d`
- * (forward needs none).  Holds delta = rowsum(dO * O) and the per-block
- * partial sums of dL/dalpha. */
-int sfa_workspace_size(const sfa_desc* d, int interp, size_t* bytes);
+/* Workspace bytes a call needs: interp != 0 for sfa_forward / sfa_backward,
+ * 0 for the integer path; backward != 0 for the backward calls.  The forward
+ * keeps the RoPE-rotated keys there (bf16 I/O); the backward keeps them,
+ * delta = rowsum(dO * O), the rotated queries and the per-(query, slot, head)
+ * softmax terms its key-side kernel reads, and the per-block partial sums of
+ * dL/dalpha.  The contents are scratch: nothing persists between calls. */
+int sfa_workspace_size(const sfa_desc* d, int interp, int backward, size_t* bytes);
 
 /* Interpolated-path forward.  Writes o [B,Hq,T,64] (d->dtype) and lse
  * (fp32 [B,Hq,T], natural log of the softmax denominator including the max
  * shift).  Keys for query i: window distances 0..min(W, i) and every rung
  * of sfa_rung_table with c_k <= i (a rung whose position precedes the
- * sequence is absent, not zero-filled). */
+ * sequence is absent, not zero-filled).  ws must hold
+ * sfa_workspace_size(d, 1, 0) bytes (may be NULL when that is 0). */
 int sfa_forward(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
-                float* lse, void* stream);
+                float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Interpolated-path backward.  Inputs are those of the forward plus its
  * o and lse and the upstream gradient dO.  Writes dq, dk, dv (d->dtype) and,
@@ -157,7 +161,7 @@ int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v,
  * with s <= i.  Same outputs as sfa_forward / sfa_backward without the alpha
  * gradient. */
 int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
-                    float* lse, void* stream);
+                    float* lse, void* ws, size_t ws_bytes, void* stream);
 int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void* v,
                      const void* o, const float* lse, const void* dO, void* dq, void* dk,
                      void* dv, void* ws, size_t ws_bytes, void* stream);
@@ -174,7 +178,8 @@ typedef enum {
   SFA_KERNEL_BWD_KV = 2,
   SFA_KERNEL_DALPHA = 3,
   SFA_KERNEL_ROPE = 4,
-  SFA_KERNEL_KINDS = 5
+  SFA_KERNEL_PREP = 5, /* RoPE-rotated bf16 copy of K for the tensor-core kernels */
+  SFA_KERNEL_KINDS = 6
 } sfa_kernel_kind;
 int sfa_timing_enable(int on);
 int sfa_timing_read(double* ms, int64_t* launches, int n);

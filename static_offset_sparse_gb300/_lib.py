@@ -62,9 +62,9 @@ def _lib():
                 "sfa_int_distances": [_I32P, C.c_int32, _I32P, C.c_int32, _I32P],
                 "sfa_rope_table_bytes": [C.c_int32, C.POINTER(C.c_size_t)],
                 "sfa_rope_table": [C.c_int32, C.c_double, _P, _P],
-                "sfa_workspace_size": [C.POINTER(Desc), C.c_int, C.POINTER(C.c_size_t)],
-                "sfa_forward": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P],
-                "sfa_forward_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P],
+                "sfa_workspace_size": [C.POINTER(Desc), C.c_int, C.c_int, C.POINTER(C.c_size_t)],
+                "sfa_forward": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, C.c_size_t, _P],
+                "sfa_forward_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, C.c_size_t, _P],
                 "sfa_backward": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                  C.c_size_t, _P],
                 "sfa_backward_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,

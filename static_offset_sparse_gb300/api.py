@@ -143,13 +143,21 @@ def _ptr(t):
     return C.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def workspace_size(desc, interp: bool = True) -> int:
+def workspace_size(desc, interp: bool = True, backward: bool = True) -> int:
     n = C.c_size_t(0)
-    check(_lib().sfa_workspace_size(C.byref(desc), int(interp), C.byref(n)), "sfa_workspace_size")
+    check(_lib().sfa_workspace_size(C.byref(desc), int(interp), int(backward), C.byref(n)),
+          "sfa_workspace_size")
     return n.value
 
 
-def _fwd(fn, name, q, k, v, desc, o=None, lse=None):
+def _workspace(desc, interp, backward, device, ws=None):
+    n = workspace_size(desc, interp, backward)
+    if ws is None or ws.numel() < n:
+        ws = _torch().empty((max(n, 1),), dtype=_torch().uint8, device=device)
+    return ws, n
+
+
+def _fwd(fn, name, interp, q, k, v, desc, o=None, lse=None, ws=None):
     torch = _torch()
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, nm)
@@ -158,20 +166,23 @@ def _fwd(fn, name, q, k, v, desc, o=None, lse=None):
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
-    check(fn(C.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream()), name)
+    ws, n = _workspace(desc, interp, False, q.device, ws)
+    check(fn(C.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), n, _stream()),
+          name)
     return o, lse
 
 
-def forward(q, k, v, *, W: int, alpha: float, base, rope_theta: float = 1e4, o=None, lse=None):
+def forward(q, k, v, *, W: int, alpha: float, base, rope_theta: float = 1e4, o=None, lse=None,
+            ws=None):
     """Interpolated path: window 0..W plus rungs alpha*f for f in base."""
     desc = make_desc(q, k, W=W, alpha=alpha, base=base, rope_theta=rope_theta)
-    return _fwd(_lib().sfa_forward, "sfa_forward", q, k, v, desc, o, lse)
+    return _fwd(_lib().sfa_forward, "sfa_forward", True, q, k, v, desc, o, lse, ws)
 
 
-def forward_int(q, k, v, *, dist, rope_theta: float = 1e4, o=None, lse=None):
+def forward_int(q, k, v, *, dist, rope_theta: float = 1e4, o=None, lse=None, ws=None):
     """Integer path: keys i - s for s in dist (0 required)."""
     desc = make_desc(q, k, dist=dist, rope_theta=rope_theta)
-    return _fwd(_lib().sfa_forward_int, "sfa_forward_int", q, k, v, desc, o, lse)
+    return _fwd(_lib().sfa_forward_int, "sfa_forward_int", False, q, k, v, desc, o, lse, ws)
 
 
 def _bwd(interp, q, k, v, o, lse, do, desc, dq=None, dk=None, dv=None, ws=None, dadt=None):
@@ -181,9 +192,7 @@ def _bwd(interp, q, k, v, o, lse, do, desc, dq=None, dk=None, dv=None, ws=None, 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    nws = workspace_size(desc, interp)
-    if ws is None or ws.numel() < nws:
-        ws = torch.empty((nws,), dtype=torch.uint8, device=q.device)
+    ws, nws = _workspace(desc, interp, True, q.device, ws)
     L = _lib()
     if interp:
         if dadt is None:
@@ -215,7 +224,7 @@ def get_device_status() -> int:
     return out.value
 
 
-KERNEL_KINDS = ("fwd", "bwd_q", "bwd_kv", "dalpha_reduce", "rope_table")
+KERNEL_KINDS = ("fwd", "bwd_q", "bwd_kv", "dalpha_reduce", "rope_table", "prep")
 
 
 def timing_enable(on: bool = True) -> None:

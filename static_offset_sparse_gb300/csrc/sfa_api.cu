@@ -70,8 +70,11 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
   return status_ptr(&a->status);
 }
 
+static size_t forward_workspace_bytes(const sfa_desc* d) { return use_tc(d) ? kr_bytes(d) : 0; }
+
 static int forward_common(const sfa_desc* d, int interp, const void* q, const void* k,
-                          const void* v, void* o, float* lse, void* stream) {
+                          const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
+                          void* stream) {
   int rc = validate_shape(d);
   if (rc != SFA_OK) return rc;
   if (!q || !k || !v || !o || !lse) return SFA_ERR_INVALID_ARG;
@@ -79,6 +82,9 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
+  const size_t need = forward_workspace_bytes(d);
+  if (need && (!ws || !aligned16(ws))) return SFA_ERR_INVALID_ARG;
+  if (ws_bytes < need) return SFA_ERR_CAPACITY;
   AttnArgs a;
   if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
   a.q = q;
@@ -86,7 +92,15 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   a.v = v;
   a.out_o = o;
   a.out_lse = lse;
-  return launch_forward(a, p, d->dtype, stream);
+  if (!use_tc(d)) return launch_forward(a, p, d->dtype, stream);
+  const void* kr = k;
+  if (d->rope) {
+    LaunchTimer tm(SFA_KERNEL_PREP, stream);
+    rc = launch_rope_prep(k, d->rope, ws, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
+    if (rc != SFA_OK) return rc;
+    kr = ws;
+  }
+  return launch_forward_tc(a, p, kr, stream);
 }
 
 static int backward_common(const sfa_desc* d, int interp, const void* q, const void* k,
@@ -143,25 +157,25 @@ int sfa_rope_table(int32_t T, double theta, float* table, void* stream) {
   return launch_rope_table(T, theta, table, stream);
 }
 
-int sfa_workspace_size(const sfa_desc* d, int interp, size_t* bytes) {
+int sfa_workspace_size(const sfa_desc* d, int interp, int backward, size_t* bytes) {
   if (!bytes) return SFA_ERR_INVALID_ARG;
   int rc = validate_shape(d);
   if (rc != SFA_OK) return rc;
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
-  *bytes = backward_workspace_bytes(d, p);
+  *bytes = backward ? backward_workspace_bytes(d, p) : forward_workspace_bytes(d);
   return SFA_OK;
 }
 
 int sfa_forward(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
-                float* lse, void* stream) {
-  return forward_common(d, 1, q, k, v, o, lse, stream);
+                float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return forward_common(d, 1, q, k, v, o, lse, ws, ws_bytes, stream);
 }
 
 int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
-                    float* lse, void* stream) {
-  return forward_common(d, 0, q, k, v, o, lse, stream);
+                    float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return forward_common(d, 0, q, k, v, o, lse, ws, ws_bytes, stream);
 }
 
 int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v, const void* o,

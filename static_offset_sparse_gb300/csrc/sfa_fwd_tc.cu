@@ -1,0 +1,332 @@
+// Tensor-core forward (bf16 I/O, G = 4 query heads per KV head).
+//
+// Same result as the SIMT forward ("Depth-Staggered Fibonacci Spacing for
+// Sparse Attention", method section: window 0..W plus rungs read by two-row
+// interpolation after RoPE), organised for mma.sync m16n8k16 (bf16 in, fp32
+// accumulate):
+//
+//  * A warp owns 4 consecutive query positions x the 4 heads of one KV
+//    group = 16 rows (row r = 4 h + p).  Its q' (rotated, scaled by
+//    log2(e)/8) stays in registers as bf16 A fragments.
+//  * Keys are the raw rotated rows K' (bf16, written by the prep kernel) and
+//    raw V rows, staged per CTA as contiguous shifted slabs with cp.async
+//    (rows outside the sequence are zero-filled).
+//  * Window: the 16 keys i0w + 3 - s_lo - 15 .. i0w + 3 - s_lo of a chunk of
+//    12 distances form two n-tiles; the band is masked per row.
+//  * Rung: the 8 B-columns are (floor row, floor-plus-one row) of each of the
+//    4 positions, so the lane holding position p (tig = p) has both raw
+//    logits and applies the interpolation on the logit:
+//    s = (1 - w) q'.K'[i - c] + w q'.K'[i - c + 1].  The probability is split
+//    the same way over the two V rows in the P.V product, so no interpolated
+//    row is ever materialised.  Two rungs share one k16 step of P.V.
+//  * Online softmax in base 2 across window chunks and rung pairs.
+#include <math.h>
+
+#include "sfa_device.cuh"
+#include "sfa_mma.cuh"
+
+namespace sfa {
+
+constexpr int kTcTQ = 64;                  // query positions per CTA
+constexpr int kTcWarps = kTcTQ / 4;        // 16 warps
+constexpr int kTcThreads = kTcWarps * 32;  // 512
+constexpr int kTcRowB = 144;               // smem bytes per staged row (128 + 16 pad)
+constexpr int kTcRegion = 2 * (kTcTQ + 1); // rows per K (or V) region of a stage
+constexpr int kTcStageB = 2 * kTcRegion * kTcRowB;
+constexpr int kTcStages = 3;
+constexpr int kTcWC = 12;                  // window distances per chunk (16 key columns)
+constexpr size_t kFwdTcSmem = (size_t)kTcStages * kTcStageB;
+
+// K' = RoPE(K) as bf16 rows (the operand of every key-side product).
+__global__ void rope_prep_kernel(const bf16* __restrict__ k, const float2* __restrict__ rope,
+                                 bf16* __restrict__ kr, int64_t rows, int T) {
+  const int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (it >= rows * 4) return;
+  const int64_t row = it >> 2;
+  const int pc = (int)(it & 3);
+  const int pos = (int)(row % T);
+  float lo[8], hi[8];
+  load_pair_chunk(k + row * kD, pc, rope, pos, lo, hi);
+  store8(kr + row * kD + 8 * pc, lo);
+  store8(kr + row * kD + 32 + 8 * pc, hi);
+}
+
+int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream) {
+  const int64_t n = rows * 4;
+  rope_prep_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+      static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), rows, T);
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+// q' fragments of a warp's 16 rows: rows gid (head gid>>2) and gid+8 (head
+// 2 + (gid>>2)), position i, scaled by `scale`; RoPE pairs (d, d + 32) sit in
+// k-steps kk and kk + 2 of the same lane.
+__device__ __forceinline__ void load_q_frags(const bf16* q0, const bf16* q1, const float2* rope,
+                                             int i, float scale, uint32_t (*qa)[4]) {
+  const int tig = threadIdx.x & 3;
+  float x[2][4][4];  // [row][kk][e]: e = dims 2tig, 2tig+1, 2tig+8, 2tig+9 of k-step kk
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const bf16* q = rr ? q1 : q0;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float2 u = unpack_bf16(*reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig));
+      const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig + 8));
+      x[rr][kk][0] = u.x;
+      x[rr][kk][1] = u.y;
+      x[rr][kk][2] = v.x;
+      x[rr][kk][3] = v.y;
+    }
+  }
+  if (rope) {
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig + 8));
+      const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = x[rr][kk][e], hi = x[rr][kk + 2][e];
+          x[rr][kk][e] = lo * cs[e] - hi * sn[e];
+          x[rr][kk + 2][e] = lo * sn[e] + hi * cs[e];
+        }
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    qa[kk][0] = pack_bf16(x[0][kk][0] * scale, x[0][kk][1] * scale);
+    qa[kk][1] = pack_bf16(x[1][kk][0] * scale, x[1][kk][1] * scale);
+    qa[kk][2] = pack_bf16(x[0][kk][2] * scale, x[0][kk][3] * scale);
+    qa[kk][3] = pack_bf16(x[1][kk][2] * scale, x[1][kk][3] * scale);
+  }
+}
+
+// S[16 x 8] += q' . K'^T for the 8 key rows whose smem row addresses lane
+// (l & 7) supplies in `rowaddr` (byte address of the row start).
+__device__ __forceinline__ void qk_tile(const uint32_t (*qa)[4], uint32_t rowaddr, float* s) {
+  const int mi = (threadIdx.x & 31) >> 3;
+  uint32_t b[8];
+  ldsm_x4(rowaddr + mi * 16, b[0], b[1], b[2], b[3]);
+  ldsm_x4(rowaddr + 64 + mi * 16, b[4], b[5], b[6], b[7]);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) mma_bf16(s, qa[kk], b[2 * kk], b[2 * kk + 1]);
+}
+
+// O[16 x 64] += P[16 x 16] . V[16 keys x 64]; lane l supplies the address of
+// key row (l & 7) of k-half ((l >> 3) & 1): rowaddr_lo for keys 0..7,
+// rowaddr_hi for keys 8..15.
+__device__ __forceinline__ void pv_tile(const uint32_t* pa, uint32_t rowaddr_lo, uint32_t rowaddr_hi,
+                                        float (*o)[4]) {
+  const int mi = (threadIdx.x & 31) >> 3;
+  const uint32_t base = (mi & 1) ? rowaddr_hi : rowaddr_lo;
+#pragma unroll
+  for (int nd = 0; nd < 8; nd += 2) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(base + (nd + (mi >> 1)) * 16, b0, b1, b2, b3);
+    mma_bf16(o[nd], pa, b0, b1);
+    mma_bf16(o[nd + 1], pa, b2, b3);
+  }
+}
+
+// Stage one group (a window chunk or a rung pair) of K' and V rows.
+//   window chunk s_lo: rows = positions i0 - 12 - s_lo + r, r < 76
+//   rung pair r0:      region a (a = 0, 1) rows = positions i0 - c_{r0+a} + r, r < 65
+// Rows outside [0, T) (and the second region of an unpaired rung) are zeros.
+__device__ __forceinline__ void tc_load_group(const bf16* Kr, const bf16* Vb, const Plan& P, int T,
+                                              int i0, int nwc, int nr, int grp, uint32_t kst,
+                                              uint32_t vst) {
+  const bool win = grp < nwc;
+  const int nrows = win ? kTcTQ + kTcWC : kTcRegion;
+  const int r0 = 2 * (grp - nwc);
+  for (int it = threadIdx.x; it < nrows * 16; it += kTcThreads) {
+    const int r = it >> 4, ch = it & 15;
+    int pos;
+    bool ok;
+    if (win) {
+      pos = i0 - kTcWC - kTcWC * grp + r;
+      ok = true;
+    } else {
+      const int a = r >= kTcTQ + 1;
+      const int rg = r0 + a;
+      ok = rg < nr;
+      pos = i0 - (ok ? P.c[rg] : 0) + (r - a * (kTcTQ + 1));
+    }
+    ok = ok && pos >= 0 && pos < T;
+    const bf16* src = (ch < 8 ? Kr : Vb) + (ok ? (int64_t)pos * kD : 0) + (ch & 7) * 8;
+    const uint32_t dst = (ch < 8 ? kst : vst) + r * kTcRowB + (ch & 7) * 16;
+    cp_async16(dst, src, ok ? 16 : 0);
+  }
+}
+
+template <bool INTERP>
+__global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a, const bf16* Kr,
+                                                                const __grid_constant__ Plan P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int T = a.T;
+  const int i0 = blockIdx.x * kTcTQ, i0w = i0 + 4 * warp;
+  const int p = gid & 3, i = i0w + p;  // position of rows gid and gid + 8
+  const int imax = min(T - 1, i0 + kTcTQ - 1);
+  const int hA = g * 4 + (gid >> 2), hB = hA + 2;  // heads of rows gid, gid + 8
+  const bf16* Kb = Kr + (int64_t)bg * T * kD;
+  const bf16* Vb = static_cast<const bf16*>(a.v) + (int64_t)bg * T * kD;
+  const float2* rope = static_cast<const float2*>(a.rope);
+  const uint32_t sbase = smem_u32(smem);
+
+  uint32_t qa[4][4];
+  {
+    const int ic = min(i, T - 1);
+    const bf16* q = static_cast<const bf16*>(a.q);
+    load_q_frags(q + ((int64_t)(b * a.Hq + hA) * T + ic) * kD, q + ((int64_t)(b * a.Hq + hB) * T + ic) * kD,
+                 rope, ic, 0.125f * kLog2e, qa);
+  }
+  float o[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+
+  // online-softmax step for this lane's logits of rows gid (r = 0) and gid + 8
+  // (r = 1); `s` holds n values per row (invalid = -inf), returns P in place.
+  auto softmax_step = [&](float (*s)[8], int n) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mx = -INFINITY;
+      for (int e = 0; e < n; ++e) mx = fmaxf(mx, s[r][e]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m[r], mx);
+      if (mn == -INFINITY) {  // no key for this row yet
+        for (int e = 0; e < n; ++e) s[r][e] = 0.0f;
+        continue;
+      }
+      const float corr = exp2f(m[r] - mn);
+      m[r] = mn;
+      l[r] *= corr;
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) {
+        o[nd][2 * r] *= corr;
+        o[nd][2 * r + 1] *= corr;
+      }
+      for (int e = 0; e < n; ++e) {
+        const float pe = exp2f(s[r][e] - mn);  // exp2(-inf) = 0
+        s[r][e] = pe;
+        l[r] += pe;
+      }
+    }
+  };
+
+  const int wmax = min(P.W, imax);
+  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
+  int nr = 0;
+  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int NG = nwc + (nr + 1) / 2;
+
+#pragma unroll
+  for (int st = 0; st < kTcStages - 1; ++st) {
+    if (st < NG)
+      tc_load_group(Kb, Vb, P, T, i0, nwc, nr, st, sbase + st * kTcStageB,
+                    sbase + st * kTcStageB + kTcRegion * kTcRowB);
+    cp_async_commit();
+  }
+  for (int grp = 0; grp < NG; ++grp) {
+    cp_async_wait<kTcStages - 2>();
+    __syncthreads();
+    {
+      const int gn = grp + kTcStages - 1;
+      if (gn < NG) {
+        const uint32_t st = sbase + (gn % kTcStages) * kTcStageB;
+        tc_load_group(Kb, Vb, P, T, i0, nwc, nr, gn, st, st + kTcRegion * kTcRowB);
+      }
+      cp_async_commit();
+    }
+    const uint32_t kst = sbase + (grp % kTcStages) * kTcStageB;
+    const uint32_t vst = kst + kTcRegion * kTcRowB;
+    uint32_t pa[4];
+    if (grp < nwc) {
+      // window chunk: key columns n = 0..15 <-> key i0w + 3 - s_lo - 15 + n = smem row 4w + n
+      const int s_lo = kTcWC * grp, s_hi = min(s_lo + kTcWC - 1, P.W);
+      float s[2][8];
+      float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        qk_tile(qa, kst + (4 * warp + 8 * nt + (lane & 7)) * kTcRowB, acc[nt]);
+      const int kb = i0w + 3 - s_lo - 15;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = 8 * nt + 2 * tig + (e & 1);
+          const int dist = i - (kb + n);
+          const bool ok = dist >= s_lo && dist <= s_hi && dist <= i;
+          s[e >> 1][2 * nt + (e & 1)] = ok ? acc[nt][e] : -INFINITY;
+        }
+      softmax_step(s, 4);
+      pa[0] = pack_bf16(s[0][0], s[0][1]);
+      pa[1] = pack_bf16(s[1][0], s[1][1]);
+      pa[2] = pack_bf16(s[0][2], s[0][3]);
+      pa[3] = pack_bf16(s[1][2], s[1][3]);
+      pv_tile(pa, vst + (4 * warp + (lane & 7)) * kTcRowB, vst + (4 * warp + 8 + (lane & 7)) * kTcRowB, o);
+    } else {
+      // rung pair: B column n = 2 p' + e' is row p' + e' of the warp's slab
+      const int r0 = 2 * (grp - nwc);
+      const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
+      float s[2][8];
+      float wgt[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int rg = r0 + x;
+        float acc[4] = {0, 0, 0, 0};
+        qk_tile(qa, kst + (x * (kTcTQ + 1) + colrow) * kTcRowB, acc);
+        const bool ok = rg < nr && p == tig && i >= P.c[rg];
+        const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
+        wgt[x] = w;
+        s[0][x] = ok ? fmaf(w, acc[1], (1.0f - w) * acc[0]) : -INFINITY;
+        s[1][x] = ok ? fmaf(w, acc[3], (1.0f - w) * acc[2]) : -INFINITY;
+      }
+      softmax_step(s, 2);
+      pa[0] = pack_bf16(s[0][0] * (1.0f - wgt[0]), s[0][0] * wgt[0]);
+      pa[1] = pack_bf16(s[1][0] * (1.0f - wgt[0]), s[1][0] * wgt[0]);
+      pa[2] = pack_bf16(s[0][1] * (1.0f - wgt[1]), s[0][1] * wgt[1]);
+      pa[3] = pack_bf16(s[1][1] * (1.0f - wgt[1]), s[1][1] * wgt[1]);
+      pv_tile(pa, vst + colrow * kTcRowB, vst + (kTcTQ + 1 + colrow) * kTcRowB, o);
+    }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+  }
+  if (i >= T) return;
+  bf16* out = static_cast<bf16*>(a.out_o);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int h = r ? hB : hA;
+    const int64_t row = (int64_t)(b * a.Hq + h) * T + i;
+    const float inv = 1.0f / l[r];
+    bf16* op = out + row * kD + 2 * tig;
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd)
+      *reinterpret_cast<uint32_t*>(op + 8 * nd) = pack_bf16(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
+    if (tig == 0) a.out_lse[row] = (m[r] + log2f(l[r])) * kLn2;
+  }
+}
+
+int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  auto kern = p.interp ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
+      cudaSuccess)
+    return SFA_ERR_CUDA;
+  dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
+  LaunchTimer tm(SFA_KERNEL_FWD, stream);
+  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, static_cast<const bf16*>(kr), p);
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+}  // namespace sfa

@@ -49,6 +49,15 @@ struct AttnArgs {
 };
 
 // Kernel launchers (stream is a cudaStream_t).
+// The tensor-core kernels serve bf16 I/O with G = 4; everything else runs the
+// fp32 SIMT kernels.
+inline bool use_tc(const sfa_desc* d) { return d->dtype == SFA_BF16 && d->Hq == 4 * d->Hkv; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline size_t kr_bytes(const sfa_desc* d) {
+  return d->rope ? align256((size_t)d->B * d->Hkv * d->T * 64 * 2) : 0;
+}
+int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream);
+int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream);
 int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 int launch_backward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p);

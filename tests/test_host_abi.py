@@ -95,14 +95,14 @@ def test_descriptor_validation_without_gpu(sfa_lib):
     size = C.c_size_t(0)
     d = Desc()
     d.B, d.T, d.Hq, d.Hkv, d.D, d.dtype, d.W, d.alpha = 1, 16, 8, 2, 64, 1, 8, 1.0
-    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, C.byref(size)) == 0 and size.value > 0
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 0 and size.value > 0
     d.D = 128
-    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, C.byref(size)) == 2
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 2
     d.D, d.Hq = 64, 6  # G = 3 not a power of two
-    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, C.byref(size)) == 2
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 2
     d.Hq, d.dtype = 8, 7
-    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, C.byref(size)) == 1
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 1
     d.dtype = 1
     dist = (C.c_int32 * 2)(3, 5)  # distance 0 missing: a query could have no key
     d.dist, d.n_dist = C.cast(dist, C.POINTER(C.c_int32)), 2
-    assert sfa_lib.sfa_workspace_size(C.byref(d), 0, C.byref(size)) == 1
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 0, 1, C.byref(size)) == 1
