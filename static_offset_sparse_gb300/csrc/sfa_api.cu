@@ -103,6 +103,11 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   return launch_forward_tc(a, p, kr, stream);
 }
 
+static size_t backward_bytes(const sfa_desc* d, const Plan& p) {
+  size_t a, b, c;
+  return use_tc(d) ? backward_tc_workspace_bytes(d, p, &a, &b, &c) : backward_workspace_bytes(d, p);
+}
+
 static int backward_common(const sfa_desc* d, int interp, const void* q, const void* k,
                            const void* v, const void* o, const float* lse, const void* dO,
                            void* dq, void* dk, void* dv, double* dadt, void* ws,
@@ -117,8 +122,7 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
-  const size_t need = backward_workspace_bytes(d, p);
-  if (ws_bytes < need) return SFA_ERR_CAPACITY;
+  if (ws_bytes < backward_bytes(d, p)) return SFA_ERR_CAPACITY;
   AttnArgs a;
   if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
   a.q = q;
@@ -130,12 +134,24 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  a.dalpha_out = interp ? dadt : nullptr;
+  a.dalpha_part = static_cast<double*>(ws);
+  char* w = static_cast<char*>(ws);
+  if (use_tc(d)) {
+    size_t okr, oqt, oco;
+    backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco);
+    const void* kr = k;
+    if (d->rope) {
+      LaunchTimer tm(SFA_KERNEL_PREP, stream);
+      rc = launch_rope_prep(k, d->rope, w + okr, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
+      if (rc != SFA_OK) return rc;
+      kr = w + okr;
+    }
+    return launch_backward_tc(a, p, kr, w + oqt, w + oco, stream);
+  }
   const int TK = 128 >> a.lgG;
   const size_t nparts = (size_t)((d->T + TK - 1) / TK) * d->B * d->Hkv;
-  const size_t parts = (nparts * sizeof(double) + 255) & ~(size_t)255;
-  a.dalpha_part = static_cast<double*>(ws);
-  a.delta = reinterpret_cast<float*>(static_cast<char*>(ws) + parts);
-  a.dalpha_out = interp ? dadt : nullptr;
+  a.delta = reinterpret_cast<float*>(w + align256(nparts * sizeof(double)));
   return launch_backward(a, p, d->dtype, stream);
 }
 
@@ -164,7 +180,7 @@ int sfa_workspace_size(const sfa_desc* d, int interp, int backward, size_t* byte
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
-  *bytes = backward ? backward_workspace_bytes(d, p) : forward_workspace_bytes(d);
+  *bytes = backward ? backward_bytes(d, p) : forward_workspace_bytes(d);
   return SFA_OK;
 }
 

@@ -401,14 +401,19 @@ __global__ void dalpha_reduce_kernel(const double* part, int64_t n, double alpha
   }
 }
 
+int launch_dalpha_reduce(const double* part, int64_t n, double alpha, double* out, void* stream) {
+  LaunchTimer tm(SFA_KERNEL_DALPHA, stream);
+  dalpha_reduce_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(part, n, alpha, out);
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
 static int kv_grid_x(int T, int lgG) { return (T + (128 >> lgG) - 1) / (128 >> lgG); }
 
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p) {
   (void)p;
   const int lgG = __builtin_ctz((unsigned)(d->Hq / d->Hkv));
   const size_t nparts = (size_t)kv_grid_x(d->T, lgG) * d->B * d->Hkv;
-  const size_t parts = (nparts * sizeof(double) + 255) & ~(size_t)255;
-  return parts + (size_t)d->B * d->Hq * d->T * sizeof(float);
+  return align256(nparts * sizeof(double)) + (size_t)d->B * d->Hq * d->T * sizeof(float);
 }
 
 template <typename TIO, bool INTERP>

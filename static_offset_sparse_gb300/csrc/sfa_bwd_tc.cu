@@ -1,0 +1,454 @@
+// Tensor-core backward (bf16 I/O, G = 4): gradients of L = sum(O * dO) for
+// the key set of "Depth-Staggered Fibonacci Spacing for Sparse Attention"
+// (method section), the same quantities as the SIMT backward.
+//
+// bwd_q_tc (per query tile, the forward's warp layout and slab staging):
+//   S = q~.K'^T and dP = dO.V^T from raw rows (a rung's two raw values are
+//   interpolated on the fragment), P = exp(S - LSE), dS = P (dP - delta);
+//   dQ += dS~.K' (dS~ = dS split (1 - w, w) over a rung's two rows), then
+//   dQ = R(-phi) dQ / 8.  dL/dd_k = dS (q~.K'[i-c] - q~.K'[i-c+1])
+//   + P (dO.V[i-c] - dO.V[i-c+1]) comes from the same raw fragments.  For
+//   the key side it writes q~ = q'/8 (bf16) and, per (query, slot, head),
+//   the pair (P, dS) in fp32.
+// bwd_kv_tc (per key tile): dK^T and dV^T accumulate as [64 dims x 8 keys]
+//   mma tiles per warp: A = q~^T or dO^T of the (query, head) pairs that
+//   read the warp's 8 key rows, B = their (dS, P) coefficients: a window
+//   slot s reaches key i - s; a rung (c, w) reaches key i - c with weight
+//   1 - w and key i - c + 1 with weight w.  Each key row is written by one
+//   warp: no atomics.
+#include <math.h>
+
+#include "sfa_tc.cuh"
+
+namespace sfa {
+
+// Partial dot over the 16 dims a lane holds of two rows (the fragment
+// positions of load_q_frags), completed across the quad.
+__device__ __forceinline__ void quad_row_dots(const bf16* x0, const bf16* x1, const bf16* y0,
+                                              const bf16* y1, float* out) {
+  const int tig = threadIdx.x & 3;
+  float acc[2] = {0.0f, 0.0f};
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const bf16* x = rr ? x1 : x0;
+    const bf16* y = rr ? y1 : y0;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) {
+        const float2 u = unpack_bf16(*reinterpret_cast<const uint32_t*>(x + 16 * kk + 2 * tig + 8 * h8));
+        const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(y + 16 * kk + 2 * tig + 8 * h8));
+        acc[rr] = fmaf(u.x, v.x, fmaf(u.y, v.y, acc[rr]));
+      }
+    acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 1);
+    acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 2);
+    out[rr] = acc[rr];
+  }
+}
+
+template <bool INTERP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    bwd_q_tc_kernel(const AttnArgs a, const bf16* Kr, bf16* qt, float2* coef, int NS,
+                    const __grid_constant__ Plan P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ double red[kTcWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int T = a.T;
+  const int i0 = blockIdx.x * kTcTQ, i0w = i0 + 4 * warp;
+  const int p = gid & 3, i = i0w + p;
+  const int ic = min(i, T - 1);
+  const bool act = i < T;
+  const int imax = min(T - 1, i0 + kTcTQ - 1);
+  const int hA = g * 4 + (gid >> 2), hB = hA + 2;
+  const int64_t rowA = (int64_t)(b * a.Hq + hA) * T + ic, rowB = (int64_t)(b * a.Hq + hB) * T + ic;
+  const bf16* Kb = Kr + (int64_t)bg * T * kD;
+  const bf16* Vb = static_cast<const bf16*>(a.v) + (int64_t)bg * T * kD;
+  const float2* rope = static_cast<const float2*>(a.rope);
+  const uint32_t sbase = smem_u32(smem);
+
+  uint32_t qa[4][4], da[4][4];
+  float delta[2], lse2[2];
+  {
+    const bf16* q = static_cast<const bf16*>(a.q);
+    const bf16* dO = static_cast<const bf16*>(a.dO);
+    const bf16* O = static_cast<const bf16*>(a.o);
+    load_q_frags(q + rowA * kD, q + rowB * kD, rope, ic, 0.125f, qa);
+    load_q_frags(dO + rowA * kD, dO + rowB * kD, nullptr, ic, 1.0f, da);
+    quad_row_dots(dO + rowA * kD, dO + rowB * kD, O + rowA * kD, O + rowB * kD, delta);
+    lse2[0] = a.lse[rowA] * kLog2e;
+    lse2[1] = a.lse[rowB] * kLog2e;
+    if (act) {  // q~ = q'/8 for the key side, from the fragments this lane holds
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        *reinterpret_cast<uint32_t*>(qt + rowA * kD + 16 * kk + 2 * tig) = qa[kk][0];
+        *reinterpret_cast<uint32_t*>(qt + rowB * kD + 16 * kk + 2 * tig) = qa[kk][1];
+        *reinterpret_cast<uint32_t*>(qt + rowA * kD + 16 * kk + 2 * tig + 8) = qa[kk][2];
+        *reinterpret_cast<uint32_t*>(qt + rowB * kD + 16 * kk + 2 * tig + 8) = qa[kk][3];
+      }
+    }
+  }
+  float dq[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
+  float dacc = 0.0f;
+  float2* crow = coef + ((int64_t)bg * T + ic) * NS * 4;  // [slot][head] (P, dS) of query i
+  const int hlA = gid >> 2, hlB = hlA + 2;
+
+  const int wmax = min(P.W, imax);
+  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
+  int nr = 0;
+  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int NG = nwc + (nr + 1) / 2;
+
+#pragma unroll
+  for (int st = 0; st < kTcStages - 1; ++st) {
+    if (st < NG)
+      tc_load_group(Kb, Vb, P, T, i0, nwc, nr, st, sbase + st * kTcStageB,
+                    sbase + st * kTcStageB + kTcRegion * kTcRowB);
+    cp_async_commit();
+  }
+  for (int grp = 0; grp < NG; ++grp) {
+    cp_async_wait<kTcStages - 2>();
+    __syncthreads();
+    {
+      const int gn = grp + kTcStages - 1;
+      if (gn < NG) {
+        const uint32_t st = sbase + (gn % kTcStages) * kTcStageB;
+        tc_load_group(Kb, Vb, P, T, i0, nwc, nr, gn, st, st + kTcRegion * kTcRowB);
+      }
+      cp_async_commit();
+    }
+    const uint32_t kst = sbase + (grp % kTcStages) * kTcStageB;
+    const uint32_t vst = kst + kTcRegion * kTcRowB;
+    uint32_t sa[4];
+    if (grp < nwc) {
+      const int s_lo = kTcWC * grp, s_hi = min(s_lo + kTcWC - 1, P.W);
+      float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, dp[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t ro = (4 * warp + 8 * nt + (lane & 7)) * kTcRowB;
+        qk_tile(qa, kst + ro, sc[nt]);
+        qk_tile(da, vst + ro, dp[nt]);
+      }
+      const int kb = i0w + 3 - s_lo - 15;
+      float ds[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = e >> 1;
+          const int dist = i - (kb + 8 * nt + 2 * tig + (e & 1));
+          const bool ok = act && dist >= s_lo && dist <= s_hi && dist <= i;
+          const float pr = ok ? exp2f(fmaf(sc[nt][e], kLog2e, -lse2[r])) : 0.0f;
+          const float d = pr * (dp[nt][e] - delta[r]);
+          ds[r][2 * nt + (e & 1)] = d;
+          if (ok) crow[dist * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
+        }
+      sa[0] = pack_bf16(ds[0][0], ds[0][1]);
+      sa[1] = pack_bf16(ds[1][0], ds[1][1]);
+      sa[2] = pack_bf16(ds[0][2], ds[0][3]);
+      sa[3] = pack_bf16(ds[1][2], ds[1][3]);
+      pv_tile(sa, kst + (4 * warp + (lane & 7)) * kTcRowB, kst + (4 * warp + 8 + (lane & 7)) * kTcRowB, dq);
+    } else {
+      const int r0 = 2 * (grp - nwc);
+      const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
+      float ds[2][2], wgt[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int rg = r0 + x;
+        float sc[4] = {0, 0, 0, 0}, dp[4] = {0, 0, 0, 0};
+        const uint32_t ro = (x * (kTcTQ + 1) + colrow) * kTcRowB;
+        qk_tile(qa, kst + ro, sc);
+        qk_tile(da, vst + ro, dp);
+        const bool ok = act && rg < nr && p == tig && i >= P.c[rg];
+        const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
+        const float f = (INTERP && rg < nr) ? P.f[rg] : 0.0f;
+        wgt[x] = w;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float s = fmaf(w, sc[2 * r + 1], (1.0f - w) * sc[2 * r]);
+          const float dpi = fmaf(w, dp[2 * r + 1], (1.0f - w) * dp[2 * r]);
+          const float pr = ok ? exp2f(fmaf(s, kLog2e, -lse2[r])) : 0.0f;
+          const float d = pr * (dpi - delta[r]);
+          ds[r][x] = d;
+          if (ok) {
+            crow[(P.W + 1 + rg) * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
+            if (INTERP)
+              dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
+          }
+        }
+      }
+      sa[0] = pack_bf16(ds[0][0] * (1.0f - wgt[0]), ds[0][0] * wgt[0]);
+      sa[1] = pack_bf16(ds[1][0] * (1.0f - wgt[0]), ds[1][0] * wgt[0]);
+      sa[2] = pack_bf16(ds[0][1] * (1.0f - wgt[1]), ds[0][1] * wgt[1]);
+      sa[3] = pack_bf16(ds[1][1] * (1.0f - wgt[1]), ds[1][1] * wgt[1]);
+      pv_tile(sa, kst + colrow * kTcRowB, kst + (kTcTQ + 1 + colrow) * kTcRowB, dq);
+    }
+  }
+  cp_async_wait<0>();
+
+  if (INTERP) {  // per-CTA partial of dL/dalpha (fixed-order reduction)
+    double d = (double)dacc;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_down_sync(0xffffffffu, d, off);
+    if (lane == 0) red[warp] = d;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double s = 0.0;
+      for (int x = 0; x < kTcWarps; ++x) s += red[x];
+      a.dalpha_part[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = s;
+    }
+  }
+  if (!act) return;
+  // dQ = R(-phi) dq / 8; dims d (tile nd) and d + 32 (tile nd + 4) share a lane
+  bf16* out = static_cast<bf16*>(a.dq);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int64_t row = r ? rowB : rowA;
+    float v[8][2];
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd) {
+      v[nd][0] = dq[nd][2 * r] * 0.125f;
+      v[nd][1] = dq[nd][2 * r + 1] * 0.125f;
+    }
+    if (rope) {
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {
+        const float4 cs = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)ic * 32 + 8 * nd + 2 * tig));
+        const float c2[2] = {cs.x, cs.z}, s2[2] = {cs.y, cs.w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float lo = v[nd][e], hi = v[nd + 4][e];
+          v[nd][e] = lo * c2[e] + hi * s2[e];
+          v[nd + 4][e] = hi * c2[e] - lo * s2[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd)
+      *reinterpret_cast<uint32_t*>(out + row * kD + 8 * nd + 2 * tig) = pack_bf16(v[nd][0], v[nd][1]);
+  }
+}
+
+constexpr int kKvTK = 32;                 // key rows per CTA (4 warps x 8)
+constexpr int kKvThreads = 128;
+constexpr int kKvQ = kKvTK + 8;           // queries staged per group
+constexpr int kKvRows = kKvQ * 4;         // (query, head) rows per tensor
+constexpr int kKvWC = 9;                  // window distances per chunk (16 queries x 4 heads)
+constexpr int kKvStageB = 2 * kKvRows * kTcRowB;
+constexpr int kKvStages = 2;
+constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB;
+
+// Stage q~ and dO rows of queries qb .. qb + kKvQ - 1 (all 4 heads of the
+// group), row r = 4 (query - qb) + head; queries outside [0, T) are zeros.
+__device__ __forceinline__ void kv_load_group(const bf16* qt, const bf16* dO, int64_t hrow0, int T,
+                                              int qb, uint32_t qst, uint32_t dst) {
+  for (int it = threadIdx.x; it < kKvRows * 16; it += kKvThreads) {
+    const int r = it >> 4, ch = it & 15;
+    const int qq = qb + (r >> 2), h = r & 3;
+    const bool ok = qq >= 0 && qq < T;
+    const int64_t row = (hrow0 + h) * T + (ok ? qq : 0);
+    const bf16* src = (ch < 8 ? qt : dO) + row * kD + (ch & 7) * 8;
+    cp_async16((ch < 8 ? qst : dst) + r * kTcRowB + (ch & 7) * 16, src, ok ? 16 : 0);
+  }
+}
+
+template <bool INTERP>
+__global__ void __launch_bounds__(kKvThreads)
+    bwd_kv_tc_kernel(const AttnArgs a, const bf16* qt, const float2* coef, int NS,
+                     const __grid_constant__ Plan P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int T = a.T;
+  const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * warp;
+  const int j = j0w + gid;  // key row of B column gid
+  const int64_t hrow0 = (int64_t)b * a.Hq + g * 4;
+  const bf16* dO = static_cast<const bf16*>(a.dO);
+  const float2* cbase = coef + (int64_t)bg * T * NS * 4;
+  const uint32_t sbase = smem_u32(smem);
+
+  float dk[4][4], dv[4][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) dk[mt][0] = dk[mt][1] = dk[mt][2] = dk[mt][3] = dv[mt][0] =
+      dv[mt][1] = dv[mt][2] = dv[mt][3] = 0.0f;
+
+  const int wmax = min(P.W, T - 1 - j0);
+  const int nwc = wmax >= 0 ? wmax / kKvWC + 1 : 0;
+  int nr = 0;
+  while (nr < P.n && P.c[nr] <= T - j0) ++nr;
+  const int NG = nwc + nr;
+  auto qbase = [&](int grp) { return grp < nwc ? j0 + kKvWC * grp : j0 + P.c[grp - nwc] - 1; };
+
+  kv_load_group(qt, dO, hrow0, T, qbase(0), sbase, sbase + kKvRows * kTcRowB);
+  cp_async_commit();
+  for (int grp = 0; grp < NG; ++grp) {
+    if (grp + 1 < NG) {
+      const uint32_t st = sbase + ((grp + 1) % kKvStages) * kKvStageB;
+      kv_load_group(qt, dO, hrow0, T, qbase(grp + 1), st, st + kKvRows * kTcRowB);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    const uint32_t qst = sbase + (grp % kKvStages) * kKvStageB;
+    const uint32_t dst = qst + kKvRows * kTcRowB;
+    const bool win = grp < nwc;
+    const int rg = grp - nwc;
+    const int s_lo = kKvWC * grp, s_hi = min(s_lo + kKvWC - 1, P.W);
+    const int c = win ? 0 : P.c[rg];
+    const float w = (!win && INTERP) ? P.w[rg] : 0.0f;
+    const int slot_r = P.W + 1 + rg;
+    const int qb = (win ? j0w + s_lo : j0w + c - 1);  // query of k index 0 (head 0)
+    const int nks = win ? 4 : 3;
+    for (int ks = 0; ks < nks; ++ks) {
+      // B: coefficients of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) for key j,
+      // each as a bf16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi)) so the
+      // products keep the fp32 coefficient to ~2^-16
+      uint32_t bk[2], bvv[2], bkl[2], bvl[2];
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int qi = qb + 4 * ks + 2 * hb + (tig >> 1);
+        float wt = 0.0f;
+        int slot = 0;
+        if (win) {
+          const int s = qi - j;
+          if (s >= s_lo && s <= s_hi) {
+            wt = 1.0f;
+            slot = s;
+          }
+        } else {
+          slot = slot_r;
+          if (qi - j == c) wt = 1.0f - w;
+          else if (qi - j == c - 1) wt = w;
+          if (qi < c) wt = 0.0f;
+        }
+        float pk[2] = {0.0f, 0.0f}, dsk[2] = {0.0f, 0.0f};
+        if (wt != 0.0f && qi < T && j < T) {
+          const float4 cv = __ldg(reinterpret_cast<const float4*>(cbase + ((int64_t)qi * NS + slot) * 4 + 2 * (tig & 1)));
+          pk[0] = wt * cv.x;  // (P, dS) of heads h, h + 1
+          dsk[0] = wt * cv.y;
+          pk[1] = wt * cv.z;
+          dsk[1] = wt * cv.w;
+        }
+        bk[hb] = pack_bf16(dsk[0], dsk[1]);
+        bvv[hb] = pack_bf16(pk[0], pk[1]);
+        const float2 kh = unpack_bf16(bk[hb]), vh = unpack_bf16(bvv[hb]);
+        bkl[hb] = pack_bf16(dsk[0] - kh.x, dsk[1] - kh.y);
+        bvl[hb] = pack_bf16(pk[0] - vh.x, pk[1] - vh.y);
+      }
+      // A: q~^T and dO^T tiles [16 dims x 16 (query, head)] by transposed ldmatrix
+      const int mi = lane >> 3;
+      const uint32_t roff = (32 * warp + 16 * ks + 8 * (mi >> 1) + (lane & 7)) * kTcRowB + 16 * (mi & 1);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t aq[4], ad[4];
+        ldsm_x4_t(qst + roff + 32 * mt, aq[0], aq[1], aq[2], aq[3]);
+        ldsm_x4_t(dst + roff + 32 * mt, ad[0], ad[1], ad[2], ad[3]);
+        mma_bf16(dk[mt], aq, bk[0], bk[1]);
+        mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
+        mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
+        mma_bf16(dv[mt], ad, bvl[0], bvl[1]);
+      }
+    }
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+
+  // dK = R(-phi) dk' at key positions; transpose through shared memory for
+  // row-contiguous stores.  Lane holds dims 16 mt + gid (+8), keys 2 tig (+1).
+  const float2* rope = static_cast<const float2*>(a.rope);
+  if (rope) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int jj = min(j0w + 2 * tig + e, T - 1);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float2 cs = __ldg(rope + (int64_t)jj * 32 + 16 * mt + gid + 8 * hh);
+          const float lo = dk[mt][2 * hh + e], hi = dk[mt + 2][2 * hh + e];
+          dk[mt][2 * hh + e] = lo * cs.x + hi * cs.y;
+          dk[mt + 2][2 * hh + e] = hi * cs.x - lo * cs.y;
+        }
+    }
+  }
+  __syncthreads();
+  bf16* tk = reinterpret_cast<bf16*>(smem) + warp * 2 * 8 * 72;  // [2][8 keys][72]
+  bf16* tv = tk + 8 * 72;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int d = 16 * mt + gid + 8 * hh, n = 2 * tig + e;
+        tk[n * 72 + d] = __float2bfloat16_rn(dk[mt][2 * hh + e]);
+        tv[n * 72 + d] = __float2bfloat16_rn(dv[mt][2 * hh + e]);
+      }
+  __syncwarp();
+  {
+    const int n = lane >> 2, part = lane & 3;  // key n, 16 dims per lane
+    const int jr = j0w + n;
+    if (jr < T) {
+      const int64_t row = ((int64_t)bg * T + jr) * kD + 16 * part;
+      bf16* okp = static_cast<bf16*>(a.dk) + row;
+      bf16* ovp = static_cast<bf16*>(a.dv) + row;
+      const uint4* sk = reinterpret_cast<const uint4*>(tk + n * 72 + 16 * part);
+      const uint4* sv = reinterpret_cast<const uint4*>(tv + n * 72 + 16 * part);
+      reinterpret_cast<uint4*>(okp)[0] = sk[0];
+      reinterpret_cast<uint4*>(okp)[1] = sk[1];
+      reinterpret_cast<uint4*>(ovp)[0] = sv[0];
+      reinterpret_cast<uint4*>(ovp)[1] = sv[1];
+    }
+  }
+}
+
+int launch_dalpha_reduce(const double* part, int64_t n, double alpha, double* out, void* stream);
+
+size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
+                                   size_t* off_coef) {
+  const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * d->Hkv;
+  size_t o = align256(nparts * sizeof(double));
+  *off_kr = o;
+  o += kr_bytes(d);
+  *off_qt = o;
+  o += align256((size_t)d->B * d->Hq * d->T * kD * 2);
+  *off_coef = o;
+  const size_t NS = (size_t)p.W + 1 + p.n;
+  o += align256((size_t)d->B * d->Hkv * d->T * NS * 4 * sizeof(float2));
+  return o;
+}
+
+int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* qt, void* coef,
+                       void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  const int NS = p.W + 1 + p.n;
+  auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
+  auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdKvTcSmem) !=
+          cudaSuccess)
+    return SFA_ERR_CUDA;
+  dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
+  {
+    LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
+    kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, static_cast<const bf16*>(kr), static_cast<bf16*>(qt),
+                                          static_cast<float2*>(coef), NS, p);
+  }
+  dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
+  {
+    LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
+    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, static_cast<const bf16*>(qt),
+                                              static_cast<const float2*>(coef), NS, p);
+  }
+  if (cudaGetLastError() != cudaSuccess) return SFA_ERR_CUDA;
+  if (p.interp && a.dalpha_out)
+    return launch_dalpha_reduce(a.dalpha_part, (int64_t)gq.x * gq.y, a.alpha, a.dalpha_out, stream);
+  return SFA_OK;
+}
+
+}  // namespace sfa

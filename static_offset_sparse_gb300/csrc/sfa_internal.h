@@ -58,6 +58,10 @@ inline size_t kr_bytes(const sfa_desc* d) {
 }
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream);
 int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream);
+size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
+                                   size_t* off_coef);
+int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* qt, void* coef,
+                       void* stream);
 int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 int launch_backward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p);
