@@ -1,5 +1,7 @@
 // C ABI device entry points of libsfa: argument checks, the per-call key plan,
 // kernel launches and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -8,6 +10,50 @@
 #include "sfa_internal.h"
 
 namespace sfa {
+
+// ---- TMA tensor maps (driver entry point, no libcuda link) -----------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h) {
+  auto fn = encode_fn();
+  if (!fn) return SFA_ERR_CUDA;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)T * 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_h};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
+
+int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int box_slots,
+                  int box_q) {
+  auto fn = encode_fn();
+  if (!fn) return SFA_ERR_CUDA;
+  const cuuint64_t dims[4] = {8, (cuuint64_t)NS, (cuuint64_t)T, (cuuint64_t)planes};
+  const cuuint64_t strides[3] = {32, (cuuint64_t)NS * 32, (cuuint64_t)T * NS * 32};
+  const cuuint32_t box[4] = {8, (cuuint32_t)box_slots, (cuuint32_t)box_q, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
 
 int launch_rope_table(int T, double theta, float* table, void* stream);
 

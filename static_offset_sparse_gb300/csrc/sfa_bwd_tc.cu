@@ -12,6 +12,7 @@
 //   the pair (P, dS) in fp32.
 // bwd_kv_tc (per key tile): dK^T and dV^T accumulate as [64 dims x 8 keys]
 //   mma tiles per warp: A = q~^T or dO^T of the (query, head) pairs that
+//   (staged by TMA)
 //   read the warp's 8 key rows, B = their (dS, P) coefficients: a window
 //   slot s reaches key i - s; a rung (c, w) reaches key i - c with weight
 //   1 - w and key i - c + 1 with weight w.  Each key row is written by one
@@ -48,10 +49,13 @@ __device__ __forceinline__ void quad_row_dots(const bf16* x0, const bf16* x1, co
 
 template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    bwd_q_tc_kernel(const AttnArgs a, const bf16* Kr, bf16* qt, float2* coef, int NS,
+    bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, bf16* qt, float2* coef, int NS,
                     const __grid_constant__ Plan P) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kTcStages];
   __shared__ double red[kTcWarps];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
@@ -63,10 +67,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int imax = min(T - 1, i0 + kTcTQ - 1);
   const int hA = g * 4 + (gid >> 2), hB = hA + 2;
   const int64_t rowA = (int64_t)(b * a.Hq + hA) * T + ic, rowB = (int64_t)(b * a.Hq + hB) * T + ic;
-  const bf16* Kb = Kr + (int64_t)bg * T * kD;
-  const bf16* Vb = static_cast<const bf16*>(a.v) + (int64_t)bg * T * kD;
   const float2* rope = static_cast<const float2*>(a.rope);
-  const uint32_t sbase = smem_u32(smem);
 
   uint32_t qa[4][4], da[4][4];
   float delta[2], lse2[2];
@@ -101,68 +102,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int nr = 0;
   while (nr < P.n && P.c[nr] <= imax) ++nr;
   const int NG = nwc + (nr + 1) / 2;
+  const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
-#pragma unroll
-  for (int st = 0; st < kTcStages - 1; ++st) {
-    if (st < NG)
-      tc_load_group(Kb, Vb, P, T, i0, nwc, nr, st, sbase + st * kTcStageB,
-                    sbase + st * kTcStageB + kTcRegion * kTcRowB);
-    cp_async_commit();
-  }
-  for (int grp = 0; grp < NG; ++grp) {
-    cp_async_wait<kTcStages - 2>();
-    __syncthreads();
-    {
-      const int gn = grp + kTcStages - 1;
-      if (gn < NG) {
-        const uint32_t st = sbase + (gn % kTcStages) * kTcStageB;
-        tc_load_group(Kb, Vb, P, T, i0, nwc, nr, gn, st, st + kTcRegion * kTcRowB);
-      }
-      cp_async_commit();
-    }
-    const uint32_t kst = sbase + (grp % kTcStages) * kTcStageB;
-    const uint32_t vst = kst + kTcRegion * kTcRowB;
+  const bool ok = tc_pipeline(&mk, &mv, P, bg, i0, nwc, nr, NG, sbase, bars, a.status,
+                              [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t sa[4];
     if (grp < nwc) {
       const int s_lo = kTcWC * grp, s_hi = min(s_lo + kTcWC - 1, P.W);
       float sc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, dp[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t ro = (4 * warp + 8 * nt + (lane & 7)) * kTcRowB;
-        qk_tile(qa, kst + ro, sc[nt]);
-        qk_tile(da, vst + ro, dp[nt]);
+        const int row = 4 * warp + 8 * nt + (lane & 7);
+        qk_tile(qa, kst, row, sc[nt]);
+        qk_tile(da, vst, row, dp[nt]);
       }
-      const int kb = i0w + 3 - s_lo - 15;
       float ds[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = e >> 1;
-          const int dist = i - (kb + 8 * nt + 2 * tig + (e & 1));
-          const bool ok = act && dist >= s_lo && dist <= s_hi && dist <= i;
-          const float pr = ok ? exp2f(fmaf(sc[nt][e], kLog2e, -lse2[r])) : 0.0f;
+          const int dist = p + 12 + s_lo - (8 * nt + 2 * tig + (e & 1));
+          const bool v = act && dist >= s_lo && dist <= s_hi && dist <= i;
+          const float pr = v ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[r])) : 0.0f;
           const float d = pr * (dp[nt][e] - delta[r]);
           ds[r][2 * nt + (e & 1)] = d;
-          if (ok) crow[dist * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
+          if (v) crow[dist * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
         }
       sa[0] = pack_bf16(ds[0][0], ds[0][1]);
       sa[1] = pack_bf16(ds[1][0], ds[1][1]);
       sa[2] = pack_bf16(ds[0][2], ds[0][3]);
       sa[3] = pack_bf16(ds[1][2], ds[1][3]);
-      pv_tile(sa, kst + (4 * warp + (lane & 7)) * kTcRowB, kst + (4 * warp + 8 + (lane & 7)) * kTcRowB, dq);
+      pv_tile(sa, kst, 4 * warp + (lane & 7), 4 * warp + 8 + (lane & 7), dq);
     } else {
       const int r0 = 2 * (grp - nwc);
-      const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
       float ds[2][2], wgt[2];
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int rg = r0 + x;
         float sc[4] = {0, 0, 0, 0}, dp[4] = {0, 0, 0, 0};
-        const uint32_t ro = (x * (kTcTQ + 1) + colrow) * kTcRowB;
-        qk_tile(qa, kst + ro, sc);
-        qk_tile(da, vst + ro, dp);
-        const bool ok = act && rg < nr && p == tig && i >= P.c[rg];
+        const int row = x * kTcBoxRows + colrow;
+        qk_tile(qa, kst, row, sc);
+        qk_tile(da, vst, row, dp);
+        const bool v = act && rg < nr && p == tig && i >= P.c[rg];
         const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
         const float f = (INTERP && rg < nr) ? P.f[rg] : 0.0f;
         wgt[x] = w;
@@ -170,10 +152,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int r = 0; r < 2; ++r) {
           const float s = fmaf(w, sc[2 * r + 1], (1.0f - w) * sc[2 * r]);
           const float dpi = fmaf(w, dp[2 * r + 1], (1.0f - w) * dp[2 * r]);
-          const float pr = ok ? exp2f(fmaf(s, kLog2e, -lse2[r])) : 0.0f;
+          const float pr = v ? ex2(fmaf(s, kLog2e, -lse2[r])) : 0.0f;
           const float d = pr * (dpi - delta[r]);
           ds[r][x] = d;
-          if (ok) {
+          if (v) {
             crow[(P.W + 1 + rg) * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
             if (INTERP)
               dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
@@ -184,10 +166,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       sa[1] = pack_bf16(ds[1][0] * (1.0f - wgt[0]), ds[1][0] * wgt[0]);
       sa[2] = pack_bf16(ds[0][1] * (1.0f - wgt[1]), ds[0][1] * wgt[1]);
       sa[3] = pack_bf16(ds[1][1] * (1.0f - wgt[1]), ds[1][1] * wgt[1]);
-      pv_tile(sa, kst + colrow * kTcRowB, kst + (kTcTQ + 1 + colrow) * kTcRowB, dq);
+      pv_tile(sa, kst, colrow, kTcBoxRows + colrow, dq);
     }
-  }
-  cp_async_wait<0>();
+  });
+  if (!ok) return;
 
   if (INTERP) {  // per-CTA partial of dL/dalpha (fixed-order reduction)
     double d = (double)dacc;
@@ -232,44 +214,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-constexpr int kKvTK = 32;                 // key rows per CTA (4 warps x 8)
+constexpr int kKvTK = 32;                     // key rows per CTA (4 warps x 8)
 constexpr int kKvThreads = 128;
-constexpr int kKvQ = kKvTK + 8;           // queries staged per group
-constexpr int kKvRows = kKvQ * 4;         // (query, head) rows per tensor
-constexpr int kKvWC = 9;                  // window distances per chunk (16 queries x 4 heads)
-constexpr int kKvStageB = 2 * kKvRows * kTcRowB;
+constexpr int kKvQ = kKvTK + 8;               // queries staged per group
+constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
+constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][40 queries][128 B]
+constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // (P, dS) box: [40 queries][9 slots][4 heads]
+constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
-constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB;
-
-// Stage q~ and dO rows of queries qb .. qb + kKvQ - 1 (all 4 heads of the
-// group), row r = 4 (query - qb) + head; queries outside [0, T) are zeros.
-__device__ __forceinline__ void kv_load_group(const bf16* qt, const bf16* dO, int64_t hrow0, int T,
-                                              int qb, uint32_t qst, uint32_t dst) {
-  for (int it = threadIdx.x; it < kKvRows * 16; it += kKvThreads) {
-    const int r = it >> 4, ch = it & 15;
-    const int qq = qb + (r >> 2), h = r & 3;
-    const bool ok = qq >= 0 && qq < T;
-    const int64_t row = (hrow0 + h) * T + (ok ? qq : 0);
-    const bf16* src = (ch < 8 ? qt : dO) + row * kD + (ch & 7) * 8;
-    cp_async16((ch < 8 ? qst : dst) + r * kTcRowB + (ch & 7) * 16, src, ok ? 16 : 0);
-  }
-}
+constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 
 template <bool INTERP>
 __global__ void __launch_bounds__(kKvThreads)
-    bwd_kv_tc_kernel(const AttnArgs a, const bf16* qt, const float2* coef, int NS,
-                     const __grid_constant__ Plan P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    bwd_kv_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mq,
+                     const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mcw,
+                     const __grid_constant__ CUtensorMap mcr, const __grid_constant__ Plan P) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kKvStages];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int T = a.T;
   const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * warp;
   const int j = j0w + gid;  // key row of B column gid
-  const int64_t hrow0 = (int64_t)b * a.Hq + g * 4;
-  const bf16* dO = static_cast<const bf16*>(a.dO);
-  const float2* cbase = coef + (int64_t)bg * T * NS * 4;
-  const uint32_t sbase = smem_u32(smem);
+  const int hplane = b * a.Hq + g * 4;
 
   float dk[4][4], dv[4][4];
 #pragma unroll
@@ -281,53 +251,74 @@ __global__ void __launch_bounds__(kKvThreads)
   int nr = 0;
   while (nr < P.n && P.c[nr] <= T - j0) ++nr;
   const int NG = nwc + nr;
-  auto qbase = [&](int grp) { return grp < nwc ? j0 + kKvWC * grp : j0 + P.c[grp - nwc] - 1; };
+  // group -> first staged query: window chunk s_lo = 9 grp, or rung grp - nwc
+  auto qb_of = [&](int grp) { return grp < nwc ? j0 + kKvWC * grp : j0 + P.c[grp - nwc] - 1; };
+  auto issue = [&](int grp, uint32_t st, uint32_t bar) {
+    const bool win = grp < nwc;
+    const int qb = qb_of(grp);
+    mbar_expect_tx(bar, 2 * kKvPlaneB + (win ? kKvCoefB : kKvQ * 32));
+    tma_load_3d(st, &mq, 0, qb, hplane, bar);
+    tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
+    if (win)
+      tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, bg, bar);
+    else
+      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + (grp - nwc), qb, bg, bar);
+  };
 
-  kv_load_group(qt, dO, hrow0, T, qbase(0), sbase, sbase + kKvRows * kTcRowB);
-  cp_async_commit();
+  if (tid == 0) {
+    for (int s = 0; s < kKvStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int s = 0; s < kKvStages && s < NG; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
   for (int grp = 0; grp < NG; ++grp) {
-    if (grp + 1 < NG) {
-      const uint32_t st = sbase + ((grp + 1) % kKvStages) * kKvStageB;
-      kv_load_group(qt, dO, hrow0, T, qbase(grp + 1), st, st + kKvRows * kTcRowB);
+    const int st = grp % kKvStages;
+    const bool okw = mbar_wait_bounded(smem_u32(&bars[st]), (grp / kKvStages) & 1);
+    if (__syncthreads_or(!okw)) {
+      if (tid == 0) {
+        record_status(a.status, SFA_ERR_TIMEOUT);
+        for (int g2 = grp; g2 < NG && g2 < grp + kKvStages; ++g2)
+          mbar_wait_bounded(smem_u32(&bars[g2 % kKvStages]), (g2 / kKvStages) & 1);
+      }
+      return;
     }
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const uint32_t qst = sbase + (grp % kKvStages) * kKvStageB;
-    const uint32_t dst = qst + kKvRows * kTcRowB;
+    const uint32_t qst = sbase + st * kKvStageB;
+    const uint32_t dst = qst + kKvPlaneB;
+    const float* csm = reinterpret_cast<const float*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
     const bool win = grp < nwc;
     const int rg = grp - nwc;
     const int s_lo = kKvWC * grp, s_hi = min(s_lo + kKvWC - 1, P.W);
     const int c = win ? 0 : P.c[rg];
     const float w = (!win && INTERP) ? P.w[rg] : 0.0f;
-    const int slot_r = P.W + 1 + rg;
-    const int qb = (win ? j0w + s_lo : j0w + c - 1);  // query of k index 0 (head 0)
+    const int nsl = win ? kKvWC : 1;      // slots per staged query
+    const int qb = qb_of(grp);            // first staged query (slab row 0)
+    const int qw = qb + 8 * warp;         // query of k index 0 of this warp
     const int nks = win ? 4 : 3;
     for (int ks = 0; ks < nks; ++ks) {
-      // B: coefficients of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) for key j,
-      // each as a bf16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi)) so the
-      // products keep the fp32 coefficient to ~2^-16
+      // B: (dS, P) of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) for key j,
+      // as bf16 hi + lo pairs (hi = bf16(x), lo = bf16(x - hi))
       uint32_t bk[2], bvv[2], bkl[2], bvl[2];
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
-        const int qi = qb + 4 * ks + 2 * hb + (tig >> 1);
+        const int ql = 4 * ks + 2 * hb + (tig >> 1);  // query offset from qw
+        const int qi = qw + ql;
         float wt = 0.0f;
-        int slot = 0;
+        int sl = 0;
         if (win) {
           const int s = qi - j;
           if (s >= s_lo && s <= s_hi) {
             wt = 1.0f;
-            slot = s;
+            sl = s - s_lo;
           }
         } else {
-          slot = slot_r;
           if (qi - j == c) wt = 1.0f - w;
           else if (qi - j == c - 1) wt = w;
           if (qi < c) wt = 0.0f;
         }
         float pk[2] = {0.0f, 0.0f}, dsk[2] = {0.0f, 0.0f};
         if (wt != 0.0f && qi < T && j < T) {
-          const float4 cv = __ldg(reinterpret_cast<const float4*>(cbase + ((int64_t)qi * NS + slot) * 4 + 2 * (tig & 1)));
+          const float4 cv = *reinterpret_cast<const float4*>(csm + ((8 * warp + ql) * nsl + sl) * 8 + 4 * (tig & 1));
           pk[0] = wt * cv.x;  // (P, dS) of heads h, h + 1
           dsk[0] = wt * cv.y;
           pk[1] = wt * cv.z;
@@ -339,14 +330,17 @@ __global__ void __launch_bounds__(kKvThreads)
         bkl[hb] = pack_bf16(dsk[0] - kh.x, dsk[1] - kh.y);
         bvl[hb] = pack_bf16(pk[0] - vh.x, pk[1] - vh.y);
       }
-      // A: q~^T and dO^T tiles [16 dims x 16 (query, head)] by transposed ldmatrix
+      // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
+      // k index kx = 4 (query offset) + head lives in slab row head * 40 + query
       const int mi = lane >> 3;
-      const uint32_t roff = (32 * warp + 16 * ks + 8 * (mi >> 1) + (lane & 7)) * kTcRowB + 16 * (mi & 1);
+      const int kx = 8 * (mi >> 1) + (lane & 7);
+      const int arow = (kx & 3) * kKvQ + 8 * warp + 4 * ks + (kx >> 2);
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t aq[4], ad[4];
-        ldsm_x4_t(qst + roff + 32 * mt, aq[0], aq[1], aq[2], aq[3]);
-        ldsm_x4_t(dst + roff + 32 * mt, ad[0], ad[1], ad[2], ad[3]);
+        const uint32_t off = swz(arow, 2 * mt + (mi & 1));
+        ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
+        ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
         mma_bf16(dk[mt], aq, bk[0], bk[1]);
         mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
         mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
@@ -354,8 +348,8 @@ __global__ void __launch_bounds__(kKvThreads)
       }
     }
     __syncthreads();
+    if (tid == 0 && grp + kKvStages < NG) issue(grp + kKvStages, qst, smem_u32(&bars[st]));
   }
-  cp_async_wait<0>();
 
   // dK = R(-phi) dk' at key positions; transpose through shared memory for
   // row-contiguous stores.  Lane holds dims 16 mt + gid (+8), keys 2 tig (+1).
@@ -375,8 +369,7 @@ __global__ void __launch_bounds__(kKvThreads)
         }
     }
   }
-  __syncthreads();
-  bf16* tk = reinterpret_cast<bf16*>(smem) + warp * 2 * 8 * 72;  // [2][8 keys][72]
+  bf16* tk = reinterpret_cast<bf16*>(sgen) + warp * 2 * 8 * 72;  // [2][8 keys][72]
   bf16* tv = tk + 8 * 72;
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt)
@@ -394,14 +387,14 @@ __global__ void __launch_bounds__(kKvThreads)
     const int jr = j0w + n;
     if (jr < T) {
       const int64_t row = ((int64_t)bg * T + jr) * kD + 16 * part;
-      bf16* okp = static_cast<bf16*>(a.dk) + row;
-      bf16* ovp = static_cast<bf16*>(a.dv) + row;
       const uint4* sk = reinterpret_cast<const uint4*>(tk + n * 72 + 16 * part);
       const uint4* sv = reinterpret_cast<const uint4*>(tv + n * 72 + 16 * part);
-      reinterpret_cast<uint4*>(okp)[0] = sk[0];
-      reinterpret_cast<uint4*>(okp)[1] = sk[1];
-      reinterpret_cast<uint4*>(ovp)[0] = sv[0];
-      reinterpret_cast<uint4*>(ovp)[1] = sv[1];
+      uint4* okp = reinterpret_cast<uint4*>(static_cast<bf16*>(a.dk) + row);
+      uint4* ovp = reinterpret_cast<uint4*>(static_cast<bf16*>(a.dv) + row);
+      okp[0] = sk[0];
+      okp[1] = sk[1];
+      ovp[0] = sv[0];
+      ovp[1] = sv[1];
     }
   }
 }
@@ -426,6 +419,15 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
                        void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   const int NS = p.W + 1 + p.n;
+  const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
+  CUtensorMap mk, mv, mq, md, mcw, mcr;
+  if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
+      make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
+      make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
+      make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
+      make_coef_map(&mcw, coef, kvplanes, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
+      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 1, kKvQ) != SFA_OK)
+    return SFA_ERR_CUDA;
   auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
   auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
   if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
@@ -436,14 +438,13 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
-    kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, static_cast<const bf16*>(kr), static_cast<bf16*>(qt),
+    kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, static_cast<bf16*>(qt),
                                           static_cast<float2*>(coef), NS, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
-    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, static_cast<const bf16*>(qt),
-                                              static_cast<const float2*>(coef), NS, p);
+    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, mq, md, mcw, mcr, p);
   }
   if (cudaGetLastError() != cudaSuccess) return SFA_ERR_CUDA;
   if (p.interp && a.dalpha_out)

@@ -9,8 +9,8 @@
 //    group = 16 rows (row r = 4 h + p).  Its q' (rotated, scaled by
 //    log2(e)/8) stays in registers as bf16 A fragments.
 //  * Keys are the raw rotated rows K' (bf16, written by the prep kernel) and
-//    raw V rows, staged per CTA as contiguous shifted slabs with cp.async
-//    (rows outside the sequence are zero-filled).
+//    raw V rows, staged per CTA as contiguous shifted slabs by TMA (rows
+//    outside the sequence are zero-filled by the copy engine).
 //  * Window: the 16 keys i0w + 3 - s_lo - 15 .. i0w + 3 - s_lo of a chunk of
 //    12 distances form two n-tiles; the band is masked per row.
 //  * Rung: the 8 B-columns are (floor row, floor-plus-one row) of each of the
@@ -48,9 +48,12 @@ int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, in
 }
 
 template <bool INTERP>
-__global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a, const bf16* Kr,
-                                                                const __grid_constant__ Plan P) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ Plan P) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kTcStages];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
@@ -59,10 +62,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a,
   const int p = gid & 3, i = i0w + p;  // position of rows gid and gid + 8
   const int imax = min(T - 1, i0 + kTcTQ - 1);
   const int hA = g * 4 + (gid >> 2), hB = hA + 2;  // heads of rows gid, gid + 8
-  const bf16* Kb = Kr + (int64_t)bg * T * kD;
-  const bf16* Vb = static_cast<const bf16*>(a.v) + (int64_t)bg * T * kD;
   const float2* rope = static_cast<const float2*>(a.rope);
-  const uint32_t sbase = smem_u32(smem);
 
   uint32_t qa[4][4];
   {
@@ -77,29 +77,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a,
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
 
   // online-softmax step for this lane's logits of rows gid (r = 0) and gid + 8
-  // (r = 1); `s` holds n values per row (invalid = -inf), returns P in place.
-  auto softmax_step = [&](float (*s)[8], int n) {
+  // (r = 1); s holds N values per row (invalid = -inf), returns P in place.
+  auto softmax_step = [&](float (*s)[4], auto Nc) {
+    constexpr int N = decltype(Nc)::value;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float mx = -INFINITY;
-      for (int e = 0; e < n; ++e) mx = fmaxf(mx, s[r][e]);
+      float mx = s[r][0];
+#pragma unroll
+      for (int e = 1; e < N; ++e) mx = fmaxf(mx, s[r][e]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float mn = fmaxf(m[r], mx);
       if (mn == -INFINITY) {  // no key for this row yet
-        for (int e = 0; e < n; ++e) s[r][e] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) s[r][e] = 0.0f;
         continue;
       }
-      const float corr = exp2f(m[r] - mn);
-      m[r] = mn;
-      l[r] *= corr;
+      if (mn > m[r]) {  // rescale only when the running maximum moves
+        const float corr = ex2(m[r] - mn);
+        m[r] = mn;
+        l[r] *= corr;
 #pragma unroll
-      for (int nd = 0; nd < 8; ++nd) {
-        o[nd][2 * r] *= corr;
-        o[nd][2 * r + 1] *= corr;
+        for (int nd = 0; nd < 8; ++nd) {
+          o[nd][2 * r] *= corr;
+          o[nd][2 * r + 1] *= corr;
+        }
       }
-      for (int e = 0; e < n; ++e) {
-        const float pe = exp2f(s[r][e] - mn);  // exp2(-inf) = 0
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float pe = ex2(s[r][e] - mn);  // ex2(-inf) = 0
         s[r][e] = pe;
         l[r] += pe;
       }
@@ -111,78 +117,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a,
   int nr = 0;
   while (nr < P.n && P.c[nr] <= imax) ++nr;
   const int NG = nwc + (nr + 1) / 2;
+  const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
-#pragma unroll
-  for (int st = 0; st < kTcStages - 1; ++st) {
-    if (st < NG)
-      tc_load_group(Kb, Vb, P, T, i0, nwc, nr, st, sbase + st * kTcStageB,
-                    sbase + st * kTcStageB + kTcRegion * kTcRowB);
-    cp_async_commit();
-  }
-  for (int grp = 0; grp < NG; ++grp) {
-    cp_async_wait<kTcStages - 2>();
-    __syncthreads();
-    {
-      const int gn = grp + kTcStages - 1;
-      if (gn < NG) {
-        const uint32_t st = sbase + (gn % kTcStages) * kTcStageB;
-        tc_load_group(Kb, Vb, P, T, i0, nwc, nr, gn, st, st + kTcRegion * kTcRowB);
-      }
-      cp_async_commit();
-    }
-    const uint32_t kst = sbase + (grp % kTcStages) * kTcStageB;
-    const uint32_t vst = kst + kTcRegion * kTcRowB;
+  const bool ok = tc_pipeline(&mk, &mv, P, bg, i0, nwc, nr, NG, sbase, bars, a.status,
+                              [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t pa[4];
     if (grp < nwc) {
-      // window chunk: key columns n = 0..15 <-> key i0w + 3 - s_lo - 15 + n = smem row 4w + n
+      // window chunk: key column n = 0..15 <-> key i0w + 3 - s_lo - 15 + n = row 4w + n
       const int s_lo = kTcWC * grp, s_hi = min(s_lo + kTcWC - 1, P.W);
-      float s[2][8];
       float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-        qk_tile(qa, kst + (4 * warp + 8 * nt + (lane & 7)) * kTcRowB, acc[nt]);
-      const int kb = i0w + 3 - s_lo - 15;
+      qk_tile(qa, kst, 4 * warp + (lane & 7), acc[0]);
+      qk_tile(qa, kst, 4 * warp + 8 + (lane & 7), acc[1]);
+      // distance of column n for this lane's rows: p + 12 + s_lo - n
+      float s[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int n = 8 * nt + 2 * tig + (e & 1);
-          const int dist = i - (kb + n);
-          const bool ok = dist >= s_lo && dist <= s_hi && dist <= i;
-          s[e >> 1][2 * nt + (e & 1)] = ok ? acc[nt][e] : -INFINITY;
+          const int dist = p + 12 + s_lo - (8 * nt + 2 * tig + (e & 1));
+          const bool v = dist >= s_lo && dist <= s_hi && dist <= i;
+          s[e >> 1][2 * nt + (e & 1)] = v ? acc[nt][e] : -INFINITY;
         }
-      softmax_step(s, 4);
+      softmax_step(s, std::integral_constant<int, 4>());
       pa[0] = pack_bf16(s[0][0], s[0][1]);
       pa[1] = pack_bf16(s[1][0], s[1][1]);
       pa[2] = pack_bf16(s[0][2], s[0][3]);
       pa[3] = pack_bf16(s[1][2], s[1][3]);
-      pv_tile(pa, vst + (4 * warp + (lane & 7)) * kTcRowB, vst + (4 * warp + 8 + (lane & 7)) * kTcRowB, o);
+      pv_tile(pa, vst, 4 * warp + (lane & 7), 4 * warp + 8 + (lane & 7), o);
     } else {
-      // rung pair: B column n = 2 p' + e' is row p' + e' of the warp's slab
+      // rung pair: box x, B column n = 2 p' + e' is row 4w + p' + e'
       const int r0 = 2 * (grp - nwc);
-      const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
-      float s[2][8];
+      float s[2][4];
       float wgt[2];
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         const int rg = r0 + x;
         float acc[4] = {0, 0, 0, 0};
-        qk_tile(qa, kst + (x * (kTcTQ + 1) + colrow) * kTcRowB, acc);
-        const bool ok = rg < nr && p == tig && i >= P.c[rg];
+        qk_tile(qa, kst, x * kTcBoxRows + colrow, acc);
+        const bool v = rg < nr && p == tig && i >= P.c[rg];
         const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
         wgt[x] = w;
-        s[0][x] = ok ? fmaf(w, acc[1], (1.0f - w) * acc[0]) : -INFINITY;
-        s[1][x] = ok ? fmaf(w, acc[3], (1.0f - w) * acc[2]) : -INFINITY;
+        s[0][x] = v ? fmaf(w, acc[1], (1.0f - w) * acc[0]) : -INFINITY;
+        s[1][x] = v ? fmaf(w, acc[3], (1.0f - w) * acc[2]) : -INFINITY;
       }
-      softmax_step(s, 2);
+      softmax_step(s, std::integral_constant<int, 2>());
       pa[0] = pack_bf16(s[0][0] * (1.0f - wgt[0]), s[0][0] * wgt[0]);
       pa[1] = pack_bf16(s[1][0] * (1.0f - wgt[0]), s[1][0] * wgt[0]);
       pa[2] = pack_bf16(s[0][1] * (1.0f - wgt[1]), s[0][1] * wgt[1]);
       pa[3] = pack_bf16(s[1][1] * (1.0f - wgt[1]), s[1][1] * wgt[1]);
-      pv_tile(pa, vst + colrow * kTcRowB, vst + (kTcTQ + 1 + colrow) * kTcRowB, o);
+      pv_tile(pa, vst, colrow, kTcBoxRows + colrow, o);
     }
-  }
-  cp_async_wait<0>();
+  });
+  if (!ok) return;
 
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -206,13 +192,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) fwd_tc_kernel(const AttnArgs a,
 
 int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
+  CUtensorMap mk, mv;
+  const int64_t planes = (int64_t)a.B * a.Hkv;
+  if (make_rows_map(&mk, kr, planes, a.T, kTcBoxRows, 1) != SFA_OK ||
+      make_rows_map(&mv, a.v, planes, a.T, kTcBoxRows, 1) != SFA_OK)
+    return SFA_ERR_CUDA;
   auto kern = p.interp ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
       cudaSuccess)
     return SFA_ERR_CUDA;
   dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
   LaunchTimer tm(SFA_KERNEL_FWD, stream);
-  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, static_cast<const bf16*>(kr), p);
+  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
