@@ -48,7 +48,7 @@ __device__ __forceinline__ void quad_row_dots(const bf16* x0, const bf16* x1, co
 }
 
 template <bool INTERP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, bf16* qt, float2* coef, int NS,
                     const __grid_constant__ Plan P) {
@@ -216,10 +216,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 constexpr int kKvTK = 32;                     // key rows per CTA (4 warps x 8)
 constexpr int kKvThreads = 128;
-constexpr int kKvQ = kKvTK + 8;               // queries staged per group
+// Queries staged per group: 40 are read; 42 rows per head plane make the
+// plane stride 2 (mod 8) rows, so the 128B swizzle puts the 8 (query, head)
+// rows of one ldmatrix tile on distinct banks.
+constexpr int kKvQ = kKvTK + 10;
 constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
-constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][40 queries][128 B]
-constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // (P, dS) box: [40 queries][9 slots][4 heads]
+constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][42 queries][128 B]
+constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // (P, dS) box: [42 queries][9 slots][4 heads]
 constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
 constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
