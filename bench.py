@@ -41,11 +41,21 @@ ROPE = 1e4
 SEED = 0
 # unique bytes per token per layer, bf16: Q, O, dO, dQ (Hq heads) + K, V, dK, dV (Hkv heads)
 UNIQUE_BYTES_PER_TOKEN = 2 * D * (4 * HQ + 4 * HKV)
-# FP32 SIMT peak: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2.070 GHz max SM clock
-ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+# algorithmic bytes per token of each kernel (bf16, 8/2 heads): the method's
+# tensors it must read or write once
+KERNEL_BYTES_PER_TOKEN = {"fwd": 2 * D * (2 * HQ + 2 * HKV),   # Q, O, K, V
+                          "bwd_q": 2 * D * (4 * HQ + 2 * HKV),  # Q, O, dO, dQ, K, V
+                          "bwd_kv": 2 * D * (2 * HQ + 2 * HKV)}  # Q, dO, dK, dV
 # algorithmic flop per (query head, key) pair, per kernel; D = 64
-FLOP_PER_PAIR = {"fwd": 4 * D, "bwd_q": 6 * D, "bwd_kv": 8 * D}
-FLOP_PER_RUNG_PAIR_DALPHA = 4 * D  # bwd_kv: q.(k0 - k1) and dO.(v0 - v1)
+FLOP_PER_PAIR = {"fwd": 4 * D, "bwd_q": 6 * D, "bwd_kv": 4 * D}
+FLOP_PER_RUNG_PAIR_DALPHA = 4 * D  # q.(k0 - k1) and dO.(v0 - v1)
+
+
+def hbm_peak():
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        return json.load(open(pk))["hbm_gbs"], "MEASURED_PEAKS.json hbm_gbs (of measured)"
+    return 6800.0, "fallback 6.8 TB/s (of fallback)"
 
 
 SCHED_L = 16  # the schedules are defined over the 16-layer stack
@@ -139,6 +149,25 @@ class Clocks:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+def rank_seed(rank: int) -> int:
+    """Input seed of a rank: every rank draws its own batch (weak scaling)."""
+    import sfa_inputs as si
+
+    return si.mix_seed(SEED, 1000 + rank)
+
+
+def allreduce_dtheta(dadt_per_layer, out):
+    """Sum the per-layer dL/dtheta over ranks (data-parallel theta): gathers
+    element 1 of each layer's (dalpha, dtheta) pair into `out` and all-reduces
+    it.  The only collective of the benchmark."""
+    import torch.distributed as dist
+
+    for l, d in enumerate(dadt_per_layer):
+        out[l] = d[1]
+    dist.all_reduce(out)
+    return out
+
+
 def kernel_traffic(kind: str):
     """Per-launch DRAM bytes of `kind` from the committed ncu summary, or None
     when there is none or the kernel source changed since it was captured."""
@@ -207,7 +236,7 @@ def gpu_arm(args, rank, world, dev):
     al = alphas(args.schedule)
     layers = []
     for l in layer_ids():
-        x = si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", si.mix_seed(SEED, 1000 + rank), dev, layer=l)
+        x = si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", rank_seed(rank), dev, layer=l)
         layers.append(Layer(sfa, lib, x, al[l], args.W, dev))
     stream = torch.cuda.current_stream()
     sp = C.c_void_p(stream.cuda_stream)
@@ -217,9 +246,7 @@ def gpu_arm(args, rank, world, dev):
         for L in layers:
             L.run(sp)
         if world > 1:
-            for l, L in enumerate(layers):
-                dtheta[l] = L.dadt[1]
-            dist.all_reduce(dtheta)
+            allreduce_dtheta([L.dadt for L in layers], dtheta)
 
     def barrier():
         if world > 1:
@@ -253,24 +280,24 @@ def gpu_arm(args, rank, world, dev):
         ms = float(t.item())
     launches = int(sum(c for _, c in kt.values()))
 
-    # roofline of the dominant kernel (largest summed device time)
+    # roofline of the dominant kernel (largest summed device time), HBM view:
+    # algorithmic bytes per launch / mean launch time vs the measured copy peak
     dom = max(("fwd", "bwd_q", "bwd_kv"), key=lambda k: kt[k][0])
+    per_launch_ms = kt[dom][0] / max(1, kt[dom][1])
+    bytes_per_launch = KERNEL_BYTES_PER_TOKEN[dom] * B * T
+    achieved = bytes_per_launch / (per_launch_ms * 1e-3) / 1e9
+    peak, src = hbm_peak()
     flops = 0.0
     for L in layers:
         pairs, rung_pairs = pair_counts(L.alpha, args.W)
-        f = pairs * FLOP_PER_PAIR[dom]
-        if dom == "bwd_kv":
-            f += rung_pairs * FLOP_PER_RUNG_PAIR_DALPHA
+        f = pairs * FLOP_PER_PAIR[dom] + (rung_pairs * FLOP_PER_RUNG_PAIR_DALPHA if dom == "bwd_q" else 0)
         flops += f * B * HQ
-    per_launch_ms = kt[dom][0] / max(1, kt[dom][1])
-    flops_per_launch = flops / LAYERS
-    achieved = flops_per_launch / (per_launch_ms * 1e-3) / 1e12
-    traffic = kernel_traffic(dom)
-    roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 3),
-                "peak": round(ALU_PEAK_TFLOPS, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / ALU_PEAK_TFLOPS, 4), "traffic": traffic,
-                "peak_source": "FP32 SIMT: 152 SM x 128 lanes x 2 x 2.070 GHz",
+    useful_tflops = flops / len(layers) / (per_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": kernel_traffic(dom),
+                "peak_source": src, "algorithmic_bytes_per_launch": bytes_per_launch,
                 "per_launch_ms": round(per_launch_ms, 4),
+                "useful_tflops": round(useful_tflops, 2),
                 "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kt.items() if v[1]}}
     return layers, ms, clk, launches, roofline
 
@@ -322,7 +349,7 @@ def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
     import sfa_inputs as si
 
     a = alphas(schedule)[layer]
-    x = si.make_qkvdo(nb, T, HQ, HKV, D, "bf16", si.mix_seed(SEED, 1000), layer=layer)
+    x = si.make_qkvdo(nb, T, HQ, HKV, D, "bf16", rank_seed(0), layer=layer)
     slots = o.interp_slots(FIB, a, W)
     t0 = time.perf_counter()
     o.forward(x["q"], x["k"], x["v"], slots, ROPE)
@@ -412,19 +439,15 @@ def main():
     layers, ms, clk, launches, roofline = gpu_arm(args, rank, world, dev)
     value = world * B * T / (ms * 1e-3)
     hbm = UNIQUE_BYTES_PER_TOKEN * B * T * LAYERS / (ms * 1e-3) / 1e9
-    peak = None
-    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk):
-        peak = json.load(open(pk)).get("hbm_gbs")
+    peak, peak_src = hbm_peak()
     out = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic: seeded N(0,1) Q, K, V, dO per layer", "config": config(args),
            "roofline": roofline,
            "hbm": {"unique_bytes_per_token_layer": UNIQUE_BYTES_PER_TOKEN,
-                   "achieved_gbs": round(hbm, 1), "peak_gbs": peak,
-                   "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if peak else "fallback 6800",
-                   "frac": round(hbm / (peak or 6800.0), 4)},
+                   "achieved_gbs": round(hbm, 1), "peak_gbs": peak, "peak_source": peak_src,
+                   "frac": round(hbm / peak, 4)},
            "gpu_launches": launches, "clocks": clk}
     if not args.no_e2e:
         out["e2e"] = e2e_arm(layers, min(args.steps, 5), world, dev)
