@@ -166,6 +166,24 @@ int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void
                      const void* o, const float* lse, const void* dO, void* dq, void* dk,
                      void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of sfa_forward (no counterpart on the pages; it
+ * exists for callers that cannot allocate device memory: programs whose
+ * allocator owns all device memory and bars raw cudaMalloc from libraries,
+ * or that run under a hard memory budget).  Same arguments and results as
+ * sfa_forward without ws / ws_bytes: the scratch lives in a file-scope device
+ * array of SFA_STATIC_WS_BYTES that every GPU loading the library keeps until
+ * the process exits.  Calls whose sfa_workspace_size(d, 1, 0) exceeds that
+ * return SFA_ERR_CAPACITY and launch nothing (B * Hkv * T <= 65536 rows with
+ * RoPE, e.g. B = 32, Hkv = 2, T = 1024).  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, that device current);
+ * make it before any stream capture.  Nothing is allocated or freed.  All
+ * calls share the one array: calls that overlap on the GPU (other streams,
+ * other threads) race on it; serialize them.  The array needs no clearing
+ * (each call writes the scratch rows it reads). */
+#define SFA_STATIC_WS_BYTES (8u << 20)
+int sfa_forward_noalloc(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* stream);
+
 /* Per-kernel timing for measurement tools.  While enabled, every kernel the
  * library launches is bracketed by two CUDA events recorded on its own
  * stream.  sfa_timing_read waits for the recorded events, writes for each

@@ -19,7 +19,8 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsfa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["sfa_host.cpp", "sfa_api.cu", "sfa_fwd.cu", "sfa_bwd.cu", "sfa_fwd_tc.cu", "sfa_bwd_tc.cu"]
+SOURCES = ["sfa_host.cpp", "sfa_api.cu", "sfa_fwd.cu", "sfa_bwd.cu", "sfa_fwd_tc.cu", "sfa_bwd_tc.cu",
+           "sfa_noalloc.cu"]
 
 
 def _nvcc() -> str:
