@@ -48,7 +48,7 @@ int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int N
   const cuuint64_t strides[3] = {32, (cuuint64_t)NS * 32, (cuuint64_t)T * NS * 32};
   const cuuint32_t box[4] = {8, (cuuint32_t)box_slots, (cuuint32_t)box_q, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
              ? SFA_OK

@@ -9,7 +9,8 @@
 //   dQ = R(-phi) dQ / 8.  dL/dd_k = dS (q~.K'[i-c] - q~.K'[i-c+1])
 //   + P (dO.V[i-c] - dO.V[i-c+1]) comes from the same raw fragments.  For
 //   the key side it writes q~ = q'/8 (bf16) and, per (query, slot, head),
-//   the pair (P, dS) in fp32.
+//   the pair (P, dS) as a key-side-ready record (bf16 hi + lo; a rung gets
+//   one record per role: weight 1 - w for key i - c, w for key i - c + 1).
 // bwd_kv_tc (per key tile): dK^T and dV^T accumulate as [64 dims x 8 keys]
 //   mma tiles per warp: A = q~^T or dO^T of the (query, head) pairs that
 //   (staged by TMA)
@@ -47,10 +48,27 @@ __device__ __forceinline__ void quad_row_dots(const bf16* x0, const bf16* x1, co
   }
 }
 
+// One 32-byte record of key-side coefficients for a (query, slot): the four
+// heads' wt * dS and wt * P, each as bf16 hi + lo (hi = bf16(x),
+// lo = bf16(x - hi)).  Words: dS hi (h0,h1) (h2,h3), dS lo .., P hi .., P lo ..
+__device__ __forceinline__ void write_coef(uint4* dst, float wt, const float* ds4, const float* p4) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const float* src = x < 2 ? ds4 : p4;
+    const float a = wt * src[2 * (x & 1)], b = wt * src[2 * (x & 1) + 1];
+    hi[x] = pack_bf16(a, b);
+    const float2 h = unpack_bf16(hi[x]);
+    lo[x] = pack_bf16(a - h.x, b - h.y);
+  }
+  dst[0] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+  dst[1] = make_uint4(hi[2], hi[3], lo[2], lo[3]);
+}
+
 template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 2)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
-                    const __grid_constant__ CUtensorMap mv, bf16* qt, float2* coef, int NS,
+                    const __grid_constant__ CUtensorMap mv, bf16* qt, uint4* coef, int NS,
                     const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bars[kTcStages];
@@ -94,8 +112,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
   float dacc = 0.0f;
-  float2* crow = coef + ((int64_t)bg * T + ic) * NS * 4;  // [slot][head] (P, dS) of query i
-  const int hlA = gid >> 2, hlB = hlA + 2;
+  // records of query i: [slot][2 x uint4]; lanes with gid < 4 hold heads 0, 2
+  // and receive heads 1, 3 from lane ^ 16 (same position and columns)
+  uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2;
+  const bool writer = gid < 4;
 
   const int wmax = min(P.W, imax);
   const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
@@ -116,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         qk_tile(qa, kst, row, sc[nt]);
         qk_tile(da, vst, row, dp[nt]);
       }
-      float ds[2][4];
+      float ds[2][4], pp[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -125,10 +145,22 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const int dist = p + 12 + s_lo - (8 * nt + 2 * tig + (e & 1));
           const bool v = act && dist >= s_lo && dist <= s_hi && dist <= i;
           const float pr = v ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[r])) : 0.0f;
-          const float d = pr * (dp[nt][e] - delta[r]);
-          ds[r][2 * nt + (e & 1)] = d;
-          if (v) crow[dist * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
+          ds[r][2 * nt + (e & 1)] = pr * (dp[nt][e] - delta[r]);
+          pp[r][2 * nt + (e & 1)] = pr;
         }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const float o_ds0 = __shfl_xor_sync(0xffffffffu, ds[0][cc], 16);
+        const float o_ds1 = __shfl_xor_sync(0xffffffffu, ds[1][cc], 16);
+        const float o_p0 = __shfl_xor_sync(0xffffffffu, pp[0][cc], 16);
+        const float o_p1 = __shfl_xor_sync(0xffffffffu, pp[1][cc], 16);
+        const int dist = p + 12 + s_lo - (8 * (cc >> 1) + 2 * tig + (cc & 1));
+        if (writer && act && dist >= s_lo && dist <= s_hi && dist <= i) {
+          const float d4[4] = {ds[0][cc], o_ds0, ds[1][cc], o_ds1};
+          const float p4[4] = {pp[0][cc], o_p0, pp[1][cc], o_p1};
+          write_coef(crow + 2 * dist, 1.0f, d4, p4);
+        }
+      }
       sa[0] = pack_bf16(ds[0][0], ds[0][1]);
       sa[1] = pack_bf16(ds[1][0], ds[1][1]);
       sa[2] = pack_bf16(ds[0][2], ds[0][3]);
@@ -148,6 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
         const float f = (INTERP && rg < nr) ? P.f[rg] : 0.0f;
         wgt[x] = w;
+        float prr[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float s = fmaf(w, sc[2 * r + 1], (1.0f - w) * sc[2 * r]);
@@ -155,11 +188,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           const float pr = v ? ex2(fmaf(s, kLog2e, -lse2[r])) : 0.0f;
           const float d = pr * (dpi - delta[r]);
           ds[r][x] = d;
-          if (v) {
-            crow[(P.W + 1 + rg) * 4 + (r ? hlB : hlA)] = make_float2(pr, d);
-            if (INTERP)
-              dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
-          }
+          prr[r] = pr;
+          if (INTERP && v)
+            dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
+        }
+        const float o_d0 = __shfl_xor_sync(0xffffffffu, ds[0][x], 16);
+        const float o_d1 = __shfl_xor_sync(0xffffffffu, ds[1][x], 16);
+        const float o_p0 = __shfl_xor_sync(0xffffffffu, prr[0], 16);
+        const float o_p1 = __shfl_xor_sync(0xffffffffu, prr[1], 16);
+        if (writer && v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
+          const float d4[4] = {ds[0][x], o_d0, ds[1][x], o_d1};
+          const float p4[4] = {prr[0], o_p0, prr[1], o_p1};
+          write_coef(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, d4, p4);
+          write_coef(crow + 2 * (P.W + 2 + 2 * rg), w, d4, p4);
         }
       }
       sa[0] = pack_bf16(ds[0][0] * (1.0f - wgt[0]), ds[0][0] * wgt[0]);
@@ -222,7 +263,7 @@ constexpr int kKvThreads = 128;
 constexpr int kKvQ = kKvTK + 10;
 constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
 constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][42 queries][128 B]
-constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // (P, dS) box: [42 queries][9 slots][4 heads]
+constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // records box: [42 queries][9 slots][32 B]
 constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
 constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
@@ -259,13 +300,13 @@ __global__ void __launch_bounds__(kKvThreads)
   auto issue = [&](int grp, uint32_t st, uint32_t bar) {
     const bool win = grp < nwc;
     const int qb = qb_of(grp);
-    mbar_expect_tx(bar, 2 * kKvPlaneB + (win ? kKvCoefB : kKvQ * 32));
+    mbar_expect_tx(bar, 2 * kKvPlaneB + (win ? kKvCoefB : kKvQ * 2 * 32));
     tma_load_3d(st, &mq, 0, qb, hplane, bar);
     tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
     if (win)
       tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, bg, bar);
     else
-      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + (grp - nwc), qb, bg, bar);
+      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, bg, bar);
   };
 
   if (tid == 0) {
@@ -288,50 +329,42 @@ __global__ void __launch_bounds__(kKvThreads)
     }
     const uint32_t qst = sbase + st * kKvStageB;
     const uint32_t dst = qst + kKvPlaneB;
-    const float* csm = reinterpret_cast<const float*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
+    const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
     const bool win = grp < nwc;
     const int rg = grp - nwc;
     const int s_lo = kKvWC * grp, s_hi = min(s_lo + kKvWC - 1, P.W);
     const int c = win ? 0 : P.c[rg];
-    const float w = (!win && INTERP) ? P.w[rg] : 0.0f;
-    const int nsl = win ? kKvWC : 1;      // slots per staged query
+    const int nsl = win ? kKvWC : 2;      // records per staged query
     const int qb = qb_of(grp);            // first staged query (slab row 0)
     const int qw = qb + 8 * warp;         // query of k index 0 of this warp
     const int nks = win ? 4 : 3;
     for (int ks = 0; ks < nks; ++ks) {
-      // B: (dS, P) of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) for key j,
-      // as bf16 hi + lo pairs (hi = bf16(x), lo = bf16(x - hi))
+      // B: the records of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
+      // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
+      // (q - j = c - 1); words (tig & 1) + {0, 2, 4, 6} = dS hi, dS lo, P hi,
+      // P lo of heads 2 (tig & 1) and 2 (tig & 1) + 1
       uint32_t bk[2], bvv[2], bkl[2], bvl[2];
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         const int ql = 4 * ks + 2 * hb + (tig >> 1);  // query offset from qw
         const int qi = qw + ql;
-        float wt = 0.0f;
-        int sl = 0;
+        int sl = -1;
         if (win) {
           const int s = qi - j;
-          if (s >= s_lo && s <= s_hi) {
-            wt = 1.0f;
-            sl = s - s_lo;
-          }
+          if (s >= s_lo && s <= s_hi) sl = s - s_lo;
+        } else if (qi >= c) {
+          if (qi - j == c) sl = 0;
+          else if (qi - j == c - 1) sl = 1;
+        }
+        if (sl >= 0 && qi < T && j < T) {
+          const uint32_t* rec = csm + ((8 * warp + ql) * nsl + sl) * 8 + (tig & 1);
+          bk[hb] = rec[0];
+          bkl[hb] = rec[2];
+          bvv[hb] = rec[4];
+          bvl[hb] = rec[6];
         } else {
-          if (qi - j == c) wt = 1.0f - w;
-          else if (qi - j == c - 1) wt = w;
-          if (qi < c) wt = 0.0f;
+          bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
         }
-        float pk[2] = {0.0f, 0.0f}, dsk[2] = {0.0f, 0.0f};
-        if (wt != 0.0f && qi < T && j < T) {
-          const float4 cv = *reinterpret_cast<const float4*>(csm + ((8 * warp + ql) * nsl + sl) * 8 + 4 * (tig & 1));
-          pk[0] = wt * cv.x;  // (P, dS) of heads h, h + 1
-          dsk[0] = wt * cv.y;
-          pk[1] = wt * cv.z;
-          dsk[1] = wt * cv.w;
-        }
-        bk[hb] = pack_bf16(dsk[0], dsk[1]);
-        bvv[hb] = pack_bf16(pk[0], pk[1]);
-        const float2 kh = unpack_bf16(bk[hb]), vh = unpack_bf16(bvv[hb]);
-        bkl[hb] = pack_bf16(dsk[0] - kh.x, dsk[1] - kh.y);
-        bvl[hb] = pack_bf16(pk[0] - vh.x, pk[1] - vh.y);
       }
       // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
       // k index kx = 4 (query offset) + head lives in slab row head * 40 + query
@@ -413,15 +446,15 @@ size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off
   *off_qt = o;
   o += align256((size_t)d->B * d->Hq * d->T * kD * 2);
   *off_coef = o;
-  const size_t NS = (size_t)p.W + 1 + p.n;
-  o += align256((size_t)d->B * d->Hkv * d->T * NS * 4 * sizeof(float2));
+  const size_t NS = (size_t)p.W + 1 + 2 * p.n;  // records per query: window slots, 2 per rung
+  o += align256((size_t)d->B * d->Hkv * d->T * NS * 32);
   return o;
 }
 
 int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* qt, void* coef,
                        void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  const int NS = p.W + 1 + p.n;
+  const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
   CUtensorMap mk, mv, mq, md, mcw, mcr;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
@@ -429,7 +462,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_coef_map(&mcw, coef, kvplanes, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
-      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 1, kKvQ) != SFA_OK)
+      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 2, kKvQ) != SFA_OK)
     return SFA_ERR_CUDA;
   auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
   auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
@@ -442,7 +475,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
     kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, static_cast<bf16*>(qt),
-                                          static_cast<float2*>(coef), NS, p);
+                                          static_cast<uint4*>(coef), NS, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {

@@ -163,8 +163,8 @@ __device__ __forceinline__ bool tc_pipeline(const CUtensorMap* mk, const CUtenso
 // Host: tensor map over [B*H, T, 64] bf16 rows with a (64, box_rows, box_h)
 // box and 128B swizzle (sfa_api.cu).
 int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h);
-// Host: tensor map over the (P, dS) terms [B*Hkv, T, NS, 8 floats], box
-// (8, box_slots, box_q, 1), no swizzle.
+// Host: tensor map over the key-side coefficient records [B*Hkv, T, NS, 8
+// words], box (8, box_slots, box_q, 1), no swizzle.
 int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int box_slots,
                   int box_q);
 
