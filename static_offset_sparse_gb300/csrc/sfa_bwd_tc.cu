@@ -69,7 +69,7 @@ template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 2)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, bf16* qt, uint4* coef, int NS,
-                    const __grid_constant__ Plan P) {
+                    unsigned* ticket, const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bars[kTcStages];
   __shared__ double red[kTcWarps];
@@ -212,16 +212,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   });
   if (!ok) return;
 
-  if (INTERP) {  // per-CTA partial of dL/dalpha (fixed-order reduction)
+  if (INTERP && a.dalpha_out) {
+    // per-CTA partial of dL/dalpha; the last CTA to finish sums all partials
+    // in a fixed order (deterministic) and writes dL/dalpha and dL/dtheta
+    __shared__ bool last;
     double d = (double)dacc;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_down_sync(0xffffffffu, d, off);
     if (lane == 0) red[warp] = d;
     __syncthreads();
+    const unsigned nblk = gridDim.x * gridDim.y;
     if (threadIdx.x == 0) {
       double s = 0.0;
       for (int x = 0; x < kTcWarps; ++x) s += red[x];
       a.dalpha_part[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = s;
+      __threadfence();
+      last = atomicAdd(ticket, 1u) == nblk - 1;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      const volatile double* part = a.dalpha_part;
+      double s = 0.0;
+      for (unsigned x = threadIdx.x; x < nblk; x += kTcThreads) s += part[x];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xffffffffu, s, off);
+      if (lane == 0) red[warp] = s;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int x = 0; x < kTcWarps; ++x) t += red[x];
+        a.dalpha_out[0] = t;
+        a.dalpha_out[1] = t * (a.alpha - 0.5) * (1.5 - a.alpha);
+      }
     }
   }
   if (!act) return;
@@ -255,8 +278,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
 }
 
-constexpr int kKvTK = 32;                     // key rows per CTA (4 warps x 8)
-constexpr int kKvThreads = 128;
+constexpr int kKvTK = 32;                     // key rows per CTA
+constexpr int kKvThreads = 256;               // 8 warps: 4 key groups of 8 rows x 2 dim halves
 // Queries staged per group: 40 are read; 42 rows per head plane make the
 // plane stride 2 (mod 8) rows, so the 128B swizzle puts the 8 (query, head)
 // rows of one ldmatrix tile on distinct banks.
@@ -268,8 +291,63 @@ constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
 constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 
+// One group's products for a warp: NKS k-steps of 16 (query, head) pairs.
+// dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
+template <int NKS>
+__device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int nsl,
+                                         bool win, int s_lo, int s_hi, int c, int qw, int kw, int j,
+                                         int T, int dh, float (*dk)[4], float (*dv)[4]) {
+  const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
+#pragma unroll
+  for (int ks = 0; ks < NKS; ++ks) {
+    // B: the records of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
+    // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
+    // (q - j = c - 1); words (tig & 1) + {0, 2, 4, 6} = dS hi, dS lo, P hi,
+    // P lo of heads 2 (tig & 1) and 2 (tig & 1) + 1
+    uint32_t bk[2], bvv[2], bkl[2], bvl[2];
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int ql = 4 * ks + 2 * hb + (tig >> 1);  // query offset from qw
+      const int qi = qw + ql;
+      int sl = -1;
+      if (win) {
+        const int s = qi - j;
+        if (s >= s_lo && s <= s_hi) sl = s - s_lo;
+      } else if (qi >= c) {
+        if (qi - j == c) sl = 0;
+        else if (qi - j == c - 1) sl = 1;
+      }
+      if (sl >= 0 && qi < T && j < T) {
+        const uint32_t* rec = csm + ((8 * kw + ql) * nsl + sl) * 8 + (tig & 1);
+        bk[hb] = rec[0];
+        bkl[hb] = rec[2];
+        bvv[hb] = rec[4];
+        bvl[hb] = rec[6];
+      } else {
+        bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
+      }
+    }
+    // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
+    // k index kx = 4 (query offset) + head lives in slab row head * 42 + query
+    const int kx = 8 * (mi >> 1) + (lane & 7);
+    const int arow = (kx & 3) * kKvQ + 8 * kw + 4 * ks + (kx >> 2);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int mt = dh + 2 * x;
+      uint32_t aq[4], ad[4];
+      const uint32_t off = swz(arow, 2 * mt + (mi & 1));
+      ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
+      ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
+      mma_bf16(dk[x], aq, bk[0], bk[1]);
+      mma_bf16(dv[x], ad, bvv[0], bvv[1]);
+      mma_bf16(dk[x], aq, bkl[0], bkl[1]);
+      mma_bf16(dv[x], ad, bvl[0], bvl[1]);
+    }
+  }
+}
+
 template <bool INTERP>
-__global__ void __launch_bounds__(kKvThreads)
+__global__ void __launch_bounds__(kKvThreads, 2)
     bwd_kv_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mcw,
                      const __grid_constant__ CUtensorMap mcr, const __grid_constant__ Plan P) {
@@ -279,16 +357,17 @@ __global__ void __launch_bounds__(kKvThreads)
   unsigned char* sgen = smem_raw + (sbase - smem_u32(smem_raw));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
+  const int kw = warp >> 1, dh = warp & 1;
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int T = a.T;
-  const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * warp;
+  const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * kw;
   const int j = j0w + gid;  // key row of B column gid
   const int hplane = b * a.Hq + g * 4;
 
-  float dk[4][4], dv[4][4];
+  float dk[2][4], dv[2][4];
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt) dk[mt][0] = dk[mt][1] = dk[mt][2] = dk[mt][3] = dv[mt][0] =
-      dv[mt][1] = dv[mt][2] = dv[mt][3] = 0.0f;
+  for (int x = 0; x < 2; ++x) dk[x][0] = dk[x][1] = dk[x][2] = dk[x][3] = dv[x][0] = dv[x][1] =
+      dv[x][2] = dv[x][3] = 0.0f;
 
   const int wmax = min(P.W, T - 1 - j0);
   const int nwc = wmax >= 0 ? wmax / kKvWC + 1 : 0;
@@ -328,119 +407,64 @@ __global__ void __launch_bounds__(kKvThreads)
       return;
     }
     const uint32_t qst = sbase + st * kKvStageB;
-    const uint32_t dst = qst + kKvPlaneB;
     const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
-    const bool win = grp < nwc;
-    const int rg = grp - nwc;
-    const int s_lo = kKvWC * grp, s_hi = min(s_lo + kKvWC - 1, P.W);
-    const int c = win ? 0 : P.c[rg];
-    const int nsl = win ? kKvWC : 2;      // records per staged query
-    const int qb = qb_of(grp);            // first staged query (slab row 0)
-    const int qw = qb + 8 * warp;         // query of k index 0 of this warp
-    const int nks = win ? 4 : 3;
-    for (int ks = 0; ks < nks; ++ks) {
-      // B: the records of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
-      // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
-      // (q - j = c - 1); words (tig & 1) + {0, 2, 4, 6} = dS hi, dS lo, P hi,
-      // P lo of heads 2 (tig & 1) and 2 (tig & 1) + 1
-      uint32_t bk[2], bvv[2], bkl[2], bvl[2];
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int ql = 4 * ks + 2 * hb + (tig >> 1);  // query offset from qw
-        const int qi = qw + ql;
-        int sl = -1;
-        if (win) {
-          const int s = qi - j;
-          if (s >= s_lo && s <= s_hi) sl = s - s_lo;
-        } else if (qi >= c) {
-          if (qi - j == c) sl = 0;
-          else if (qi - j == c - 1) sl = 1;
-        }
-        if (sl >= 0 && qi < T && j < T) {
-          const uint32_t* rec = csm + ((8 * warp + ql) * nsl + sl) * 8 + (tig & 1);
-          bk[hb] = rec[0];
-          bkl[hb] = rec[2];
-          bvv[hb] = rec[4];
-          bvl[hb] = rec[6];
-        } else {
-          bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
-        }
-      }
-      // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
-      // k index kx = 4 (query offset) + head lives in slab row head * 40 + query
-      const int mi = lane >> 3;
-      const int kx = 8 * (mi >> 1) + (lane & 7);
-      const int arow = (kx & 3) * kKvQ + 8 * warp + 4 * ks + (kx >> 2);
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        uint32_t aq[4], ad[4];
-        const uint32_t off = swz(arow, 2 * mt + (mi & 1));
-        ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
-        ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
-        mma_bf16(dk[mt], aq, bk[0], bk[1]);
-        mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
-        mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
-        mma_bf16(dv[mt], ad, bvl[0], bvl[1]);
-      }
+    const int qw = qb_of(grp) + 8 * kw;  // query of k index 0 of this warp
+    if (grp < nwc) {
+      const int s_lo = kKvWC * grp;
+      kv_group<4>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0, qw,
+                  kw, j, T, dh, dk, dv);
+    } else {
+      kv_group<3>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qw, kw, j, T, dh, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && grp + kKvStages < NG) issue(grp + kKvStages, qst, smem_u32(&bars[st]));
   }
 
   // dK = R(-phi) dk' at key positions; transpose through shared memory for
-  // row-contiguous stores.  Lane holds dims 16 mt + gid (+8), keys 2 tig (+1).
+  // row-contiguous stores.  Lane holds dims 16 mt + gid (+8) for mt = dh,
+  // dh + 2, keys 2 tig (+1) of its key group.
   const float2* rope = static_cast<const float2*>(a.rope);
   if (rope) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int jj = min(j0w + 2 * tig + e, T - 1);
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float2 cs = __ldg(rope + (int64_t)jj * 32 + 16 * mt + gid + 8 * hh);
-          const float lo = dk[mt][2 * hh + e], hi = dk[mt + 2][2 * hh + e];
-          dk[mt][2 * hh + e] = lo * cs.x + hi * cs.y;
-          dk[mt + 2][2 * hh + e] = hi * cs.x - lo * cs.y;
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        const float2 cs = __ldg(rope + (int64_t)jj * 32 + 16 * dh + gid + 8 * hh);
+        const float lo = dk[0][2 * hh + e], hi = dk[1][2 * hh + e];
+        dk[0][2 * hh + e] = lo * cs.x + hi * cs.y;
+        dk[1][2 * hh + e] = hi * cs.x - lo * cs.y;
+      }
     }
   }
-  bf16* tk = reinterpret_cast<bf16*>(sgen) + warp * 2 * 8 * 72;  // [2][8 keys][72]
-  bf16* tv = tk + 8 * 72;
+  bf16* tk = reinterpret_cast<bf16*>(sgen);  // [32 keys][72] for dK, then dV
+  bf16* tv = tk + kKvTK * 72;
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
+  for (int x = 0; x < 2; ++x)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int d = 16 * mt + gid + 8 * hh, n = 2 * tig + e;
-        tk[n * 72 + d] = __float2bfloat16_rn(dk[mt][2 * hh + e]);
-        tv[n * 72 + d] = __float2bfloat16_rn(dv[mt][2 * hh + e]);
+        const int d = 16 * (dh + 2 * x) + gid + 8 * hh, n = 8 * kw + 2 * tig + e;
+        tk[n * 72 + d] = __float2bfloat16_rn(dk[x][2 * hh + e]);
+        tv[n * 72 + d] = __float2bfloat16_rn(dv[x][2 * hh + e]);
       }
-  __syncwarp();
+  __syncthreads();
   {
-    const int n = lane >> 2, part = lane & 3;  // key n, 16 dims per lane
-    const int jr = j0w + n;
+    const int n = tid >> 3, ch = tid & 7;  // key row n of the tile, 8 dims per thread
+    const int jr = j0 + n;
     if (jr < T) {
-      const int64_t row = ((int64_t)bg * T + jr) * kD + 16 * part;
-      const uint4* sk = reinterpret_cast<const uint4*>(tk + n * 72 + 16 * part);
-      const uint4* sv = reinterpret_cast<const uint4*>(tv + n * 72 + 16 * part);
-      uint4* okp = reinterpret_cast<uint4*>(static_cast<bf16*>(a.dk) + row);
-      uint4* ovp = reinterpret_cast<uint4*>(static_cast<bf16*>(a.dv) + row);
-      okp[0] = sk[0];
-      okp[1] = sk[1];
-      ovp[0] = sv[0];
-      ovp[1] = sv[1];
+      const int64_t row = ((int64_t)bg * T + jr) * kD + 8 * ch;
+      *reinterpret_cast<uint4*>(static_cast<bf16*>(a.dk) + row) = *reinterpret_cast<const uint4*>(tk + n * 72 + 8 * ch);
+      *reinterpret_cast<uint4*>(static_cast<bf16*>(a.dv) + row) = *reinterpret_cast<const uint4*>(tv + n * 72 + 8 * ch);
     }
   }
 }
 
-int launch_dalpha_reduce(const double* part, int64_t n, double alpha, double* out, void* stream);
-
 size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
                                    size_t* off_coef) {
   const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * d->Hkv;
-  size_t o = align256(nparts * sizeof(double));
+  size_t o = align256(nparts * sizeof(double)) + 256;  // partials, then the ticket counter
   *off_kr = o;
   o += kr_bytes(d);
   *off_qt = o;
@@ -472,20 +496,20 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
           cudaSuccess)
     return SFA_ERR_CUDA;
   dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
+  unsigned* ticket = reinterpret_cast<unsigned*>(
+      reinterpret_cast<char*>(a.dalpha_part) + align256((size_t)gq.x * gq.y * sizeof(double)));
+  if (cudaMemsetAsync(ticket, 0, sizeof(unsigned), s) != cudaSuccess) return SFA_ERR_CUDA;
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
     kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, static_cast<bf16*>(qt),
-                                          static_cast<uint4*>(coef), NS, p);
+                                          static_cast<uint4*>(coef), NS, ticket, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
     kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, mq, md, mcw, mcr, p);
   }
-  if (cudaGetLastError() != cudaSuccess) return SFA_ERR_CUDA;
-  if (p.interp && a.dalpha_out)
-    return launch_dalpha_reduce(a.dalpha_part, (int64_t)gq.x * gq.y, a.alpha, a.dalpha_out, stream);
-  return SFA_OK;
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
 }  // namespace sfa
