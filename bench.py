@@ -113,7 +113,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
@@ -358,18 +358,19 @@ def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
 
 
 def cpu_baseline(schedule: str, W: int, budget_s: float = 10.0):
-    """The oracle as it stands on this host: one layer (layer 7), one
-    sequence at a time until ~budget_s of CPU work; throughput scaled to the
-    16-layer step (tokens / (16 x seconds per layer))."""
+    """The oracle as it stands on this host: one sequence of one layer at a
+    time, cycling through the 16 layers' alphas, until ~budget_s of CPU work;
+    throughput scaled to the 16-layer step (tokens / (16 x seconds per
+    layer-sequence))."""
     spent, n = 0.0, 0
-    while spent < budget_s and n < 32:
-        spent += oracle_step_sample(schedule, W, 1, 7)
+    while spent < budget_s and n < 16 * 32:
+        spent += oracle_step_sample(schedule, W, 1, n % SCHED_L)
         n += 1
-    tok_s = n * T / (spent * LAYERS)
+    tok_s = n * T / (spent * SCHED_L)
     return {"value": round(tok_s, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, layer 7 of 16 (alpha={alphas(schedule)[7]:.4f}), W={W}, "
-                      f"{n} sequence(s) x {T} tokens, fwd+bwd incl. dtheta, single thread; "
-                      f"{spent:.1f} s; scaled to 16 layers"}
+            "sample": f"fp64 numpy oracle, {n} (layer, sequence) units of {T} tokens cycling over the "
+                      f"16 layers' alphas, W={W}, fwd+bwd incl. dtheta, single thread; {spent:.1f} s; "
+                      "scaled to the 16-layer step"}
 
 
 def reference_arm(args):
@@ -403,7 +404,7 @@ def config(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--W", type=int, default=8)
