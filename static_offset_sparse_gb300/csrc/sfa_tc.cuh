@@ -143,20 +143,25 @@ __device__ __forceinline__ bool tc_pipeline(const CUtensorMap* mk, const CUtenso
   for (int grp = 0; grp < NG; ++grp) {
     const int s = grp % kTcStages;
     const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (grp / kTcStages) & 1);
+    // One barrier per group: it makes the timeout decision uniform and, as
+    // every thread has finished group grp - 1, frees that group's stage.
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         record_status(status, SFA_ERR_TIMEOUT);
-        for (int g2 = grp; g2 < NG && g2 < grp + kTcStages; ++g2)  // loads still in flight
+        for (int g2 = grp; g2 < NG && g2 < grp + kTcStages - 1; ++g2)  // loads still in flight
           mbar_wait_bounded(smem_u32(&bars[g2 % kTcStages]), (g2 / kTcStages) & 1);
       }
       return false;
     }
+    if (tid == 0 && grp > 0 && grp - 1 + kTcStages < NG) {
+      const int sp = (grp - 1) % kTcStages;
+      tc_issue_group(mk, mv, P, bg, i0, nwc, nr, grp - 1 + kTcStages, sbase + sp * kTcStageB,
+                     smem_u32(&bars[sp]));
+    }
     const uint32_t kst = sbase + s * kTcStageB;
     compute(grp, kst, kst + kTcRegionB);
-    __syncthreads();
-    if (tid == 0 && grp + kTcStages < NG)
-      tc_issue_group(mk, mv, P, bg, i0, nwc, nr, grp + kTcStages, kst, smem_u32(&bars[s]));
   }
+  __syncthreads();  // the caller may reuse shared memory
   return true;
 }
 
