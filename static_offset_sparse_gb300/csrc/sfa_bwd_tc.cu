@@ -68,10 +68,12 @@ __device__ __forceinline__ void write_coef(uint4* dst, float wt, const float* ds
 template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 2)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
-                    const __grid_constant__ CUtensorMap mv, bf16* qt, uint4* coef, int NS,
-                    unsigned* ticket, const __grid_constant__ Plan P) {
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
+                    const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mqt,
+                    const __grid_constant__ CUtensorMap mdq, uint4* coef, int NS, unsigned* ticket,
+                    const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bars[kTcStages];
+  __shared__ uint64_t bars[kTcStages + 1];
   __shared__ double red[kTcWarps];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -87,27 +89,39 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int64_t rowA = (int64_t)(b * a.Hq + hA) * T + ic, rowB = (int64_t)(b * a.Hq + hB) * T + ic;
   const float2* rope = static_cast<const float2*>(a.rope);
 
+  const int wmax = min(P.W, imax);
+  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
+  int nr = 0;
+  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int NG = nwc + (nr + 1) / 2;
+  const uint32_t qtile = sbase, dotile = sbase + kTcQTileB, stages = sbase + 2 * kTcQTileB;
+  const int qplane = b * a.Hq + g * 4;
+  const CUtensorMap* qmaps[2] = {&mq, &mdo};
+  tc_start(&mk, &mv, qmaps, 2, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+
   uint32_t qa[4][4], da[4][4];
   float delta[2], lse2[2];
   {
-    const bf16* q = static_cast<const bf16*>(a.q);
     const bf16* dO = static_cast<const bf16*>(a.dO);
     const bf16* O = static_cast<const bf16*>(a.o);
-    load_q_frags(q + rowA * kD, q + rowB * kD, rope, ic, 0.125f, qa);
-    load_q_frags(dO + rowA * kD, dO + rowB * kD, nullptr, ic, 1.0f, da);
     quad_row_dots(dO + rowA * kD, dO + rowB * kD, O + rowA * kD, O + rowB * kD, delta);
     lse2[0] = a.lse[rowA] * kLog2e;
     lse2[1] = a.lse[rowB] * kLog2e;
-    if (act) {  // q~ = q'/8 for the key side, from the fragments this lane holds
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        *reinterpret_cast<uint32_t*>(qt + rowA * kD + 16 * kk + 2 * tig) = qa[kk][0];
-        *reinterpret_cast<uint32_t*>(qt + rowB * kD + 16 * kk + 2 * tig) = qa[kk][1];
-        *reinterpret_cast<uint32_t*>(qt + rowA * kD + 16 * kk + 2 * tig + 8) = qa[kk][2];
-        *reinterpret_cast<uint32_t*>(qt + rowB * kD + 16 * kk + 2 * tig + 8) = qa[kk][3];
-      }
-    }
   }
+  if (!tc_wait_qtiles(bars, a.status)) return;
+  tile_frags(qtile, warp, rope, ic, 0.125f, true, qa);
+  tile_frags(dotile, warp, nullptr, ic, 1.0f, false, da);
+  __syncthreads();  // the dO tile is read: it now carries q~ = q'/8 out for the key side
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    st_shared_u32(otile_addr(dotile, warp, gid, 16 * kk + 2 * tig), qa[kk][0]);
+    st_shared_u32(otile_addr(dotile, warp, gid + 8, 16 * kk + 2 * tig), qa[kk][1]);
+    st_shared_u32(otile_addr(dotile, warp, gid, 16 * kk + 2 * tig + 8), qa[kk][2]);
+    st_shared_u32(otile_addr(dotile, warp, gid + 8, 16 * kk + 2 * tig + 8), qa[kk][3]);
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) tc_store_tile(&mqt, dotile, i0, qplane);
   float dq[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
@@ -117,14 +131,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2;
   const bool writer = gid < 4;
 
-  const int wmax = min(P.W, imax);
-  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
-  int nr = 0;
-  while (nr < P.n && P.c[nr] <= imax) ++nr;
-  const int NG = nwc + (nr + 1) / 2;
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
-  const bool ok = tc_pipeline(&mk, &mv, P, bg, i0, nwc, nr, NG, sbase, bars, a.status,
+  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a.status,
                               [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t sa[4];
     if (grp < nwc) {
@@ -247,12 +256,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
     }
   }
-  if (!act) return;
-  // dQ = R(-phi) dq / 8; dims d (tile nd) and d + 32 (tile nd + 4) share a lane
-  bf16* out = static_cast<bf16*>(a.dq);
+  // dQ = R(-phi) dq / 8 (dims d in tile nd and d + 32 in tile nd + 4 share a
+  // lane), out through the Q tile's space and one TMA store
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int64_t row = r ? rowB : rowA;
     float v[8][2];
 #pragma unroll
     for (int nd = 0; nd < 8; ++nd) {
@@ -274,7 +281,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
 #pragma unroll
     for (int nd = 0; nd < 8; ++nd)
-      *reinterpret_cast<uint32_t*>(out + row * kD + 8 * nd + 2 * tig) = pack_bf16(v[nd][0], v[nd][1]);
+      st_shared_u32(otile_addr(qtile, warp, gid + 8 * r, 8 * nd + 2 * tig), pack_bf16(v[nd][0], v[nd][1]));
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc_store_tile(&mdq, qtile, i0, qplane);
+    bulk_wait_read();  // the q~ and dQ tiles have been read
   }
 }
 
@@ -480,9 +493,13 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   cudaStream_t s = (cudaStream_t)stream;
   const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
-  CUtensorMap mk, mv, mq, md, mcw, mcr;
+  CUtensorMap mk, mv, mq, md, mcw, mcr, mq36, mdo36, mqt32, mdq32;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
+      make_rows_map(&mq36, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&mdo36, a.dO, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&mqt32, qt, qplanes, a.T, kTcORows, 4) != SFA_OK ||
+      make_rows_map(&mdq32, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_coef_map(&mcw, coef, kvplanes, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
@@ -490,7 +507,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
     return SFA_ERR_CUDA;
   auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
   auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
-  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
+  if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdQTcSmem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdKvTcSmem) !=
           cudaSuccess)
@@ -501,8 +518,8 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   if (cudaMemsetAsync(ticket, 0, sizeof(unsigned), s) != cudaSuccess) return SFA_ERR_CUDA;
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
-    kq<<<gq, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, static_cast<bf16*>(qt),
-                                          static_cast<uint4*>(coef), NS, ticket, p);
+    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, mq36, mdo36, mqt32, mdq32,
+                                           static_cast<uint4*>(coef), NS, ticket, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {

@@ -50,9 +50,10 @@ int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, in
 template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 2)
     fwd_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
-                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ Plan P) {
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
+                  const __grid_constant__ CUtensorMap mo, const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t bars[kTcStages];
+  __shared__ uint64_t bars[kTcStages + 1];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -64,13 +65,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int hA = g * 4 + (gid >> 2), hB = hA + 2;  // heads of rows gid, gid + 8
   const float2* rope = static_cast<const float2*>(a.rope);
 
+  const int wmax = min(P.W, imax);
+  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
+  int nr = 0;
+  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int NG = nwc + (nr + 1) / 2;
+  const uint32_t qtile = sbase, stages = sbase + kTcQTileB;
+  const int qplane = b * a.Hq + g * 4;
+  const CUtensorMap* qmaps[1] = {&mq};
+  tc_start(&mk, &mv, qmaps, 1, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+  if (!tc_wait_qtiles(bars, a.status)) return;
   uint32_t qa[4][4];
-  {
-    const int ic = min(i, T - 1);
-    const bf16* q = static_cast<const bf16*>(a.q);
-    load_q_frags(q + ((int64_t)(b * a.Hq + hA) * T + ic) * kD, q + ((int64_t)(b * a.Hq + hB) * T + ic) * kD,
-                 rope, ic, 0.125f * kLog2e, qa);
-  }
+  tile_frags(qtile, warp, rope, min(i, T - 1), 0.125f * kLog2e, true, qa);
   float o[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
@@ -112,14 +118,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
   };
 
-  const int wmax = min(P.W, imax);
-  const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
-  int nr = 0;
-  while (nr < P.n && P.c[nr] <= imax) ++nr;
-  const int NG = nwc + (nr + 1) / 2;
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
-  const bool ok = tc_pipeline(&mk, &mv, P, bg, i0, nwc, nr, NG, sbase, bars, a.status,
+  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a.status,
                               [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t pa[4];
     if (grp < nwc) {
@@ -175,27 +176,33 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
   }
-  if (i >= T) return;
-  bf16* out = static_cast<bf16*>(a.out_o);
+  // O = acc / l through an output tile (the Q tile's space) and one TMA store
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int h = r ? hB : hA;
-    const int64_t row = (int64_t)(b * a.Hq + h) * T + i;
     const float inv = 1.0f / l[r];
-    bf16* op = out + row * kD + 2 * tig;
 #pragma unroll
     for (int nd = 0; nd < 8; ++nd)
-      *reinterpret_cast<uint32_t*>(op + 8 * nd) = pack_bf16(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
-    if (tig == 0) a.out_lse[row] = (m[r] + log2f(l[r])) * kLn2;
+      st_shared_u32(otile_addr(qtile, warp, gid + 8 * r, 8 * nd + 2 * tig),
+                    pack_bf16(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv));
+    if (tig == 0 && i < T)
+      a.out_lse[(int64_t)(b * a.Hq + (r ? hB : hA)) * T + i] = (m[r] + log2f(l[r])) * kLn2;
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc_store_tile(&mo, qtile, i0, qplane);
+    bulk_wait_read();
   }
 }
 
 int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  CUtensorMap mk, mv;
-  const int64_t planes = (int64_t)a.B * a.Hkv;
+  CUtensorMap mk, mv, mq, mo;
+  const int64_t planes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
   if (make_rows_map(&mk, kr, planes, a.T, kTcBoxRows, 1) != SFA_OK ||
-      make_rows_map(&mv, a.v, planes, a.T, kTcBoxRows, 1) != SFA_OK)
+      make_rows_map(&mv, a.v, planes, a.T, kTcBoxRows, 1) != SFA_OK ||
+      make_rows_map(&mq, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&mo, a.out_o, qplanes, a.T, kTcORows, 4) != SFA_OK)
     return SFA_ERR_CUDA;
   auto kern = p.interp ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
@@ -203,7 +210,7 @@ int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* st
     return SFA_ERR_CUDA;
   dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
   LaunchTimer tm(SFA_KERNEL_FWD, stream);
-  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, p);
+  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, mq, mo, p);
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 

@@ -25,9 +25,8 @@ constexpr int kTcBoxRows = 40;                // rows per TMA box (5 KB, 1024-by
 constexpr int kTcBoxB = kTcBoxRows * 128;
 constexpr int kTcRegionB = 2 * kTcBoxB;       // K' (or V) part of a stage
 constexpr int kTcStageB = 2 * kTcRegionB;
-constexpr int kTcStages = 5;
+constexpr int kTcStages = 3;
 constexpr int kTcWC = 12;                     // window distances per chunk
-constexpr size_t kFwdTcSmem = (size_t)kTcStages * kTcStageB + 1024;  // + alignment slack
 
 // q' fragments of a warp's 16 rows: rows gid (head gid>>2) and gid+8 (head
 // 2 + (gid>>2)), position i, scaled by `scale`; RoPE pairs (d, d + 32) sit in
@@ -122,24 +121,58 @@ __device__ __forceinline__ void tc_issue_group(const CUtensorMap* mk, const CUte
   tma_load_3d(st + kTcRegionB + kTcBoxB, mv, 0, y1, bg, bar);
 }
 
-// The staged pipeline shared by the forward and the query-side backward:
-// NST stages in flight, one mbarrier each, consumed in order.  compute(grp,
-// kst, vst) runs on every warp.  Returns false (uniformly across the CTA)
-// if a wait timed out; the status word then holds SFA_ERR_TIMEOUT.
-template <typename ComputeFn>
-__device__ __forceinline__ bool tc_pipeline(const CUtensorMap* mk, const CUtensorMap* mv,
-                                            const Plan& P, int bg, int i0, int nwc, int nr, int NG,
-                                            uint32_t sbase, uint64_t* bars, int* status,
-                                            ComputeFn compute) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+// Per-CTA query tiles: Q (and dO) of the tile's 32 positions x 4 heads come in
+// by one TMA box each, [4 heads][36 rows][128 B] (the 36-row plane stride is
+// 4 mod 8, so the 16 rows of a warp's fragments sit on distinct swizzle
+// phases); outputs leave through [4 heads][32 rows][128 B] tiles and one TMA
+// store each (rows past the sequence end are not written).
+constexpr int kTcQRows = 36;
+constexpr int kTcQTileB = 4 * kTcQRows * 128;  // 18432, a 1024-byte multiple
+constexpr int kTcORows = 32;
+// shared memory: [query tiles][stages] from a 1024-aligned base (+ alignment slack)
+constexpr size_t kFwdTcSmem = (size_t)kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
+constexpr size_t kBwdQTcSmem = (size_t)2 * kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
+
+// Barriers: one per stage, then one for the query tiles.  Thread 0 issues
+// the query-tile loads (nq boxes from the maps in qmaps, at coordinates
+// (0, i0, plane)) and the first stages.
+__device__ __forceinline__ void tc_start(const CUtensorMap* mk, const CUtensorMap* mv,
+                                         const CUtensorMap* const* qmaps, int nq, uint32_t qtile,
+                                         int qplane, const Plan& P, int bg, int i0, int nwc, int nr,
+                                         int NG, uint32_t sbase, uint64_t* bars) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s <= kTcStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     mbar_fence_init();
   }
   __syncthreads();
-  if (tid == 0)
+  if (threadIdx.x == 0) {
+    const uint32_t qb = smem_u32(&bars[kTcStages]);
+    mbar_expect_tx(qb, nq * kTcQTileB);
+    for (int x = 0; x < nq; ++x) tma_load_3d(qtile + x * kTcQTileB, qmaps[x], 0, i0, qplane, qb);
     for (int s = 0; s < kTcStages && s < NG; ++s)
       tc_issue_group(mk, mv, P, bg, i0, nwc, nr, s, sbase + s * kTcStageB, smem_u32(&bars[s]));
+  }
+}
+
+// Wait (bounded) for the query tiles; uniform across the CTA.
+__device__ __forceinline__ bool tc_wait_qtiles(uint64_t* bars, int* status) {
+  const bool ok = mbar_wait_bounded(smem_u32(&bars[kTcStages]), 0);
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) record_status(status, SFA_ERR_TIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+// The staged loop shared by the forward and the query-side backward: NST
+// stages in flight, one mbarrier each, consumed in order; compute(grp, kst,
+// vst) runs on every warp.  Returns false (uniformly across the CTA) if a
+// wait timed out; the status word then holds SFA_ERR_TIMEOUT.
+template <typename ComputeFn>
+__device__ __forceinline__ bool tc_run(const CUtensorMap* mk, const CUtensorMap* mv, const Plan& P,
+                                       int bg, int i0, int nwc, int nr, int NG, uint32_t sbase,
+                                       uint64_t* bars, int* status, ComputeFn compute) {
+  const int tid = threadIdx.x;
   for (int grp = 0; grp < NG; ++grp) {
     const int s = grp % kTcStages;
     const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (grp / kTcStages) & 1);
@@ -163,6 +196,69 @@ __device__ __forceinline__ bool tc_pipeline(const CUtensorMap* mk, const CUtenso
   }
   __syncthreads();  // the caller may reuse shared memory
   return true;
+}
+
+// A fragments of a warp's 16 rows (row r = 4 h + p: head h, position 4w + p)
+// for the 4 k-steps, from a query tile; with RoPE at position i (rope !=
+// nullptr) and a scale they are unpacked, rotated, scaled and repacked.
+__device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float2* rope, int i,
+                                           float scale, bool transform, uint32_t (*qa)[4]) {
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+  const int srow = (r >> 2) * kTcQRows + 4 * warp + (r & 3);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    ldsm_x4(tile + swz(srow, 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+  if (!transform) return;
+  float x[2][4][4];  // [row gid / gid + 8][kk][dims 2tig, 2tig+1, 2tig+8, 2tig+9]
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const float2 a0 = unpack_bf16(qa[kk][0]), a1 = unpack_bf16(qa[kk][1]);
+    const float2 a2 = unpack_bf16(qa[kk][2]), a3 = unpack_bf16(qa[kk][3]);
+    x[0][kk][0] = a0.x; x[0][kk][1] = a0.y; x[0][kk][2] = a2.x; x[0][kk][3] = a2.y;
+    x[1][kk][0] = a1.x; x[1][kk][1] = a1.y; x[1][kk][2] = a3.x; x[1][kk][3] = a3.y;
+  }
+  if (rope) {
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig + 8));
+      const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = x[rr][kk][e], hi = x[rr][kk + 2][e];
+          x[rr][kk][e] = lo * cs[e] - hi * sn[e];
+          x[rr][kk + 2][e] = lo * sn[e] + hi * cs[e];
+        }
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    qa[kk][0] = pack_bf16(x[0][kk][0] * scale, x[0][kk][1] * scale);
+    qa[kk][1] = pack_bf16(x[1][kk][0] * scale, x[1][kk][1] * scale);
+    qa[kk][2] = pack_bf16(x[0][kk][2] * scale, x[0][kk][3] * scale);
+    qa[kk][3] = pack_bf16(x[1][kk][2] * scale, x[1][kk][3] * scale);
+  }
+}
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Byte address in an output tile of the bf16 pair (dim d, d + 1) of warp row
+// r (head r >> 2, position 4w + (r & 3)); d even.
+__device__ __forceinline__ uint32_t otile_addr(uint32_t tile, int warp, int r, int d) {
+  const int srow = (r >> 2) * kTcORows + 4 * warp + (r & 3);
+  return tile + swz(srow, d >> 3) + (d & 7) * 2;
+}
+
+// Store an output tile (thread 0; after every thread's fence + a barrier).
+__device__ __forceinline__ void tc_store_tile(const CUtensorMap* map, uint32_t tile, int i0,
+                                              int plane) {
+  tma_store_3d(map, 0, i0, plane, tile);
+  bulk_commit();
 }
 
 // Host: tensor map over [B*H, T, 64] bf16 rows with a (64, box_rows, box_h)
