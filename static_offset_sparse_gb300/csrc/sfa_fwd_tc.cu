@@ -26,24 +26,40 @@
 
 namespace sfa {
 
-// K' = RoPE(K) as bf16 rows (the operand of every key-side product).
-__global__ void rope_prep_kernel(const bf16* __restrict__ k, const float2* __restrict__ rope,
-                                 bf16* __restrict__ kr, int64_t rows, int T) {
+// K' = RoPE(K) as bf16 rows (the operand of every key-side product).  A
+// thread owns one position and one 8-pair chunk of the rotation: it loads
+// that chunk of the cos/sin table once and rotates the position's rows in
+// kPrepPlanes consecutive (batch, KV head) planes.
+constexpr int kPrepPlanes = 8;
+
+__global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__ k,
+                                                        const float2* __restrict__ rope,
+                                                        bf16* __restrict__ kr, int64_t planes, int T) {
   const int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (it >= rows * 4) return;
-  const int64_t row = it >> 2;
-  const int pc = (int)(it & 3);
-  const int pos = (int)(row % T);
-  float lo[8], hi[8];
-  load_pair_chunk(k + row * kD, pc, rope, pos, lo, hi);
-  store8(kr + row * kD + 8 * pc, lo);
-  store8(kr + row * kD + 32 + 8 * pc, hi);
+  if (it >= (int64_t)T * 4) return;
+  const int pos = (int)(it >> 2), pc = (int)(it & 3);
+  float cs[8], sn[8];
+  load_rope8(rope, pos, 8 * pc, cs, sn);
+  const int64_t p0 = (int64_t)blockIdx.y * kPrepPlanes;
+#pragma unroll
+  for (int x = 0; x < kPrepPlanes; ++x) {
+    const int64_t plane = p0 + x;
+    if (plane >= planes) break;
+    const int64_t row = plane * T + pos;
+    float lo[8], hi[8];
+    load8(k + row * kD + 8 * pc, lo);
+    load8(k + row * kD + 32 + 8 * pc, hi);
+    rotate8(lo, hi, cs, sn);
+    store8(kr + row * kD + 8 * pc, lo);
+    store8(kr + row * kD + 32 + 8 * pc, hi);
+  }
 }
 
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream) {
-  const int64_t n = rows * 4;
-  rope_prep_kernel<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
-      static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), rows, T);
+  const int64_t planes = rows / T;
+  dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)((planes + kPrepPlanes - 1) / kPrepPlanes));
+  rope_prep_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), planes, T);
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
