@@ -1,0 +1,64 @@
+"""CPU checks of bench.py's host logic: the algorithmic pair counts behind
+the roofline figures, the schedules, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_pair_counts_match_oracle_key_sets():
+    import bench
+
+    T = bench.T
+    for alpha in (0.5, 0.5 + 5 / 15, 1.0, 1.5):
+        for W in (6, 8, 12):
+            slots = o.interp_slots(bench.FIB, alpha, W)
+            ok = np.zeros((len(slots), T), dtype=bool)
+            for a, sl in enumerate(slots):
+                lo = sl["s"] if sl["kind"] == "win" else sl["c"]
+                ok[a, lo:] = lo < T
+            rung_rows = [a for a, sl in enumerate(slots) if sl["kind"] == "rung"]
+            pairs, rung = bench.pair_counts(alpha, W)
+            assert pairs == ok.sum() and rung == ok[rung_rows].sum()
+
+
+def test_schedules_match_oracle():
+    import bench
+
+    assert bench.alphas("linear") == o.alpha_schedule(16, o.SCHED_LINEAR)
+    assert bench.alphas("coprime") == o.alpha_schedule(16, o.SCHED_COPRIME, 7)
+    assert bench.alphas("fixed") == [1.0] * 16
+
+
+def test_unique_bytes_per_token():
+    """bf16 rows of 64 dims: a query-head tensor is 8 x 128 B per token, a
+    KV-head tensor 2 x 128 B."""
+    import bench
+
+    qh, kvh = 8 * 128, 2 * 128
+    assert bench.UNIQUE_BYTES_PER_TOKEN == 4 * qh + 4 * kvh == 5120  # Q O dO dQ, K V dK dV
+    assert bench.KERNEL_BYTES_PER_TOKEN["fwd"] == 2 * qh + 2 * kvh      # Q, O, K, V
+    assert bench.KERNEL_BYTES_PER_TOKEN["bwd_q"] == 4 * qh + 2 * kvh    # Q, O, dO, dQ, K, V
+    assert bench.KERNEL_BYTES_PER_TOKEN["bwd_kv"] == 2 * qh + 2 * kvh   # Q, dO, dK, dV
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["warmup"] >= 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["seq_len"] == 1024 and d["config"]["global_batch"] == 32
