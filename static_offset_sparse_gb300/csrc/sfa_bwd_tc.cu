@@ -66,7 +66,7 @@ __device__ __forceinline__ void write_coef(uint4* dst, float wt, const float* ds
 }
 
 template <bool INTERP>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 4)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mqt,

@@ -64,7 +64,7 @@ int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, in
 }
 
 template <bool INTERP>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, 4)
     fwd_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mo, const __grid_constant__ Plan P) {

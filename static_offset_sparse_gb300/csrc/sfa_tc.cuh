@@ -3,11 +3,11 @@
 // A warp owns 4 consecutive query positions x the 4 query heads of one KV
 // group = 16 mma rows (row r = 4 h + p).  Keys are raw RoPE-rotated K' rows
 // and raw V rows staged per CTA by TMA as shifted slabs: a stage holds a K'
-// region and a V region of two 40-row boxes each (128-byte rows, 128B
+// region and a V region of two 32-row boxes each (128-byte rows, 128B
 // swizzle, rows outside the sequence zero-filled by the TMA unit).
 //  * window chunk s_lo (12 distances): rows = positions i0 - 12 - s_lo + r,
-//    r < 80; warp w reads rows 4w .. 4w + 15 (16 key columns).
-//  * rung pair: box x holds positions i0 - c_x + r, r < 40; B column
+//    r < 64; warp w reads rows 4w .. 4w + 15 (16 key columns).
+//  * rung pair: box x holds positions i0 - c_x + r, r < 32; B column
 //    n = 2 p + e of warp w is row 4w + p + e of the box, so the lane with
 //    tig = p holds both raw logits (floor and floor-plus-one) of position p.
 #pragma once
@@ -18,14 +18,14 @@
 
 namespace sfa {
 
-constexpr int kTcTQ = 32;                     // query positions per CTA (two CTAs per SM)
-constexpr int kTcWarps = kTcTQ / 4;           // 8 warps
-constexpr int kTcThreads = kTcWarps * 32;     // 256
-constexpr int kTcBoxRows = 40;                // rows per TMA box (5 KB, 1024-byte multiple)
+constexpr int kTcTQ = 16;                     // query positions per CTA (four CTAs per SM)
+constexpr int kTcWarps = kTcTQ / 4;           // 4 warps
+constexpr int kTcThreads = kTcWarps * 32;     // 128
+constexpr int kTcBoxRows = 32;                // rows per TMA box (4 KB, 1024-byte multiple)
 constexpr int kTcBoxB = kTcBoxRows * 128;
 constexpr int kTcRegionB = 2 * kTcBoxB;       // K' (or V) part of a stage
 constexpr int kTcStageB = 2 * kTcRegionB;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 2;
 constexpr int kTcWC = 12;                     // window distances per chunk
 
 // q' fragments of a warp's 16 rows: rows gid (head gid>>2) and gid+8 (head
@@ -121,14 +121,14 @@ __device__ __forceinline__ void tc_issue_group(const CUtensorMap* mk, const CUte
   tma_load_3d(st + kTcRegionB + kTcBoxB, mv, 0, y1, bg, bar);
 }
 
-// Per-CTA query tiles: Q (and dO) of the tile's 32 positions x 4 heads come in
-// by one TMA box each, [4 heads][36 rows][128 B] (the 36-row plane stride is
+// Per-CTA query tiles: Q (and dO) of the tile's 16 positions x 4 heads come in
+// by one TMA box each, [4 heads][20 rows][128 B] (the 20-row plane stride is
 // 4 mod 8, so the 16 rows of a warp's fragments sit on distinct swizzle
-// phases); outputs leave through [4 heads][32 rows][128 B] tiles and one TMA
+// phases); outputs leave through [4 heads][16 rows][128 B] tiles and one TMA
 // store each (rows past the sequence end are not written).
-constexpr int kTcQRows = 36;
-constexpr int kTcQTileB = 4 * kTcQRows * 128;  // 18432, a 1024-byte multiple
-constexpr int kTcORows = 32;
+constexpr int kTcQRows = 20;
+constexpr int kTcQTileB = 4 * kTcQRows * 128;  // 10240, a 1024-byte multiple
+constexpr int kTcORows = 16;
 // shared memory: [query tiles][stages] from a 1024-aligned base (+ alignment slack)
 constexpr size_t kFwdTcSmem = (size_t)kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
 constexpr size_t kBwdQTcSmem = (size_t)2 * kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
