@@ -3,11 +3,11 @@
 // A warp owns 4 consecutive query positions x the 4 query heads of one KV
 // group = 16 mma rows (row r = 4 h + p).  Keys are raw RoPE-rotated K' rows
 // and raw V rows staged per CTA by TMA as shifted slabs: a stage holds a K'
-// region and a V region of two 32-row boxes each (128-byte rows, 128B
+// region and a V region of two 24-row boxes each (128-byte rows, 128B
 // swizzle, rows outside the sequence zero-filled by the TMA unit).
 //  * window chunk s_lo (12 distances): rows = positions i0 - 12 - s_lo + r,
-//    r < 64; warp w reads rows 4w .. 4w + 15 (16 key columns).
-//  * rung pair: box x holds positions i0 - c_x + r, r < 32; B column
+//    r < 48; warp w reads rows 4w .. 4w + 15 (16 key columns).
+//  * rung pair: box x holds positions i0 - c_x + r, r < 24; B column
 //    n = 2 p + e of warp w is row 4w + p + e of the box, so the lane with
 //    tig = p holds both raw logits (floor and floor-plus-one) of position p.
 #pragma once
@@ -21,7 +21,7 @@ namespace sfa {
 constexpr int kTcTQ = 16;                     // query positions per CTA (four CTAs per SM)
 constexpr int kTcWarps = kTcTQ / 4;           // 4 warps
 constexpr int kTcThreads = kTcWarps * 32;     // 128
-constexpr int kTcBoxRows = 32;                // rows per TMA box (4 KB, 1024-byte multiple)
+constexpr int kTcBoxRows = 24;                // rows per TMA box (3 KB, 1024-byte multiple)
 constexpr int kTcBoxB = kTcBoxRows * 128;
 constexpr int kTcRegionB = 2 * kTcBoxB;       // K' (or V) part of a stage
 constexpr int kTcStageB = 2 * kTcRegionB;
