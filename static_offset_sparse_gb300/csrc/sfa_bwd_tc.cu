@@ -24,30 +24,6 @@
 
 namespace sfa {
 
-// Partial dot over the 16 dims a lane holds of two rows (the fragment
-// positions of load_q_frags), completed across the quad.
-__device__ __forceinline__ void quad_row_dots(const bf16* x0, const bf16* x1, const bf16* y0,
-                                              const bf16* y1, float* out) {
-  const int tig = threadIdx.x & 3;
-  float acc[2] = {0.0f, 0.0f};
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const bf16* x = rr ? x1 : x0;
-    const bf16* y = rr ? y1 : y0;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-        const float2 u = unpack_bf16(*reinterpret_cast<const uint32_t*>(x + 16 * kk + 2 * tig + 8 * h8));
-        const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(y + 16 * kk + 2 * tig + 8 * h8));
-        acc[rr] = fmaf(u.x, v.x, fmaf(u.y, v.y, acc[rr]));
-      }
-    acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 1);
-    acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 2);
-    out[rr] = acc[rr];
-  }
-}
-
 // One 32-byte record of key-side coefficients for a (query, slot): the four
 // heads' wt * dS and wt * P, each as bf16 hi + lo (hi = bf16(x),
 // lo = bf16(x - hi)).  Words: dS hi (h0,h1) (h2,h3), dS lo .., P hi .., P lo ..
@@ -69,7 +45,8 @@ template <bool INTERP>
 __global__ void __launch_bounds__(kTcThreads, 4)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
-                    const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mqt,
+                    const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mo,
+                    const __grid_constant__ CUtensorMap mqt,
                     const __grid_constant__ CUtensorMap mdq, uint4* coef, int NS, unsigned* ticket,
                     const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
@@ -94,23 +71,37 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   int nr = 0;
   while (nr < P.n && P.c[nr] <= imax) ++nr;
   const int NG = nwc + (nr + 1) / 2;
-  const uint32_t qtile = sbase, dotile = sbase + kTcQTileB, stages = sbase + 2 * kTcQTileB;
+  const uint32_t qtile = sbase, dotile = sbase + kTcQTileB, otile = sbase + 2 * kTcQTileB;
+  const uint32_t stages = sbase + 3 * kTcQTileB;
   const int qplane = b * a.Hq + g * 4;
-  const CUtensorMap* qmaps[2] = {&mq, &mdo};
-  tc_start(&mk, &mv, qmaps, 2, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+  const CUtensorMap* qmaps[3] = {&mq, &mdo, &mo};
+  tc_start(&mk, &mv, qmaps, 3, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
 
   uint32_t qa[4][4], da[4][4];
   float delta[2], lse2[2];
-  {
-    const bf16* dO = static_cast<const bf16*>(a.dO);
-    const bf16* O = static_cast<const bf16*>(a.o);
-    quad_row_dots(dO + rowA * kD, dO + rowB * kD, O + rowA * kD, O + rowB * kD, delta);
-    lse2[0] = a.lse[rowA] * kLog2e;
-    lse2[1] = a.lse[rowB] * kLog2e;
-  }
+  lse2[0] = a.lse[rowA] * kLog2e;
+  lse2[1] = a.lse[rowB] * kLog2e;
   if (!tc_wait_qtiles(bars, a.status)) return;
   tile_frags(qtile, warp, rope, ic, 0.125f, true, qa);
   tile_frags(dotile, warp, nullptr, ic, 1.0f, false, da);
+  {  // delta = dO . O per row, from the dO and O fragments of this lane (16 dims), then the quad
+    uint32_t oa[4][4];
+    tile_frags(otile, warp, nullptr, ic, 1.0f, false, oa);
+    float acc[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float2 u = unpack_bf16(da[kk][x]), v = unpack_bf16(oa[kk][x]);
+        acc[x & 1] = fmaf(u.x, v.x, fmaf(u.y, v.y, acc[x & 1]));  // x even: row gid, odd: gid + 8
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 1);
+      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
+      delta[r] = acc[r];
+    }
+  }
   __syncthreads();  // the dO tile is read: it now carries q~ = q'/8 out for the key side
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
@@ -493,11 +484,12 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   cudaStream_t s = (cudaStream_t)stream;
   const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
-  CUtensorMap mk, mv, mq, md, mcw, mcr, mq36, mdo36, mqt32, mdq32;
+  CUtensorMap mk, mv, mq, md, mcw, mcr, mq36, mdo36, mo36, mqt32, mdq32;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mq36, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
       make_rows_map(&mdo36, a.dO, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&mo36, a.o, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
       make_rows_map(&mqt32, qt, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&mdq32, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
@@ -518,7 +510,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   if (cudaMemsetAsync(ticket, 0, sizeof(unsigned), s) != cudaSuccess) return SFA_ERR_CUDA;
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
-    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, mq36, mdo36, mqt32, mdq32,
+    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, mq36, mdo36, mo36, mqt32, mdq32,
                                            static_cast<uint4*>(coef), NS, ticket, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));

@@ -131,7 +131,7 @@ constexpr int kTcQTileB = 4 * kTcQRows * 128;  // 10240, a 1024-byte multiple
 constexpr int kTcORows = 16;
 // shared memory: [query tiles][stages] from a 1024-aligned base (+ alignment slack)
 constexpr size_t kFwdTcSmem = (size_t)kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
-constexpr size_t kBwdQTcSmem = (size_t)2 * kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
+constexpr size_t kBwdQTcSmem = (size_t)3 * kTcQTileB + (size_t)kTcStages * kTcStageB + 1024;
 
 // Barriers: one per stage, then one for the query tiles.  Thread 0 issues
 // the query-tile loads (nq boxes from the maps in qmaps, at coordinates
