@@ -290,6 +290,10 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
 
     Returns a dict with dq, dk, dv (fp64, the inputs' shapes), dd (one entry
     per rung slot: dL/dd_k) and, when ``alpha`` is given, dalpha and dtheta.
+    dd_abs / dalpha_abs are the same sums taken over the absolute values of
+    their (position, dimension) terms, and dalpha_rss the root of the sum of
+    their squares: the scales of the rounding error of a low-precision
+    evaluation of dalpha, whose terms cancel.
 
     Per query t and slot n (P, O from the forward):
       delta = dO . O;  dP = dO . v_n;  dS = P (dP - delta)
@@ -319,6 +323,8 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
     dv = np.zeros_like(v)
     rung_ids = [a for a, sl in enumerate(slots) if sl["kind"] == "rung"]
     dd = np.zeros(len(rung_ids))
+    dd_abs = np.zeros(len(rung_ids))
+    dd_sq = np.zeros(len(rung_ids))
     pairs = rows if rows is not None else [(b, g) for b in range(B) for g in range(Hkv)]
     for b, g in pairs:
         Ks, Vs, ok = _slot_rows(k[b, g], v[b, g], slots, T)
@@ -354,14 +360,19 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
                 r = rung_ids.index(a)
                 dK_row = k[b, g, : T - c] - k[b, g, 1 : T - c + 1]
                 dV_row = v[b, g, : T - c] - v[b, g, 1 : T - c + 1]
-                dd[r] += np.sum(dKs[a, c:] * dK_row) + np.sum(dVs[a, c:] * dV_row)
+                tk, tv = dKs[a, c:] * dK_row, dVs[a, c:] * dV_row
+                dd[r] += np.sum(tk) + np.sum(tv)
+                dd_abs[r] += np.sum(np.abs(tk)) + np.sum(np.abs(tv))
+                dd_sq[r] += np.sum(tk * tk) + np.sum(tv * tv)
     if rot:
         dq = rope_apply(dq, cs, sn, inverse=True)
         dk = rope_apply(dk, cs, sn, inverse=True)
-    out = {"dq": dq, "dk": dk, "dv": dv, "dd": dd}
+    out = {"dq": dq, "dk": dk, "dv": dv, "dd": dd, "dd_abs": dd_abs}
     if alpha is not None:
         f = np.array([slots[a]["f"] for a in rung_ids])
         dalpha = float(np.sum(f * dd))
         out["dalpha"] = dalpha
+        out["dalpha_abs"] = float(np.sum(np.abs(f) * dd_abs))
+        out["dalpha_rss"] = float(math.sqrt(np.sum(f * f * dd_sq)))
         out["dtheta"] = dalpha * (alpha - 0.5) * (1.5 - alpha)
     return out

@@ -357,3 +357,14 @@ def test_backward_gqa_equals_repeated_kv_summed():
     assert np.abs(g["dq"] - g2["dq"]).max() < 1e-13
     assert np.abs(g["dk"] - g2["dk"].reshape(1, 2, 2, 20, 4).sum(2)).max() < 1e-13
     assert np.abs(g["dv"] - g2["dv"].reshape(1, 2, 2, 20, 4).sum(2)).max() < 1e-13
+
+
+def test_dalpha_error_scales_bound_the_sum():
+    """dalpha_abs / dalpha_rss (tolerance scales of the bf16 dL/dalpha check):
+    |sum| <= sum of |terms| and rss <= sum of |terms| <= sqrt(#terms) rss."""
+    x = si.make_qkvdo(1, 40, 4, 1, 64, "f32", seed=7)
+    base = o.fib_offsets(8)
+    g = o.backward(x["q"], x["k"], x["v"], x["do"], o.interp_slots(base, 0.9, 2), 1e4, alpha=0.9)
+    n_terms = sum(2 * 40 * 64 for s in o.interp_slots(base, 0.9, 2) if s["kind"] == "rung")
+    assert abs(g["dalpha"]) <= g["dalpha_abs"]
+    assert 0.0 < g["dalpha_rss"] <= g["dalpha_abs"] <= math.sqrt(n_terms) * g["dalpha_rss"] * (1 + 1e-12)
