@@ -288,6 +288,10 @@ constexpr int kKvThreads = 256;               // 8 warps: 4 key groups of 8 rows
 // plane stride 2 (mod 8) rows, so the 128B swizzle puts the 8 (query, head)
 // rows of one ldmatrix tile on distinct banks.
 constexpr int kKvQ = kKvTK + 10;
+// A rung group reaches queries j + c - 1 .. j + c + 31 (33 rows); 34 rows keep
+// the plane stride at 2 (mod 8).  Each warp reads 12 of them (3 k-steps), from
+// row min(8 kw, 22) on, which covers its keys' 9 queries 8 kw .. 8 kw + 8.
+constexpr int kKvQR = kKvTK + 2;
 constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
 constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][42 queries][128 B]
 constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // records box: [42 queries][9 slots][32 B]
@@ -299,8 +303,9 @@ constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 // dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
 template <int NKS>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int nsl,
-                                         bool win, int s_lo, int s_hi, int c, int qw, int kw, int j,
-                                         int T, int dh, float (*dk)[4], float (*dv)[4]) {
+                                         bool win, int s_lo, int s_hi, int c, int qw, int kq,
+                                         int qoff, int j, int T, int dh, float (*dk)[4],
+                                         float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
@@ -322,7 +327,7 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
         else if (qi - j == c - 1) sl = 1;
       }
       if (sl >= 0 && qi < T && j < T) {
-        const uint32_t* rec = csm + ((8 * kw + ql) * nsl + sl) * 8 + (tig & 1);
+        const uint32_t* rec = csm + ((qoff + ql) * nsl + sl) * 8 + (tig & 1);
         bk[hb] = rec[0];
         bkl[hb] = rec[2];
         bvv[hb] = rec[4];
@@ -332,9 +337,9 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
       }
     }
     // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
-    // k index kx = 4 (query offset) + head lives in slab row head * 42 + query
+    // k index kx = 4 (query offset) + head lives in slab row head * kq + query
     const int kx = 8 * (mi >> 1) + (lane & 7);
-    const int arow = (kx & 3) * kKvQ + 8 * kw + 4 * ks + (kx >> 2);
+    const int arow = (kx & 3) * kq + qoff + 4 * ks + (kx >> 2);
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       const int mt = dh + 2 * x;
@@ -353,7 +358,8 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
 template <bool INTERP>
 __global__ void __launch_bounds__(kKvThreads, 2)
     bwd_kv_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mq,
-                     const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mcw,
+                     const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mqr,
+                     const __grid_constant__ CUtensorMap mdr, const __grid_constant__ CUtensorMap mcw,
                      const __grid_constant__ CUtensorMap mcr, const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bars[kKvStages];
@@ -383,13 +389,17 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   auto issue = [&](int grp, uint32_t st, uint32_t bar) {
     const bool win = grp < nwc;
     const int qb = qb_of(grp);
-    mbar_expect_tx(bar, 2 * kKvPlaneB + (win ? kKvCoefB : kKvQ * 2 * 32));
-    tma_load_3d(st, &mq, 0, qb, hplane, bar);
-    tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
-    if (win)
+    if (win) {
+      mbar_expect_tx(bar, 2 * kKvPlaneB + kKvCoefB);
+      tma_load_3d(st, &mq, 0, qb, hplane, bar);
+      tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
       tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, bg, bar);
-    else
+    } else {
+      mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * 32);
+      tma_load_3d(st, &mqr, 0, qb, hplane, bar);
+      tma_load_3d(st + kKvPlaneB, &mdr, 0, qb, hplane, bar);
       tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, bg, bar);
+    }
   };
 
   if (tid == 0) {
@@ -412,13 +422,14 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     }
     const uint32_t qst = sbase + st * kKvStageB;
     const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
-    const int qw = qb_of(grp) + 8 * kw;  // query of k index 0 of this warp
     if (grp < nwc) {
       const int s_lo = kKvWC * grp;
-      kv_group<4>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0, qw,
-                  kw, j, T, dh, dk, dv);
+      kv_group<4>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0,
+                  qb_of(grp) + 8 * kw, kKvQ, 8 * kw, j, T, dh, dk, dv);
     } else {
-      kv_group<3>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qw, kw, j, T, dh, dk, dv);
+      const int qoff = min(8 * kw, kKvQR - 12);
+      kv_group<3>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qb_of(grp) + qoff,
+                  kKvQR, qoff, j, T, dh, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && grp + kKvStages < NG) issue(grp + kKvStages, qst, smem_u32(&bars[st]));
@@ -484,7 +495,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   cudaStream_t s = (cudaStream_t)stream;
   const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
-  CUtensorMap mk, mv, mq, md, mcw, mcr, mq36, mdo36, mo36, mqt32, mdq32;
+  CUtensorMap mk, mv, mq, md, mqr, mdr, mcw, mcr, mq36, mdo36, mo36, mqt32, mdq32;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mq36, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
@@ -494,8 +505,10 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_rows_map(&mdq32, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
+      make_rows_map(&mqr, qt, qplanes, a.T, kKvQR, 4) != SFA_OK ||
+      make_rows_map(&mdr, a.dO, qplanes, a.T, kKvQR, 4) != SFA_OK ||
       make_coef_map(&mcw, coef, kvplanes, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
-      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 2, kKvQ) != SFA_OK)
+      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 2, kKvQR) != SFA_OK)
     return SFA_ERR_CUDA;
   auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
   auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
@@ -516,7 +529,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
-    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, mq, md, mcw, mcr, p);
+    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, mq, md, mqr, mdr, mcw, mcr, p);
   }
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }

@@ -28,9 +28,9 @@ namespace sfa {
 
 // K' = RoPE(K) as bf16 rows (the operand of every key-side product).  A
 // thread owns one position and one 8-pair chunk of the rotation: it loads
-// that chunk of the cos/sin table once and rotates the position's rows in
-// kPrepPlanes consecutive (batch, KV head) planes.
-constexpr int kPrepPlanes = 8;
+// that chunk of the cos/sin table once and rotates the position's row in
+// the planes blockIdx.y, + gridDim.y, ... (one plane per grid row, so a
+// layer's planes spread over thousands of CTAs and the copy streams).
 
 __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__ k,
                                                         const float2* __restrict__ rope,
@@ -40,11 +40,7 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__
   const int pos = (int)(it >> 2), pc = (int)(it & 3);
   float cs[8], sn[8];
   load_rope8(rope, pos, 8 * pc, cs, sn);
-  const int64_t p0 = (int64_t)blockIdx.y * kPrepPlanes;
-#pragma unroll
-  for (int x = 0; x < kPrepPlanes; ++x) {
-    const int64_t plane = p0 + x;
-    if (plane >= planes) break;
+  for (int64_t plane = blockIdx.y; plane < planes; plane += gridDim.y) {
     const int64_t row = plane * T + pos;
     float lo[8], hi[8];
     load8(k + row * kD + 8 * pc, lo);
@@ -57,14 +53,14 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__
 
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream) {
   const int64_t planes = rows / T;
-  dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)((planes + kPrepPlanes - 1) / kPrepPlanes));
+  dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)(planes < 65535 ? planes : 65535));
   rope_prep_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
       static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), planes, T);
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }
 
 template <bool INTERP>
-__global__ void __launch_bounds__(kTcThreads, 4)
+__global__ void __launch_bounds__(kTcThreads, 5)
     fwd_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mo, const __grid_constant__ Plan P) {
@@ -100,34 +96,46 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 
   // online-softmax step for this lane's logits of rows gid (r = 0) and gid + 8
   // (r = 1); s holds N values per row (invalid = -inf), returns P in place.
+  // The running maximum m (base 2) is refreshed only when some logit of the
+  // warp exceeds it by more than kMargin: between refreshes p = 2^(s - m) stays
+  // below 2^kMargin, and O = sum p v / sum p and LSE = m + log2 l are exact for
+  // any m.  m stays uniform over a row's quad (it changes only through the quad
+  // reduction).
+  constexpr float kMargin = 8.0f;
   auto softmax_step = [&](float (*s)[4], auto Nc) {
     constexpr int N = decltype(Nc)::value;
+    float mx[2];
+    bool need = false;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float mx = s[r][0];
+      mx[r] = s[r][0];
 #pragma unroll
-      for (int e = 1; e < N; ++e) mx = fmaxf(mx, s[r][e]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float mn = fmaxf(m[r], mx);
-      if (mn == -INFINITY) {  // no key for this row yet
+      for (int e = 1; e < N; ++e) mx[r] = fmaxf(mx[r], s[r][e]);
+      need |= mx[r] > m[r] + kMargin;  // m = -inf: any valid logit
+    }
+    if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-        for (int e = 0; e < N; ++e) s[r][e] = 0.0f;
-        continue;
-      }
-      if (mn > m[r]) {  // rescale only when the running maximum moves
-        const float corr = ex2(m[r] - mn);
-        m[r] = mn;
-        l[r] *= corr;
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        if (mx[r] > m[r]) {
+          const float corr = ex2(m[r] - mx[r]);  // 0 while the row had no key
+          m[r] = mx[r];
+          l[r] *= corr;
 #pragma unroll
-        for (int nd = 0; nd < 8; ++nd) {
-          o[nd][2 * r] *= corr;
-          o[nd][2 * r + 1] *= corr;
+          for (int nd = 0; nd < 8; ++nd) {
+            o[nd][2 * r] *= corr;
+            o[nd][2 * r + 1] *= corr;
+          }
         }
       }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float mm = m[r] == -INFINITY ? 0.0f : m[r];
 #pragma unroll
       for (int e = 0; e < N; ++e) {
-        const float pe = ex2(s[r][e] - mn);  // ex2(-inf) = 0
+        const float pe = ex2(s[r][e] - mm);  // ex2(-inf) = 0
         s[r][e] = pe;
         l[r] += pe;
       }
