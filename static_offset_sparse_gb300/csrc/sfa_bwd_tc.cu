@@ -24,21 +24,18 @@
 
 namespace sfa {
 
-// One 32-byte record of key-side coefficients for a (query, slot): the four
-// heads' wt * dS and wt * P, each as bf16 hi + lo (hi = bf16(x),
-// lo = bf16(x - hi)).  Words: dS hi (h0,h1) (h2,h3), dS lo .., P hi .., P lo ..
-__device__ __forceinline__ void write_coef(uint4* dst, float wt, const float* ds4, const float* p4) {
-  uint32_t hi[4], lo[4];
-#pragma unroll
-  for (int x = 0; x < 4; ++x) {
-    const float* src = x < 2 ? ds4 : p4;
-    const float a = wt * src[2 * (x & 1)], b = wt * src[2 * (x & 1) + 1];
-    hi[x] = pack_bf16(a, b);
-    const float2 h = unpack_bf16(hi[x]);
-    lo[x] = pack_bf16(a - h.x, b - h.y);
-  }
-  dst[0] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
-  dst[1] = make_uint4(hi[2], hi[3], lo[2], lo[3]);
+// One 32-byte record of key-side coefficients for a (query, slot) is two
+// 16-byte halves, one per head pair (0, 2) and (1, 3): the pair's wt * dS and
+// wt * P as bf16 hi + lo (hi = bf16(x), lo = bf16(x - hi)), each word
+// holding the pair's two heads (lower head in the low half).  Words:
+// dS hi, dS lo, P hi, P lo.  The lane whose fragment rows are the pair's two
+// heads writes its half directly.
+__device__ __forceinline__ void write_coef_half(uint4* dst, float wt, float ds0, float ds1, float p0,
+                                                float p1) {
+  const float a0 = wt * ds0, a1 = wt * ds1, b0 = wt * p0, b1 = wt * p1;
+  const uint32_t dh = pack_bf16(a0, a1), ph = pack_bf16(b0, b1);
+  const float2 dhf = unpack_bf16(dh), phf = unpack_bf16(ph);
+  *dst = make_uint4(dh, pack_bf16(a0 - dhf.x, a1 - dhf.y), ph, pack_bf16(b0 - phf.x, b1 - phf.y));
 }
 
 template <bool INTERP>
@@ -117,10 +114,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
   float dacc = 0.0f;
-  // records of query i: [slot][2 x uint4]; lanes with gid < 4 hold heads 0, 2
-  // and receive heads 1, 3 from lane ^ 16 (same position and columns)
-  uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2;
-  const bool writer = gid < 4;
+  // records of query i: [slot][2 x uint4]; this lane's rows gid, gid + 8 are
+  // heads hA, hA + 2 of position p, i.e. half gid >> 2 of each record
+  uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2 + (gid >> 2);
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
@@ -150,16 +146,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
         }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        const float o_ds0 = __shfl_xor_sync(0xffffffffu, ds[0][cc], 16);
-        const float o_ds1 = __shfl_xor_sync(0xffffffffu, ds[1][cc], 16);
-        const float o_p0 = __shfl_xor_sync(0xffffffffu, pp[0][cc], 16);
-        const float o_p1 = __shfl_xor_sync(0xffffffffu, pp[1][cc], 16);
         const int dist = p + 12 + s_lo - (8 * (cc >> 1) + 2 * tig + (cc & 1));
-        if (writer && act && dist >= s_lo && dist <= s_hi && dist <= i) {
-          const float d4[4] = {ds[0][cc], o_ds0, ds[1][cc], o_ds1};
-          const float p4[4] = {pp[0][cc], o_p0, pp[1][cc], o_p1};
-          write_coef(crow + 2 * dist, 1.0f, d4, p4);
-        }
+        if (act && dist >= s_lo && dist <= s_hi && dist <= i)
+          write_coef_half(crow + 2 * dist, 1.0f, ds[0][cc], ds[1][cc], pp[0][cc], pp[1][cc]);
       }
       sa[0] = pack_bf16(ds[0][0], ds[0][1]);
       sa[1] = pack_bf16(ds[1][0], ds[1][1]);
@@ -192,15 +181,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
           if (INTERP && v)
             dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
         }
-        const float o_d0 = __shfl_xor_sync(0xffffffffu, ds[0][x], 16);
-        const float o_d1 = __shfl_xor_sync(0xffffffffu, ds[1][x], 16);
-        const float o_p0 = __shfl_xor_sync(0xffffffffu, prr[0], 16);
-        const float o_p1 = __shfl_xor_sync(0xffffffffu, prr[1], 16);
-        if (writer && v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
-          const float d4[4] = {ds[0][x], o_d0, ds[1][x], o_d1};
-          const float p4[4] = {prr[0], o_p0, prr[1], o_p1};
-          write_coef(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, d4, p4);
-          write_coef(crow + 2 * (P.W + 2 + 2 * rg), w, d4, p4);
+        if (v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
+          write_coef_half(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, ds[0][x], ds[1][x], prr[0], prr[1]);
+          write_coef_half(crow + 2 * (P.W + 2 + 2 * rg), w, ds[0][x], ds[1][x], prr[0], prr[1]);
         }
       }
       sa[0] = pack_bf16(ds[0][0] * (1.0f - wgt[0]), ds[0][0] * wgt[0]);
@@ -311,8 +294,9 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
   for (int ks = 0; ks < NKS; ++ks) {
     // B: the records of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
     // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
-    // (q - j = c - 1); words (tig & 1) + {0, 2, 4, 6} = dS hi, dS lo, P hi,
-    // P lo of heads 2 (tig & 1) and 2 (tig & 1) + 1
+    // (q - j = c - 1).  Within a query the k order of the heads is 0, 2, 1, 3,
+    // so the pair of lane tig is record half tig & 1 (heads tig & 1 and
+    // (tig & 1) + 2): words dS hi, dS lo, P hi, P lo
     uint32_t bk[2], bvv[2], bkl[2], bvl[2];
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
@@ -327,19 +311,20 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
         else if (qi - j == c - 1) sl = 1;
       }
       if (sl >= 0 && qi < T && j < T) {
-        const uint32_t* rec = csm + ((qoff + ql) * nsl + sl) * 8 + (tig & 1);
-        bk[hb] = rec[0];
-        bkl[hb] = rec[2];
-        bvv[hb] = rec[4];
-        bvl[hb] = rec[6];
+        const uint4 rec = *reinterpret_cast<const uint4*>(csm + ((qoff + ql) * nsl + sl) * 8 + 4 * (tig & 1));
+        bk[hb] = rec.x;
+        bkl[hb] = rec.y;
+        bvv[hb] = rec.z;
+        bvl[hb] = rec.w;
       } else {
         bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
       }
     }
     // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
-    // k index kx = 4 (query offset) + head lives in slab row head * kq + query
+    // k index kx = 4 (query offset) + hs (head slot; head 2 (hs & 1) + (hs >> 1)
+    // by the order 0, 2, 1, 3) lives in slab row head * kq + query
     const int kx = 8 * (mi >> 1) + (lane & 7);
-    const int arow = (kx & 3) * kq + qoff + 4 * ks + (kx >> 2);
+    const int arow = (((kx & 1) << 1) | ((kx >> 1) & 1)) * kq + qoff + 4 * ks + (kx >> 2);
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       const int mt = dh + 2 * x;
