@@ -11,7 +11,9 @@ independently drawn Q, K, V, dO (N(0, 1), seeded), so each step streams
 needed between steps).
 
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
-bounded sample of the same workload instead.
+bounded sample of the same workload instead.  ``--mode decode`` measures the
+integer-path decode step instead (one new token per sequence through the
+16-layer stack against a T = 16384 cache); its JSON line names its own metric.
 
 Launch: python bench.py [--gpus N --steps K --warmup W]; N > 1 under
 torch.distributed.run (one rank per GPU, weak scaling: every rank runs its
@@ -20,10 +22,16 @@ all-reduce per step, as data-parallel training of theta would).
 """
 from __future__ import annotations
 
+import os
+
+# The CPU oracle legs report a single core: keep BLAS / OpenMP pools at one
+# thread (set before numpy is first imported).
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import argparse
 import hashlib
 import json
-import os
 import statistics
 import subprocess
 import sys
@@ -393,6 +401,247 @@ def reference_arm(args):
                     "d2h_bytes_per_step": 0}}
 
 
+# ---- decode mode (--mode decode): one new token per sequence -------------
+DEC_T = 16384  # cache capacity: the longest integer-path sequence of the configs
+DEC_METRIC = ("decode tokens/s: one query per sequence through a 16-layer staggered integer "
+              "stack (W=8, Fibonacci K=15, alpha_l rounded), cache T=16384, GQA 8/2 bf16")
+
+
+def dec_distances(alpha: float, W: int):
+    """Integer-path key set of one layer: {0..W} and round-half-even(alpha f)."""
+    return sorted(set(range(W + 1)) | {round(alpha * f) for f in FIB})
+
+
+DEC_STEPS_MAX = 1024  # positions advance one per step; starts leave room for this many
+
+
+def dec_positions(Bd: int):
+    """First positions of the Bd sequences: seeded, uniform in [T/2, T - 1024)."""
+    import sfa_inputs as si
+
+    u = si.uniform(si.mix_seed(9, Bd), Bd)
+    span = DEC_T // 2 - DEC_STEPS_MAX
+    return [DEC_T // 2 + int(x * span) for x in u]
+
+
+class DecLayer:
+    """One layer's caches, query rows and prebuilt decode descriptor."""
+
+    def __init__(self, sfa, lib, l, alpha, W, Bd, pos_dev, dev):
+        import ctypes as C
+        import sfa_inputs as si
+
+        def gen(tid, shape):
+            n = 1
+            for x in shape:
+                n *= x
+            return si.normal_device(si.mix_seed(7, l, tid), n, dev).view(*shape).to(__import__("torch").bfloat16)
+
+        self.q = gen(1, (Bd, HQ, D)).contiguous()
+        self.k = gen(2, (Bd, HKV, DEC_T, D)).contiguous()
+        self.v = gen(3, (Bd, HKV, DEC_T, D)).contiguous()
+        self.o = self.q.new_empty(self.q.shape)
+        self.lse = self.q.new_empty((Bd, HQ), dtype=__import__("torch").float32)
+        self.dist = dec_distances(alpha, W)
+        self.desc = sfa.make_desc(self.q, self.k, dist=self.dist, rope_theta=1e4)
+        self.lib, self.pos = lib, pos_dev  # [steps, Bd]: row r = positions of step r
+        self.pre = [C.byref(self.desc)] + [C.c_void_p(t.data_ptr()) for t in (self.q, self.k, self.v)]
+        self.posp = [C.c_void_p(pos_dev[r].data_ptr()) for r in range(pos_dev.shape[0])]
+        self.post = [C.c_void_p(self.o.data_ptr()), C.c_void_p(self.lse.data_ptr())]
+
+    def run(self, sp, r):
+        self.run_ptr(sp, self.posp[r])
+
+    def run_ptr(self, sp, posp):
+        rc = self.lib.sfa_decode_int(*self.pre, posp, *self.post, sp)
+        if rc:
+            raise RuntimeError(f"sfa_decode_int failed: {rc}")
+
+
+def dec_bytes_per_step(layers, Bd):
+    """HBM bytes one 16-layer decode step must move: every gathered K and V
+    row (bf16, 128 B) of every (sequence, KV head), the query rows in and the
+    output rows and LSE out."""
+    tot = 0
+    for L in layers:
+        tot += Bd * HKV * len(L.dist) * 2 * D * 2 + Bd * HQ * D * 2 * 2 + Bd * HQ * 4
+    return tot
+
+
+def decode_arm(args, dev):
+    import ctypes as C
+    import torch
+
+    import static_offset_sparse_gb300 as sfa
+    from static_offset_sparse_gb300._lib import _lib
+
+    Bd = args.decode_batch
+    n_e2e = min(args.steps, 50)
+    n_total = args.warmup + args.steps + n_e2e + 1
+    if n_total > DEC_STEPS_MAX:
+        raise SystemExit(f"--mode decode: at most {DEC_STEPS_MAX} steps in all")
+    pos0 = torch.tensor(dec_positions(Bd), dtype=torch.int32)
+    pos_dev = (pos0[None, :] + torch.arange(n_total, dtype=torch.int32)[:, None]).to(dev).contiguous()
+    al = alphas(args.schedule)
+    layers = [DecLayer(sfa, _lib(), l, al[l], args.W, Bd, pos_dev, dev) for l in layer_ids()]
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+
+    ctr = [0]
+
+    def step():  # every sequence advances one position per step
+        r = ctr[0]
+        ctr[0] += 1
+        for L in layers:
+            L.run(sp, r)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert sfa.get_device_status() == 0
+    sfa.timing_enable(True)
+    sfa.timing_read()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    kt = sfa.timing_read()
+    sfa.timing_enable(False)
+    ms_eager = ev0.elapsed_time(ev1) / args.steps
+    per_launch_eager = kt["decode"][0] / max(1, kt["decode"][1])
+    eager_launches = int(sum(c for _, c in kt.values()))
+
+    # The same step as one CUDA graph (how a decode loop amortises launch
+    # cost): advance every position by one, then the 16 decode calls.
+    pos_cur = pos_dev[ctr[0]].clone()
+    cur_p = C.c_void_p(pos_cur.data_ptr())
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm the capture path (torch requires it)
+        pos_cur.add_(0)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cs = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        pos_cur.add_(1)
+        for L in layers:
+            L.run_ptr(cs, cur_p)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert sfa.get_device_status() == 0
+    ms = ev0.elapsed_time(ev1) / args.steps
+    per_launch_ms = ms / len(layers)
+    nbytes = dec_bytes_per_step(layers, Bd)
+    peak, src = hbm_peak()
+    achieved = nbytes / len(layers) / (per_launch_ms * 1e-3) / 1e9
+    # end to end: each step copies every layer's query rows in from pinned host
+    # memory and its output rows and LSE back
+    hq = [L.q.to("cpu").pin_memory() for L in layers]
+    ho = [(torch.empty(L.o.shape, dtype=L.o.dtype).pin_memory(),
+           torch.empty(L.lse.shape, dtype=L.lse.dtype).pin_memory()) for L in layers]
+
+    def step_e2e():
+        r = ctr[0]
+        ctr[0] += 1
+        for L, a, (bo, bl) in zip(layers, hq, ho):
+            L.q.copy_(a, non_blocking=True)
+            L.run(sp, r)
+            bo.copy_(L.o, non_blocking=True)
+            bl.copy_(L.lse, non_blocking=True)
+
+    step_e2e()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e - 1):
+        step_e2e()
+    torch.cuda.synchronize()
+    el = (time.perf_counter() - t0) / (n_e2e - 1)
+    keys = sorted({len(L.dist) for L in layers})
+    out = {"metric": DEC_METRIC, "value": round(Bd / (ms * 1e-3), 1), "unit": "tokens/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic: seeded N(0,1) caches and query rows per layer",
+           "config": {"workload": f"integer decode, {len(layers)} layers (alpha_l {args.schedule}, "
+                                  f"rounded), W={args.W}: B={Bd} sequences starting at positions in "
+                                  f"[{DEC_T // 2}, {DEC_T - DEC_STEPS_MAX}), one position further each "
+                                  f"step, cache T={DEC_T}, Hq={HQ} Hkv={HKV} "
+                                  f"D={D}, RoPE 1e4, {keys[0]}-{keys[-1]} keys per query",
+                      "global_batch": Bd, "seq_len": DEC_T, "layers": len(layers),
+                      "parallelism": "dp1",
+                      "l2": "caches 4.3 GB exceed L2; positions advance each step, so a step's "
+                            "rung rows are new while most window rows were read the step before"},
+           "roofline": {"bound": "hbm", "kernel": "decode", "achieved": round(achieved, 1),
+                        "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": None, "peak_source": src,
+                        "algorithmic_bytes_per_launch": nbytes // len(layers),
+                        "per_launch_ms": round(per_launch_ms, 4),
+                        "note": "per-launch time = graph step / layers (includes the position "
+                                "advance); the step is latency-bound, not bandwidth-bound"},
+           "eager": {"value": round(Bd / (ms_eager * 1e-3), 1), "unit": "tokens/s",
+                     "ms_per_step": round(ms_eager, 4), "per_launch_ms": round(per_launch_eager, 4),
+                     "gpu_launches": eager_launches,
+                     "note": "one host call per layer and step (ctypes), no graph"},
+           "gpu_launches": len(layers) * args.steps, "clocks": clk,
+           "e2e": {"value": round(Bd / el, 1), "unit": "tokens/s",
+                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hq),
+                   "d2h_bytes_per_step": sum(a.numel() * a.element_size() + b.numel() * b.element_size()
+                                             for a, b in ho),
+                   "ms_per_step": round(el * 1e3, 3), "steps": n_e2e}}
+    if args.cpu_budget > 0:
+        out["cpu_baseline"] = dec_cpu_baseline(args, min(args.cpu_budget, 10.0))
+    return out
+
+
+def dec_cpu_baseline(args, budget_s: float):
+    """The oracle decode as it stands, timed on this host: one sequence of
+    layer 7 (seeded host cache of the workload's shape) per sample, until
+    ~budget_s of oracle work; scaled to the 16-layer step."""
+    import oracle
+    import sfa_inputs as si
+
+    l = 7
+    pos_first = dec_positions(args.decode_batch)[0]
+    dist = dec_distances(alphas(args.schedule)[l], args.W)
+    q = si.make_tensor((1, HQ, D), "bf16", si.mix_seed(7, l, 1))
+    k = si.make_tensor((1, HKV, DEC_T, D), "bf16", si.mix_seed(7, l, 2))
+    v = si.make_tensor((1, HKV, DEC_T, D), "bf16", si.mix_seed(7, l, 3))
+    spent, n = 0.0, 0
+    while spent < budget_s and n < 400:
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, [pos_first + n % DEC_STEPS_MAX], dist, 1e4)
+        spent += time.perf_counter() - t0
+        n += 1
+    tok_s = n / (spent * LAYERS)
+    return {"value": round(tok_s, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle decode, {n} single-sequence steps of layer {l} "
+                      f"({len(dist)} keys, RoPE, cache T={DEC_T}), single thread; {spent:.2f} s of "
+                      f"oracle work; scaled to the {LAYERS}-layer step"}
+
+
+def dec_reference_arm(args):
+    """--impl reference --mode decode: the oracle decode timed on this host."""
+    cb = dec_cpu_baseline(args, 10.0)
+    return {"metric": DEC_METRIC, "impl": "reference", "value": cb["value"], "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(args.decode_batch / cb["value"] * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"integer decode, cache T={DEC_T}, W={args.W}"}, "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def config(args):
     return {"workload": f"interp {args.schedule} schedule, W={args.W}: B={B} T={T} Hq={HQ} Hkv={HKV} "
                         f"D={D}, {LAYERS} layers, Fibonacci K=15, RoPE 1e4, fwd+bwd+dtheta",
@@ -412,6 +661,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
+    ap.add_argument("--mode", default="train", choices=["train", "decode"],
+                    help="train: the fwd+bwd step (default); decode: one token per sequence")
+    ap.add_argument("--decode-batch", type=int, default=32)
     args = ap.parse_args()
     global LAYERS
     LAYERS = args.layers
@@ -421,7 +673,8 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(reference_arm(args)), flush=True)
+            arm = dec_reference_arm if args.mode == "decode" else reference_arm
+            print(json.dumps(arm(args)), flush=True)
         return
 
     import torch
@@ -437,6 +690,10 @@ def main():
 
     if not os.path.exists(LIB_PATH):
         raise SystemExit("libsfa.so is not built: run __graft_entry__.build() first")
+    if args.mode == "decode":  # one process per GPU, independent replicas
+        if rank == 0:
+            print(json.dumps(decode_arm(args, dev)), flush=True)
+        return
     layers, ms, clk, launches, roofline = gpu_arm(args, rank, world, dev)
     value = world * B * T / (ms * 1e-3)
     hbm = UNIQUE_BYTES_PER_TOKEN * B * T * LAYERS / (ms * 1e-3) / 1e9

@@ -166,6 +166,25 @@ int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void
                      const void* o, const float* lse, const void* dO, void* dq, void* dk,
                      void* dv, void* ws, size_t ws_bytes, void* stream);
 
+/* Incremental decode on the integer path: one new query per sequence
+ * against a key/value cache ("Depth-Staggered ...": the method's efficiency
+ * case is inference; "Christoffel-Balanced Sparse Attention": gather only
+ * the allowed offsets of each query).
+ *   q        [B, Hq, 64]     the queries, sequence b at position pos[b]
+ *   k_cache  [B, Hkv, T, 64] raw (unrotated) keys; T = d->T is the capacity,
+ *   v_cache  [B, Hkv, T, 64] rows 0..pos[b] of sequence b must be written
+ *   pos      device int32 [B], 0 <= pos[b] < T (sequences may differ)
+ *   o        [B, Hq, 64]     output (d->dtype)
+ *   lse      fp32 [B, Hq]    natural-log softmax denominator, or NULL
+ * Keys of sequence b: pos[b] - s for every s in d->dist with s <= pos[b]
+ * (d->dist must contain 0).  With d->rope the query is rotated at pos[b] and
+ * each gathered key at its own position.  The result is row pos[b] of
+ * sfa_forward_int over that sequence's prefix, computed in fp32.  No
+ * workspace.  A position outside [0, T) is skipped on the device and
+ * recorded as SFA_ERR_DEVICE_BOUNDS. */
+int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* pos, void* o, float* lse, void* stream);
+
 /* Allocation-free variant of sfa_forward (no counterpart on the pages; it
  * exists for callers that cannot allocate device memory: programs whose
  * allocator owns all device memory and bars raw cudaMalloc from libraries,
@@ -197,7 +216,8 @@ typedef enum {
   SFA_KERNEL_DALPHA = 3,
   SFA_KERNEL_ROPE = 4,
   SFA_KERNEL_PREP = 5, /* RoPE-rotated bf16 copy of K for the tensor-core kernels */
-  SFA_KERNEL_KINDS = 6
+  SFA_KERNEL_DECODE = 6,
+  SFA_KERNEL_KINDS = 7
 } sfa_kernel_kind;
 int sfa_timing_enable(int on);
 int sfa_timing_read(double* ms, int64_t* launches, int n);

@@ -281,6 +281,43 @@ def forward(q, k, v, slots, rope_theta: float = 1e4, rows=None):
     return O, LSE
 
 
+def decode(q, k, v, pos, dist, rope_theta: float = 1e4):
+    """One decode step on the integer path (fp64).
+
+    q [B,Hq,D]: the query of sequence b at position pos[b]; k/v [B,Hkv,T,D]:
+    the caches (raw keys).  Keys of sequence b: pos[b] - s for s in dist with
+    s <= pos[b] ("Depth-Staggered ...", method section: integer offsets as an
+    exact gather).  RoPE rotates the query at pos[b] and every key at its own
+    position; logits q'.k' / sqrt(D), softmax, O = sum P v.  Returns O
+    [B,Hq,D] and LSE [B,Hq]: the forward's row pos[b] of that prefix.
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    B, Hq, D = q.shape
+    Hkv, T = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    S = sorted({int(x) for x in dist})
+    rot = bool(rope_theta and rope_theta > 0)
+    if rot:
+        cs, sn = rope_cos_sin(T, D, rope_theta)
+    O = np.zeros((B, Hq, D))
+    LSE = np.zeros((B, Hq))
+    for b in range(B):
+        t = int(pos[b])
+        keys = np.array([t - x for x in S if x <= t], dtype=np.int64)
+        for h in range(Hq):
+            g = h // G
+            qh, Kr = q[b, h], k[b, g, keys]
+            if rot:
+                qh = rope_apply(qh[None], cs[t:t + 1], sn[t:t + 1])[0]
+                Kr = rope_apply(Kr, cs[keys], sn[keys])
+            sc = Kr @ qh / math.sqrt(D)
+            m = sc.max()
+            e = np.exp(sc - m)
+            O[b, h] = (e / e.sum()) @ v[b, g, keys]
+            LSE[b, h] = m + math.log(e.sum())
+    return O, LSE
+
+
 def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = None, rows=None):
     """Gradients of L = sum(O * dO) (no batch averaging).
 

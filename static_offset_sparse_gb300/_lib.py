@@ -71,6 +71,7 @@ def _lib():
                                      C.c_size_t, _P],
                 "sfa_get_device_status": [_P, _I32P],
                 "sfa_forward_noalloc": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P],
+                "sfa_decode_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, _P],
                 "sfa_timing_enable": [C.c_int],
                 "sfa_timing_read": [C.POINTER(C.c_double), C.POINTER(C.c_int64), C.c_int],
             }

@@ -116,10 +116,11 @@ def _check_tensor(t, name):
 
 
 def make_desc(q, k, *, W=0, alpha=1.0, base=(), dist=(), rope_theta=1e4):
-    """Build the sfa_desc for q [B,Hq,T,64], k [B,Hkv,T,64].  Keeps the host
-    arrays alive on the returned object."""
-    B, Hq, T, D = q.shape
-    Hkv = k.shape[1]
+    """Build the sfa_desc for k [B,Hkv,T,64] and q [B,Hq,...] (Hq and the
+    dtype are taken from q).  Keeps the host arrays alive on the returned
+    object."""
+    B, Hkv, T, D = k.shape
+    Hq = q.shape[1]
     d = Desc()
     d.B, d.T, d.Hq, d.Hkv, d.D = B, T, Hq, Hkv, D
     d.dtype = _dtype_code(q)
@@ -218,13 +219,31 @@ def backward_int(q, k, v, o, lse, do, *, dist, rope_theta: float = 1e4, **out):
     return _bwd(False, q, k, v, o, lse, do, desc, **out)
 
 
+def decode_int(q, k_cache, v_cache, pos, *, dist, rope_theta: float = 1e4, o=None, lse=None):
+    """One decode step on the integer path: q [B, Hq, 64] at positions pos
+    (int32 [B], on the device) against caches [B, Hkv, T, 64] (raw keys).
+    Returns o [B, Hq, 64] and lse fp32 [B, Hq]."""
+    torch = _torch()
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (pos, "pos")):
+        _check_tensor(t, nm)
+    if q.dim() != 3 or k_cache.dim() != 4 or pos.dtype != torch.int32:
+        raise ValueError("decode_int: q [B, Hq, 64], caches [B, Hkv, T, 64], pos int32 [B]")
+    B, Hkv, T, D = k_cache.shape
+    desc = make_desc(q, k_cache, dist=dist, rope_theta=rope_theta)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, q.shape[1]), dtype=torch.float32, device=q.device) if lse is None else lse
+    check(_lib().sfa_decode_int(C.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos),
+                                _ptr(o), _ptr(lse), _stream()), "sfa_decode_int")
+    return o, lse
+
+
 def get_device_status() -> int:
     out = C.c_int32(0)
     check(_lib().sfa_get_device_status(_stream(), C.byref(out)), "sfa_get_device_status")
     return out.value
 
 
-KERNEL_KINDS = ("fwd", "bwd_q", "bwd_kv", "dalpha_reduce", "rope_table", "prep")
+KERNEL_KINDS = ("fwd", "bwd_q", "bwd_kv", "dalpha_reduce", "rope_table", "prep", "decode")
 
 
 def timing_enable(on: bool = True) -> None:

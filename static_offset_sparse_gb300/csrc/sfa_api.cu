@@ -253,6 +253,27 @@ int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void
   return backward_common(d, 0, q, k, v, o, lse, dO, dq, dk, dv, nullptr, ws, ws_bytes, stream);
 }
 
+int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* pos, void* o, float* lse, void* stream) {
+  int rc = validate_shape(d);
+  if (rc != SFA_OK) return rc;
+  if (!q || !k_cache || !v_cache || !pos || !o) return SFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      ((uintptr_t)pos & 3u) || ((uintptr_t)lse & 3u))
+    return SFA_ERR_INVALID_ARG;
+  Plan p;
+  if ((rc = build_int_plan(d, &p)) != SFA_OK) return rc;
+  AttnArgs a;
+  if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.pos = pos;
+  a.out_o = o;
+  a.out_lse = lse;
+  return launch_decode_int(a, p, d->dtype, stream);
+}
+
 int sfa_timing_enable(int on) {
   std::lock_guard<std::mutex> lock(g_tmu);
   g_timing = on != 0;

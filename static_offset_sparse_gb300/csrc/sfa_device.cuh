@@ -34,6 +34,22 @@ __device__ __forceinline__ void load8(const bf16* p, float* x) {
   }
 }
 
+__device__ __forceinline__ void load2(const float* p, float* x) {
+  const float2 v = *reinterpret_cast<const float2*>(p);
+  x[0] = v.x;
+  x[1] = v.y;
+}
+__device__ __forceinline__ void load2(const bf16* p, float* x) {
+  const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(p);
+  x[0] = __bfloat162float(v.x);
+  x[1] = __bfloat162float(v.y);
+}
+__device__ __forceinline__ void store2(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void store2(bf16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
 __device__ __forceinline__ void store8(float* p, const float* x) {
   reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);

@@ -28,9 +28,11 @@ namespace sfa {
 
 // K' = RoPE(K) as bf16 rows (the operand of every key-side product).  A
 // thread owns one position and one 8-pair chunk of the rotation: it loads
-// that chunk of the cos/sin table once and rotates the position's row in
-// the planes blockIdx.y, + gridDim.y, ... (one plane per grid row, so a
-// layer's planes spread over thousands of CTAs and the copy streams).
+// that chunk of the cos/sin table once and rotates the position's rows in
+// kPrepPlanes consecutive (batch, KV head) planes per grid row (loads issued
+// before the arithmetic), so a layer spreads over hundreds of CTAs.
+
+constexpr int kPrepPlanes = 2;
 
 __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__ k,
                                                         const float2* __restrict__ rope,
@@ -40,20 +42,29 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__
   const int pos = (int)(it >> 2), pc = (int)(it & 3);
   float cs[8], sn[8];
   load_rope8(rope, pos, 8 * pc, cs, sn);
-  for (int64_t plane = blockIdx.y; plane < planes; plane += gridDim.y) {
-    const int64_t row = plane * T + pos;
-    float lo[8], hi[8];
-    load8(k + row * kD + 8 * pc, lo);
-    load8(k + row * kD + 32 + 8 * pc, hi);
-    rotate8(lo, hi, cs, sn);
-    store8(kr + row * kD + 8 * pc, lo);
-    store8(kr + row * kD + 32 + 8 * pc, hi);
+  for (int64_t p0 = (int64_t)blockIdx.y * kPrepPlanes; p0 < planes;
+       p0 += (int64_t)gridDim.y * kPrepPlanes) {
+    float lo[kPrepPlanes][8], hi[kPrepPlanes][8];
+#pragma unroll
+    for (int x = 0; x < kPrepPlanes; ++x) {  // all loads first
+      const int64_t row = (p0 + x < planes ? p0 + x : p0) * T + pos;
+      load8(k + row * kD + 8 * pc, lo[x]);
+      load8(k + row * kD + 32 + 8 * pc, hi[x]);
+    }
+#pragma unroll
+    for (int x = 0; x < kPrepPlanes; ++x) {
+      if (p0 + x >= planes) break;
+      const int64_t row = (p0 + x) * T + pos;
+      rotate8(lo[x], hi[x], cs, sn);
+      store8(kr + row * kD + 8 * pc, lo[x]);
+      store8(kr + row * kD + 32 + 8 * pc, hi[x]);
+    }
   }
 }
 
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream) {
   const int64_t planes = rows / T;
-  dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)(planes < 65535 ? planes : 65535));
+  dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)((planes + kPrepPlanes - 1) / kPrepPlanes < 65535 ? (planes + kPrepPlanes - 1) / kPrepPlanes : 65535));
   rope_prep_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
       static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), planes, T);
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;

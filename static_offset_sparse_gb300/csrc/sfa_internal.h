@@ -44,6 +44,7 @@ struct AttnArgs {
   double* dalpha_part; // workspace, one per backward key-side CTA
   double* dalpha_out;  // device [2]: dL/dalpha, dL/dtheta (or nullptr)
   double alpha;
+  const int32_t* pos;  // decode: device [B] query positions
   int32_t B, T, Hq, Hkv, lgG;  // G = 1 << lgG query heads per KV head
   int* status;         // device status word
 };
@@ -63,6 +64,7 @@ size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off
 int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* qt, void* coef,
                        void* stream);
 int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
+int launch_decode_int(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 int launch_backward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p);
 

@@ -368,3 +368,37 @@ def test_dalpha_error_scales_bound_the_sum():
     n_terms = sum(2 * 40 * 64 for s in o.interp_slots(base, 0.9, 2) if s["kind"] == "rung")
     assert abs(g["dalpha"]) <= g["dalpha_abs"]
     assert 0.0 < g["dalpha_rss"] <= g["dalpha_abs"] <= math.sqrt(n_terms) * g["dalpha_rss"] * (1 + 1e-12)
+
+
+def test_decode_is_the_forward_row_of_the_prefix():
+    """oracle.decode at position t equals row t of the oracle forward over the
+    prefix 0..t with the decode query placed at t (integer key set)."""
+    B, T, Hq, Hkv = 2, 40, 4, 2
+    x = si.make_qkvdo(B, T, Hq, Hkv, 8, "f32", seed=11, with_do=False)
+    dist = o.int_distances(o.fib_offsets(8), 1.0, 3)
+    pos = [39, 17]
+    qd = x["q"][:, :, 0].numpy().astype(np.float64)
+    O, L = o.decode(qd, x["k"], x["v"], pos, dist, 1e4)
+    for b, t in enumerate(pos):
+        qf = np.zeros((1, Hq, t + 1, 8))
+        qf[0, :, t] = qd[b]
+        Of, Lf = o.forward(qf, x["k"][b:b + 1, :, : t + 1], x["v"][b:b + 1, :, : t + 1],
+                           o.dist_slots(dist), 1e4)
+        np.testing.assert_allclose(O[b], Of[0, :, t], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L[b], Lf[0, :, t], rtol=0, atol=1e-12)
+
+
+def test_decode_dense_window_is_textbook_softmax():
+    """With every distance 0..t present and no RoPE, decode is plain causal
+    softmax attention of the last query over all cached rows (brute force)."""
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 2, 4))
+    k = rng.standard_normal((1, 1, 6, 4))
+    v = rng.standard_normal((1, 1, 6, 4))
+    O, L = o.decode(q, k, v, [5], list(range(6)), 0.0)
+    for h in range(2):
+        s = [float(np.dot(q[0, h], k[0, 0, j])) / 2.0 for j in range(6)]
+        w = [math.exp(x) for x in s]
+        want = sum(w[j] * v[0, 0, j] for j in range(6)) / sum(w)
+        np.testing.assert_allclose(O[0, h], want, rtol=0, atol=1e-12)
+        assert abs(L[0, h] - math.log(sum(w))) < 1e-12
