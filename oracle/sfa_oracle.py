@@ -413,3 +413,92 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
         out["dalpha_rss"] = float(math.sqrt(np.sum(f * f * dd_sq)))
         out["dtheta"] = dalpha * (alpha - 0.5) * (1.5 - alpha)
     return out
+
+
+# --------------------------------------------------------------------------
+# offset-schedule analysis and the shared power-law offset list
+# --------------------------------------------------------------------------
+
+
+def reach(dist_sets, T: int):
+    """Distances reached through a stack of causal shared-offset layers.
+
+    ("Christoffel-Balanced Sparse Attention": measure graph reachability
+    across layers, since a single periodic mask may leave residue classes
+    unreached; "Depth-Staggered ...": coverage through the stack.)  Layer l
+    lets position i read position i - s for s in dist_sets[l] (s >= 0).  After
+    layers 1..l, distance d is reached iff d = s_1 + ... + s_l with s_j in
+    dist_sets[j - 1] and d < T; before any layer only d = 0 is.
+
+    Returns (hops, covered): hops[d] = the smallest l >= 0 after which d is
+    reached (-1 if never within the stack), covered[l - 1] = the number of
+    distances < T reached after exactly layers 1..l.
+    """
+    R = {0}
+    hops = [-1] * T
+    hops[0] = 0
+    covered = []
+    for l, S in enumerate(dist_sets, start=1):
+        R = {r + s for r in R for s in S if r + s < T}
+        for d in R:
+            if hops[d] < 0:
+                hops[d] = l
+        covered.append(len(R))
+    return hops, covered
+
+
+def residue_classes(hops, M: int):
+    """Number of reached distances (hops >= 0) in each residue class mod M."""
+    out = [0] * M
+    for d, h in enumerate(hops):
+        if h >= 0:
+            out[d % M] += 1
+    return out
+
+
+def offset_histogram(dist, T: int, nb: int):
+    """Histogram of a distance set (duplicates counted once, d < T only) in
+    log2 bins: bin 0 = {0}; bin b = [2^(b-1), 2^b) for 1 <= b < nb - 1; the
+    last bin takes every d >= 2^(nb-2)."""
+    h = [0] * nb
+    for d in sorted(set(int(x) for x in dist)):
+        if d < 0 or d >= T:
+            continue
+        if d == 0:
+            b = 0
+        else:
+            b = min(nb - 1, d.bit_length())
+        h[b] += 1
+    return h
+
+
+def powerlaw_offsets(u, sigma: float, n: int):
+    """Shared power-law offset list ("Critical power-law sparse attention",
+    integration point: the fixed-degree approximation draws m distances from
+    q(d) = d^-(1+sigma) / sum_{v=1}^{floor(n/2)} v^-(1+sigma), d = 1..floor(n/2),
+    and deduplicates).  Here one draw serves every query (shared offsets,
+    causal keys i - d); u holds the m uniforms in [0, 1).
+
+    Inverse CDF in fp64: c_d = sum_{v<=d} v^-(1+sigma) summed in increasing v,
+    Z = c_{floor(n/2)}; draw j takes the smallest d with c_d > u_j * Z.
+    Returns the distinct distances, ascending.
+    """
+    Dmax = n // 2
+    c = []
+    acc = 0.0
+    for v in range(1, Dmax + 1):
+        acc += float(v) ** (-(1.0 + sigma))
+        c.append(acc)
+    Z = c[-1]
+    out = set()
+    for x in u:
+        t = float(x) * Z
+        lo, hi = 0, Dmax - 1  # smallest index with c[idx] > t
+        while lo < hi:
+            mid = (lo + hi) // 2
+            if c[mid] > t:
+                hi = mid
+            else:
+                lo = mid + 1
+        out.add(lo + 1)
+    return sorted(out)

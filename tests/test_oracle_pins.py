@@ -402,3 +402,70 @@ def test_decode_dense_window_is_textbook_softmax():
         want = sum(w[j] * v[0, 0, j] for j in range(6)) / sum(w)
         np.testing.assert_allclose(O[0, h], want, rtol=0, atol=1e-12)
         assert abs(L[0, h] - math.log(sum(w))) < 1e-12
+
+
+# ---- offset-schedule analysis and the shared power-law list ----------------
+
+
+def test_reach_dense_window_closed_form():
+    """L layers of the window {0..W}: d is reached after ceil(d / W) layers."""
+    T, W, L = 200, 5, 7
+    hops, covered = o.reach([list(range(W + 1))] * L, T)
+    for d in range(T):
+        want = -(-d // W) if -(-d // W) <= L else -1
+        assert hops[d] == want, d
+    assert covered == [min(T, l * W + 1) for l in range(1, L + 1)]
+
+
+def test_reach_powers_of_two_is_popcount():
+    """Layers {0, 1, 2, 4, ..., 2^k}: the fewest powers of two summing to d is
+    popcount(d), so hops[d] = popcount(d) (d < 2^(k+1), within the stack)."""
+    k, L = 6, 7
+    T = 1 << (k + 1)
+    S = [0] + [1 << j for j in range(k + 1)]
+    hops, _ = o.reach([S] * L, T)
+    for d in range(T):
+        assert hops[d] == bin(d).count("1"), d
+
+
+def test_reach_christoffel_residues():
+    """Christoffel m/k = 128/1024 offsets {7, 15, ..., 1023} with 0: one layer
+    reaches residues 0 and 7 mod 8 only; l layers reach residues
+    {0, -1, ..., -l} mod 8, so 7 layers reach every class."""
+    S = o.christoffel_offsets(128, 1024, include_zero=True)
+    T = 2048
+    for l in range(1, 9):
+        hops, _ = o.reach([S] * l, T)
+        cls = o.residue_classes(hops, 8)
+        reached = {r for r in range(8) if cls[r] > 0}
+        assert reached == {(-j) % 8 for j in range(l + 1)}, l
+
+
+def test_offset_histogram_log2_bins():
+    fib = [0, 1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 89, 5000]
+    assert o.offset_histogram(fib, 1024, 12) == [1, 1, 2, 1, 2, 1, 2, 1, 0, 0, 0, 0]
+    assert o.offset_histogram([0, 600, 1023], 1024, 4) == [1, 0, 0, 2]
+
+
+def test_powerlaw_extremes_and_invariants():
+    n = 1024
+    assert o.powerlaw_offsets([0.0], 0.8, n) == [1]
+    assert o.powerlaw_offsets([1.0 - 2.0 ** -53], 0.8, n) == [n // 2]
+    u = si.uniform(si.mix_seed(3, 1), 256)
+    d = o.powerlaw_offsets(u, 0.85, n)
+    assert d == sorted(set(d)) and 1 <= d[0] and d[-1] <= n // 2 and len(d) <= 256
+
+
+def test_powerlaw_frequencies_follow_the_law():
+    """Empirical frequencies of single draws match q(d) = d^-(1+s)/Z for the
+    first distances (within 5 standard deviations of a binomial count)."""
+    n, s, N = 1024, 0.8, 40000
+    u = si.uniform(si.mix_seed(4, 2), N)
+    Z = math.fsum(v ** -(1.0 + s) for v in range(1, n // 2 + 1))
+    counts = {}
+    for x in u:
+        dd = o.powerlaw_offsets([x], s, n)[0]
+        counts[dd] = counts.get(dd, 0) + 1
+    for dd in (1, 2, 3, 10):
+        p = dd ** -(1.0 + s) / Z
+        assert abs(counts.get(dd, 0) - N * p) <= 5 * math.sqrt(N * p * (1 - p)), dd
