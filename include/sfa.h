@@ -114,6 +114,43 @@ int sfa_rung_table(const int32_t* base, int32_t n_base, double alpha, int32_t W,
 int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t cap,
                       int32_t* n_out);
 
+/* ---- offset-schedule analysis and the shared power-law offset list ---- */
+
+/* Distances reached through a stack of causal shared-offset layers
+ * ("Christoffel-Balanced Sparse Attention": measure graph reachability
+ * across layers, a single periodic mask may leave residue classes
+ * unreached; "Depth-Staggered ...": coverage through the stack).  Layer l
+ * (0-based) reads distances dist[layer_start[l]] .. dist[layer_start[l+1]-1],
+ * each >= 0 (duplicates allowed).  After layers 1..l a distance d < T is
+ * reached iff it is a sum of one distance of each of those layers; before
+ * any layer only d = 0 is.  Writes hops[T]: the smallest l >= 0 after which
+ * d is reached, -1 if never within the L layers; and, if covered != NULL,
+ * covered[L]: the number of distances < T reached after exactly layers
+ * 1..l.  layer_start has L + 1 non-decreasing entries starting at 0.
+ * 1 <= L <= 4096, 1 <= T <= 2^24. */
+int sfa_reach(const int32_t* dist, const int32_t* layer_start, int32_t L, int32_t T, int32_t* hops,
+              int64_t* covered);
+
+/* out[r] = number of d < T with hops[d] >= 0 and d mod M == r; 1 <= M <= T. */
+int sfa_residue_classes(const int32_t* hops, int32_t T, int32_t M, int64_t* out);
+
+/* Log2-binned histogram of a distance set (each distinct d with 0 <= d < T
+ * counted once): bin 0 = {0}; bin b = [2^(b-1), 2^b) for 1 <= b < nb - 1;
+ * bin nb - 1 takes every d >= 2^(nb-2).  nb >= 2; out has nb entries. */
+int sfa_offset_histogram(const int32_t* dist, int32_t n, int32_t T, int32_t nb, int64_t* out);
+
+/* Shared power-law offsets ("Critical power-law sparse attention",
+ * integration point: m distances drawn from q(d) = d^-(1+sigma) /
+ * sum_{v=1}^{floor(n/2)} v^-(1+sigma), d = 1..floor(n/2), deduplicated; here
+ * one draw serves every query as causal keys i - d).  u holds the caller's m
+ * uniforms in [0, 1).  Inverse CDF in fp64: c_d = sum_{v<=d} v^-(1+sigma)
+ * in increasing v, Z = c_{floor(n/2)}; draw j is the smallest d with
+ * c_d > u_j * Z.  Writes the distinct distances ascending; *n_out is always
+ * set, SFA_ERR_CAPACITY (nothing written) if it exceeds cap.
+ * 1 <= m, 2 <= n <= 2^26, sigma >= 0, 0 <= u_j < 1. */
+int sfa_offsets_powerlaw(const double* u, int32_t m, double sigma, int32_t n, int32_t* out,
+                         int32_t cap, int32_t* n_out);
+
 const char* sfa_status_string(int status);
 
 /* ---- device entry points ------------------------------------------- */

@@ -72,6 +72,12 @@ def _lib():
                 "sfa_get_device_status": [_P, _I32P],
                 "sfa_forward_noalloc": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P],
                 "sfa_decode_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, _P],
+                "sfa_reach": [_I32P, _I32P, C.c_int32, C.c_int32, _I32P, C.POINTER(C.c_int64)],
+                "sfa_residue_classes": [_I32P, C.c_int32, C.c_int32, C.POINTER(C.c_int64)],
+                "sfa_offset_histogram": [_I32P, C.c_int32, C.c_int32, C.c_int32,
+                                         C.POINTER(C.c_int64)],
+                "sfa_offsets_powerlaw": [C.POINTER(C.c_double), C.c_int32, C.c_double, C.c_int32,
+                                         _I32P, C.c_int32, _I32P],
                 "sfa_timing_enable": [C.c_int],
                 "sfa_timing_read": [C.POINTER(C.c_double), C.POINTER(C.c_int64), C.c_int],
             }

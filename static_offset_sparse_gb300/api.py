@@ -63,6 +63,47 @@ def int_distances(dist) -> list[int]:
     return list(out[: nout.value])
 
 
+def reach(dist_sets, T: int):
+    """Reachability through a stack of layers (sfa_reach): returns hops (list
+    of T ints, -1 = never) and covered (one count per layer)."""
+    flat = [int(x) for S in dist_sets for x in S]
+    starts = [0]
+    for S in dist_sets:
+        starts.append(starts[-1] + len(S))
+    darr, _ = i32_array(flat)
+    sarr, _ = i32_array(starts)
+    L = len(dist_sets)
+    hops = (C.c_int32 * T)()
+    cov = (C.c_int64 * max(1, L))()
+    check(_lib().sfa_reach(darr, sarr, L, T, hops, cov), "sfa_reach")
+    return list(hops), list(cov[:L])
+
+
+def residue_classes(hops, M: int) -> list[int]:
+    harr, T = i32_array(hops)
+    out = (C.c_int64 * M)()
+    check(_lib().sfa_residue_classes(harr, T, M, out), "sfa_residue_classes")
+    return list(out)
+
+
+def offset_histogram(dist, T: int, nb: int) -> list[int]:
+    darr, n = i32_array(dist)
+    out = (C.c_int64 * nb)()
+    check(_lib().sfa_offset_histogram(darr, n, T, nb, out), "sfa_offset_histogram")
+    return list(out)
+
+
+def offsets_powerlaw(u, sigma: float, n: int) -> list[int]:
+    """Shared power-law distances for the uniforms u (sfa_offsets_powerlaw)."""
+    m = len(u)
+    uarr = (C.c_double * max(1, m))(*[float(x) for x in u])
+    out = (C.c_int32 * max(1, m))()
+    nout = C.c_int32(0)
+    check(_lib().sfa_offsets_powerlaw(uarr, m, float(sigma), int(n), out, max(1, m),
+                                      C.byref(nout)), "sfa_offsets_powerlaw")
+    return list(out[: nout.value])
+
+
 def status_string(code: int) -> str:
     return _lib().sfa_status_string(code).decode()
 
