@@ -171,8 +171,16 @@ def rung_slots(rungs) -> list[dict]:
 
 
 def dist_slots(dist) -> list[dict]:
-    """Integer path: one exact-gather slot per distance."""
+    """Integer path: one exact-gather slot per distance (negative = future key)."""
     return [{"kind": "win", "s": int(s)} for s in sorted(set(int(x) for x in dist))]
+
+
+def signed_christoffel_offsets(m: int, k: int) -> list[int]:
+    """Signed offsets for bidirectional attention ("Christoffel-Balanced
+    Sparse Attention": use signed offsets): the carry-word offsets O and
+    their negatives, with 0 (self) once."""
+    O = christoffel_offsets(m, k, include_zero=True)
+    return sorted(set(O) | {-x for x in O})
 
 
 def interp_slots(base, alpha: float, W: int) -> list[dict]:
@@ -221,8 +229,11 @@ def _slot_rows(kr, v, slots, T):
 
     kr, v: [T, D] (kr already rotated).  Returns Ks, Vs [n, T, D] and the
     validity mask [n, T].  Window / integer slot s: row t - s, valid iff
-    t >= s.  Rung (c, w): (1-w) row[t-c] + w row[t-c+1], valid iff t >= c
-    (i.e. d_k <= t; the rung is absent for earlier queries).
+    0 <= t - s < T (a negative s, from a signed offset list, reads the
+    future row t + |s|: "Christoffel-Balanced Sparse Attention", signed
+    offsets for bidirectional attention).  Rung (c, w): (1-w) row[t-c] +
+    w row[t-c+1], valid iff t >= c (i.e. d_k <= t; the rung is absent for
+    earlier queries).
     """
     n, D = len(slots), kr.shape[-1]
     Ks = np.zeros((n, T, D))
@@ -231,11 +242,16 @@ def _slot_rows(kr, v, slots, T):
     for a, sl in enumerate(slots):
         if sl["kind"] == "win":
             s = sl["s"]
-            if s >= T:
+            if abs(s) >= T:
                 continue
-            Ks[a, s:] = kr[: T - s]
-            Vs[a, s:] = v[: T - s]
-            ok[a, s:] = True
+            if s >= 0:
+                Ks[a, s:] = kr[: T - s]
+                Vs[a, s:] = v[: T - s]
+                ok[a, s:] = True
+            else:  # query t reads row t + |s| while it exists
+                Ks[a, : T + s] = kr[-s:]
+                Vs[a, : T + s] = v[-s:]
+                ok[a, : T + s] = True
         else:
             c, w = sl["c"], sl["w"]
             if c >= T:
@@ -382,10 +398,14 @@ def backward(q, k, v, do, slots, rope_theta: float = 1e4, alpha: float | None = 
         for a, sl in enumerate(slots):
             if sl["kind"] == "win":
                 s_ = sl["s"]
-                if s_ >= T:
+                if abs(s_) >= T:
                     continue
-                dk[b, g, : T - s_] += dKs[a, s_:]
-                dv[b, g, : T - s_] += dVs[a, s_:]
+                if s_ >= 0:
+                    dk[b, g, : T - s_] += dKs[a, s_:]
+                    dv[b, g, : T - s_] += dVs[a, s_:]
+                else:  # key row t + |s| collects from query t
+                    dk[b, g, -s_:] += dKs[a, : T + s_]
+                    dv[b, g, -s_:] += dVs[a, : T + s_]
             else:
                 c, w = sl["c"], sl["w"]
                 if c >= T:

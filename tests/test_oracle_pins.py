@@ -469,3 +469,60 @@ def test_powerlaw_frequencies_follow_the_law():
     for dd in (1, 2, 3, 10):
         p = dd ** -(1.0 + s) / Z
         assert abs(counts.get(dd, 0) - N * p) <= 5 * math.sqrt(N * p * (1 - p)), dd
+
+
+# ---- signed offsets (bidirectional) ------------------------------------------
+
+
+def test_signed_all_distances_is_full_softmax():
+    """Distances -(T-1)..T-1, no RoPE: every query attends every key, the
+    textbook full (non-causal) softmax attention, brute force."""
+    x = _inputs(1, 7, 2, 1, 4, 31)
+    O, L = o.forward(x["q"], x["k"], x["v"], o.dist_slots(range(-6, 7)), 0.0)
+    for h in range(2):
+        for t in range(7):
+            s = [float(np.dot(x["q"][0, h, t], x["k"][0, 0, j])) / 2.0 for j in range(7)]
+            m = max(s)
+            w = [math.exp(v - m) for v in s]
+            want = sum(w[j] * x["v"][0, 0, j] for j in range(7)) / sum(w)
+            np.testing.assert_allclose(O[0, h, t], want, rtol=0, atol=1e-12)
+            assert abs(L[0, h, t] - (m + math.log(sum(w)))) < 1e-12
+
+
+def test_signed_time_reversal():
+    """Without RoPE, reversing time maps distance s to -s: the forward of the
+    reversed sequences with the negated set is the reversed forward."""
+    x = _inputs(1, 20, 4, 2, 4, 33)
+    S = [-7, -3, 0, 1, 2, 5, 11]
+    O, L = o.forward(x["q"], x["k"], x["v"], o.dist_slots(S), 0.0)
+    rev = {n: x[n][:, :, ::-1].copy() for n in ("q", "k", "v")}
+    Or, Lr = o.forward(rev["q"], rev["k"], rev["v"], o.dist_slots([-s for s in S]), 0.0)
+    np.testing.assert_allclose(Or[:, :, ::-1], O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lr[:, :, ::-1], L, rtol=0, atol=1e-12)
+
+
+def test_signed_backward_central_fd():
+    """dQ, dK, dV with future keys against central differences of L = sum O dO."""
+    x = _inputs(1, 10, 4, 2, 4, 35)
+    slots = o.dist_slots([-4, -1, 0, 2, 3])
+    g = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    h = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv")):
+        arr = x[name]
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + h
+            lp = _loss(x, slots, 1e4, x["do"])
+            arr[idx] = old - h
+            lm = _loss(x, slots, 1e4, x["do"])
+            arr[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        err = np.abs(num - g[key]).max() / max(1.0, np.abs(num).max())
+        assert err < 1e-7, (name, err)
+
+
+def test_signed_christoffel_offsets():
+    S = o.signed_christoffel_offsets(128, 1024)
+    assert len(S) == 257 and S[127] == -7 and S[128] == 0 and S[129] == 7
+    assert S == sorted(set(S)) and all(-x in S for x in S)
