@@ -69,7 +69,8 @@ typedef struct {
   const int32_t* base;      /* host: base offsets f_k (> 0), n_base entries */
   int32_t n_base;
   /* integer path (sfa_forward_int / sfa_backward_int) */
-  const int32_t* dist;      /* host: key distances (>= 0), window included; duplicates allowed */
+  const int32_t* dist;      /* host: key distances, 0 and the window included; duplicates
+                             * allowed; a negative distance is a future key (signed set) */
   int32_t n_dist;
   /* RoPE: device table written by sfa_rope_table for at least T positions
    * with D = 64, or NULL for no rotation. */
@@ -110,7 +111,8 @@ int sfa_rung_table(const int32_t* base, int32_t n_base, double alpha, int32_t W,
                    int32_t* c_out, float* w_out, float* f_out, int32_t cap, int32_t* n_out);
 
 /* Sorted, de-duplicated integer distance set used by the integer path
- * (exposed for testing).  *n_out always set; SFA_ERR_CAPACITY if > cap. */
+ * (exposed for testing); |d| < 2^30.  *n_out always set; SFA_ERR_CAPACITY if
+ * > cap. */
 int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t cap,
                       int32_t* n_out);
 
@@ -195,8 +197,10 @@ int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v,
 /* Integer-offset fast path ("Depth-Staggered ...", method section: integer
  * offsets as an exact gather; "Christoffel-Balanced Sparse Attention": keys
  * i - o kept when >= 0).  Keys for query i: i - s for every s in d->dist
- * with s <= i.  Same outputs as sfa_forward / sfa_backward without the alpha
- * gradient. */
+ * with 0 <= i - s < T.  A negative s reads the future row i + |s| (signed
+ * offsets for bidirectional attention, same page); sets with negative
+ * distances run the fp32 SIMT kernels.  Same outputs as sfa_forward /
+ * sfa_backward without the alpha gradient. */
 int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
                     float* lse, void* ws, size_t ws_bytes, void* stream);
 int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void* v,
@@ -214,7 +218,8 @@ int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void
  *   o        [B, Hq, 64]     output (d->dtype)
  *   lse      fp32 [B, Hq]    natural-log softmax denominator, or NULL
  * Keys of sequence b: pos[b] - s for every s in d->dist with s <= pos[b]
- * (d->dist must contain 0).  With d->rope the query is rotated at pos[b] and
+ * (d->dist must contain 0 and no negative distance: a cache holds no future
+ * keys; SFA_ERR_INVALID_ARG otherwise).  With d->rope the query is rotated at pos[b] and
  * each gathered key at its own position.  The result is row pos[b] of
  * sfa_forward_int over that sequence's prefix, computed in fp32.  No
  * workspace.  A position outside [0, T) is skipped on the device and

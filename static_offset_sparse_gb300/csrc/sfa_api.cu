@@ -116,7 +116,15 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
   return status_ptr(&a->status);
 }
 
-static size_t forward_workspace_bytes(const sfa_desc* d) { return use_tc(d) ? kr_bytes(d) : 0; }
+// The tensor-core kernels serve causal key sets; a signed (bidirectional)
+// integer set, whose first rung distance is negative, runs the SIMT kernels.
+static bool tc_path(const sfa_desc* d, const Plan& p) {
+  return use_tc(d) && (p.n == 0 || p.c[0] >= 0);
+}
+
+static size_t forward_workspace_bytes(const sfa_desc* d, const Plan& p) {
+  return tc_path(d, p) ? kr_bytes(d) : 0;
+}
 
 static int forward_common(const sfa_desc* d, int interp, const void* q, const void* k,
                           const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
@@ -128,7 +136,7 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
-  const size_t need = forward_workspace_bytes(d);
+  const size_t need = forward_workspace_bytes(d, p);
   if (need && (!ws || !aligned16(ws))) return SFA_ERR_INVALID_ARG;
   if (ws_bytes < need) return SFA_ERR_CAPACITY;
   AttnArgs a;
@@ -138,7 +146,7 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   a.v = v;
   a.out_o = o;
   a.out_lse = lse;
-  if (!use_tc(d)) return launch_forward(a, p, d->dtype, stream);
+  if (!tc_path(d, p)) return launch_forward(a, p, d->dtype, stream);
   const void* kr = k;
   if (d->rope) {
     LaunchTimer tm(SFA_KERNEL_PREP, stream);
@@ -151,7 +159,7 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
 
 static size_t backward_bytes(const sfa_desc* d, const Plan& p) {
   size_t a, b, c;
-  return use_tc(d) ? backward_tc_workspace_bytes(d, p, &a, &b, &c) : backward_workspace_bytes(d, p);
+  return tc_path(d, p) ? backward_tc_workspace_bytes(d, p, &a, &b, &c) : backward_workspace_bytes(d, p);
 }
 
 static int backward_common(const sfa_desc* d, int interp, const void* q, const void* k,
@@ -183,7 +191,7 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
   a.dalpha_out = interp ? dadt : nullptr;
   a.dalpha_part = static_cast<double*>(ws);
   char* w = static_cast<char*>(ws);
-  if (use_tc(d)) {
+  if (tc_path(d, p)) {
     size_t okr, oqt, oco;
     backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco);
     const void* kr = k;
@@ -226,7 +234,7 @@ int sfa_workspace_size(const sfa_desc* d, int interp, int backward, size_t* byte
   Plan p;
   rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
   if (rc != SFA_OK) return rc;
-  *bytes = backward ? backward_bytes(d, p) : forward_workspace_bytes(d);
+  *bytes = backward ? backward_bytes(d, p) : forward_workspace_bytes(d, p);
   return SFA_OK;
 }
 
@@ -263,6 +271,7 @@ int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const 
     return SFA_ERR_INVALID_ARG;
   Plan p;
   if ((rc = build_int_plan(d, &p)) != SFA_OK) return rc;
+  if (p.n > 0 && p.c[0] < 0) return SFA_ERR_INVALID_ARG;  // a cache has no future keys
   AttnArgs a;
   if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
   a.q = q;

@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const AttnArgs a,
     __syncthreads();
     stage_rungs<TIO, INTERP>(Kb, Vb, rope, P, r0, nb, i0, TQ, a.T, sK, sV);
     __syncthreads();
-    for (int x = 0; x < nb; ++x) slot_update(active && i >= P.c[r0 + x], x * TQ + pl);
+    for (int x = 0; x < nb; ++x)
+      slot_update(active && i >= P.c[r0 + x] && i - P.c[r0 + x] < a.T, x * TQ + pl);
   }
 
   // dq' = sum dS k~ / 8 (the logit is q'.k~/8); dQ = R(-phi) dq'.  The
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kv_kernel(const AttnArgs a,
     __syncthreads();
     // query j + c: interpolates rows j (weight u) and j + 1 (weight w)
     {
-      const bool ok = active && j + c < a.T;
+      const bool ok = active && j + c >= 0 && j + c < a.T;
       const int r = (ok ? jl + 1 : 0) * G + hl;
       const float* q = sQ + r * kRowPad + hoff;
       const float* d = sD + r * kRowPad + hoff;

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const AttnArgs a,
         nb,
         [&](int x, int& row) {
           row = x * TQ + pl;
-          return active && i >= P.c[r0 + x];
+          return active && i >= P.c[r0 + x] && i - P.c[r0 + x] < a.T;
         },
         qr, sK, sV, sL, m, l, acc);
   }

@@ -112,7 +112,7 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
   if (!n_out || n_dist < 0 || (n_dist > 0 && !dist)) return SFA_ERR_INVALID_ARG;
   std::vector<int32_t> s(dist, dist + n_dist);
   for (int32_t x : s)
-    if (x < 0) return SFA_ERR_INVALID_ARG;
+    if (x <= -(1 << 30) || x >= (1 << 30)) return SFA_ERR_INVALID_ARG;
   std::sort(s.begin(), s.end());
   s.erase(std::unique(s.begin(), s.end()), s.end());
   *n_out = (int32_t)s.size();
@@ -173,20 +173,24 @@ int build_int_plan(const sfa_desc* d, Plan* p) {
   s.resize((size_t)n);
   // Distance 0 (the query itself) must be present so that no query has an
   // empty key set, as the window of the method guarantees.
-  if (s.empty() || s[0] != 0) return SFA_ERR_INVALID_ARG;
-  // The contiguous prefix 0..W runs as a window; the rest are exact rungs.
+  const size_t z = (size_t)(std::lower_bound(s.begin(), s.end(), 0) - s.begin());
+  if (z == s.size() || s[z] != 0) return SFA_ERR_INVALID_ARG;
+  // The contiguous run 0..W runs as a window; every other distance is an
+  // exact rung, ascending: negative ones (future keys of a signed,
+  // bidirectional set) first, then those beyond the window.
   int32_t W = -1;
-  size_t j = 0;
+  size_t j = z;
   while (j < s.size() && s[j] == W + 1) {
     ++W;
     ++j;
   }
-  if (s.size() - j > (size_t)kMaxRungs) return SFA_ERR_UNSUPPORTED;
+  const size_t nr = z + (s.size() - j);
+  if (nr > (size_t)kMaxRungs) return SFA_ERR_UNSUPPORTED;
   p->W = W;
-  p->n = (int32_t)(s.size() - j);
+  p->n = (int32_t)nr;
   p->interp = 0;
-  for (int32_t r = 0; r < p->n; ++r) {
-    p->c[r] = s[j + r];
+  for (size_t r = 0; r < nr; ++r) {
+    p->c[r] = r < z ? s[r] : s[j + (r - z)];
     p->w[r] = 0.0f;
     p->f[r] = 0.0f;
   }

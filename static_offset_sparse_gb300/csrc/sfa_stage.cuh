@@ -46,7 +46,7 @@ __device__ __forceinline__ void stage_rungs(const TIO* Kb, const TIO* Vb, const 
     const int rr = rem >> 2, pc = rem & 3;
     const int iq = i0 + rr;
     const int p0 = iq - P.c[r0 + a];
-    if (iq >= T || p0 < 0) continue;  // rung absent for this query
+    if (iq >= T || p0 < 0 || p0 >= T) continue;  // rung absent for this query
     float* dk = sK + (a * TQ + rr) * kRowPad;
     float* dv = sV + (a * TQ + rr) * kRowPad;
     float klo[8], khi[8], vlo[8], vhi[8];

@@ -106,3 +106,13 @@ def test_descriptor_validation_without_gpu(sfa_lib):
     dist = (C.c_int32 * 2)(3, 5)  # distance 0 missing: a query could have no key
     d.dist, d.n_dist = C.cast(dist, C.POINTER(C.c_int32)), 2
     assert sfa_lib.sfa_workspace_size(C.byref(d), 0, 1, C.byref(size)) == 1
+
+
+def test_int_distances_accept_signed_sets(sfa_lib):
+    import static_offset_sparse_gb300 as s
+    from static_offset_sparse_gb300 import SfaError
+
+    d = [5, -3, 0, -3, 1, -40, 5]
+    assert s.int_distances(d) == sorted(set(d))
+    with pytest.raises(SfaError):
+        s.int_distances([0, 1 << 30])
