@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2 + (gid >> 2);
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
+  const int colrow2 = 4 * warp + ((((lane & 7) >> 1) + 2) & 3) + (lane & 1);
 
   const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a.status,
                               [&](int grp, uint32_t kst, uint32_t vst) {
@@ -156,41 +157,47 @@ __global__ void __launch_bounds__(kTcThreads, 4)
       sa[3] = pack_bf16(ds[1][2], ds[1][3]);
       pv_tile(sa, kst, 4 * warp + (lane & 7), 4 * warp + 8 + (lane & 7), dq);
     } else {
+      // rung pair; box 1's B columns rotate positions by two, so the lane of
+      // position p holding a rung's raw pair is tig == p (box 0) or
+      // tig == p + 2 (box 1): one pass of the per-rung work serves both
       const int r0 = 2 * (grp - nwc);
-      float ds[2][2], wgt[2];
+      float sc0[4] = {0, 0, 0, 0}, dp0[4] = {0, 0, 0, 0}, sc1[4] = {0, 0, 0, 0}, dp1[4] = {0, 0, 0, 0};
+      qk_tile(qa, kst, colrow, sc0);
+      qk_tile(da, vst, colrow, dp0);
+      qk_tile(qa, kst, kTcBoxRows + colrow2, sc1);
+      qk_tile(da, vst, kTcBoxRows + colrow2, dp1);
+      const bool own0 = tig == p, own1 = tig == ((p + 2) & 3);
+      const int rg = own1 ? r0 + 1 : r0;
+      const float w0 = (INTERP && r0 < nr) ? P.w[r0] : 0.0f;
+      const float w1 = (INTERP && r0 + 1 < nr) ? P.w[r0 + 1] : 0.0f;
+      const float f0 = (INTERP && r0 < nr) ? P.f[r0] : 0.0f;
+      const float f1 = (INTERP && r0 + 1 < nr) ? P.f[r0 + 1] : 0.0f;
+      const float w = own1 ? w1 : w0, f = own1 ? f1 : f0;
+      const bool v = act && (own0 || own1) && rg < nr && i >= P.c[min(rg, P.n - 1)];
+      float ds[2], prr[2];
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const int rg = r0 + x;
-        float sc[4] = {0, 0, 0, 0}, dp[4] = {0, 0, 0, 0};
-        const int row = x * kTcBoxRows + colrow;
-        qk_tile(qa, kst, row, sc);
-        qk_tile(da, vst, row, dp);
-        const bool v = act && rg < nr && p == tig && i >= P.c[rg];
-        const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
-        const float f = (INTERP && rg < nr) ? P.f[rg] : 0.0f;
-        wgt[x] = w;
-        float prr[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float s = fmaf(w, sc[2 * r + 1], (1.0f - w) * sc[2 * r]);
-          const float dpi = fmaf(w, dp[2 * r + 1], (1.0f - w) * dp[2 * r]);
-          const float pr = v ? ex2(fmaf(s, kLog2e, -lse2[r])) : 0.0f;
-          const float d = pr * (dpi - delta[r]);
-          ds[r][x] = d;
-          prr[r] = pr;
-          if (INTERP && v)
-            dacc = fmaf(f, fmaf(d, sc[2 * r] - sc[2 * r + 1], pr * (dp[2 * r] - dp[2 * r + 1])), dacc);
-        }
-        if (v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
-          write_coef_half(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, ds[0][x], ds[1][x], prr[0], prr[1]);
-          write_coef_half(crow + 2 * (P.W + 2 + 2 * rg), w, ds[0][x], ds[1][x], prr[0], prr[1]);
-        }
+      for (int r = 0; r < 2; ++r) {
+        const float a0 = own1 ? sc1[2 * r] : sc0[2 * r], a1 = own1 ? sc1[2 * r + 1] : sc0[2 * r + 1];
+        const float b0 = own1 ? dp1[2 * r] : dp0[2 * r], b1 = own1 ? dp1[2 * r + 1] : dp0[2 * r + 1];
+        const float sr = fmaf(w, a1, (1.0f - w) * a0);
+        const float dpi = fmaf(w, b1, (1.0f - w) * b0);
+        const float pr = v ? ex2(fmaf(sr, kLog2e, -lse2[r])) : 0.0f;
+        const float d = pr * (dpi - delta[r]);
+        ds[r] = d;
+        prr[r] = pr;
+        if (INTERP && v) dacc = fmaf(f, fmaf(d, a0 - a1, pr * (b0 - b1)), dacc);
       }
-      sa[0] = pack_bf16(ds[0][0] * (1.0f - wgt[0]), ds[0][0] * wgt[0]);
-      sa[1] = pack_bf16(ds[1][0] * (1.0f - wgt[0]), ds[1][0] * wgt[0]);
-      sa[2] = pack_bf16(ds[0][1] * (1.0f - wgt[1]), ds[0][1] * wgt[1]);
-      sa[3] = pack_bf16(ds[1][1] * (1.0f - wgt[1]), ds[1][1] * wgt[1]);
-      pv_tile(sa, kst, colrow, kTcBoxRows + colrow, dq);
+      if (v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
+        write_coef_half(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, ds[0], ds[1], prr[0], prr[1]);
+        write_coef_half(crow + 2 * (P.W + 2 + 2 * rg), w, ds[0], ds[1], prr[0], prr[1]);
+      }
+      const uint32_t lo = pack_bf16(ds[0] * (1.0f - w), ds[0] * w);
+      const uint32_t hi = pack_bf16(ds[1] * (1.0f - w), ds[1] * w);
+      sa[0] = own1 ? 0u : lo;  // k 0..7: box 0 (zero when the lane owns neither)
+      sa[1] = own1 ? 0u : hi;
+      sa[2] = own1 ? lo : 0u;  // k 8..15: box 1
+      sa[3] = own1 ? hi : 0u;
+      pv_tile(sa, kst, colrow, kTcBoxRows + colrow2, dq);
     }
   });
   if (!ok) return;
