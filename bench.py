@@ -10,6 +10,11 @@ independently drawn Q, K, V, dO (N(0, 1), seeded), so each step streams
 16 distinct layers' tensors (2.6 GB, far above the 129 MB L2: no L2 flush is
 needed between steps).
 
+The timed region replays the step captured as one CUDA graph (single rank;
+multi-rank runs time the eager step with its all-reduce); a separate eager
+pass with CUDA events around every library launch gives the per-kernel times
+behind the roofline, and the eager step without those events is reported too.
+
 Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
 bounded sample of the same workload instead.  ``--mode decode`` measures the
 integer-path decode step instead (one new token per sequence through the
@@ -264,29 +269,57 @@ def gpu_arm(args, rank, world, dev):
         step()
     torch.cuda.synchronize()
     assert sfa.get_device_status() == 0
-
-    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    clocks.start()
-    sfa.timing_enable(True)
-    sfa.timing_read()  # drop anything recorded before the timed region
-    barrier()
-    torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+
+    def timed(run, n):
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(n):
+            run()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return ev0.elapsed_time(ev1) / n
+
+    # 1) per-kernel breakdown for the roofline: library events around every
+    #    launch (they add gaps, so this pass does not give the headline)
+    n_k = min(args.steps, 20)
+    sfa.timing_enable(True)
+    sfa.timing_read()  # drop anything recorded before
+    timed(step, n_k)
     kt = sfa.timing_read()
     sfa.timing_enable(False)
+    # 2) eager step without events (one host call per layer and direction)
+    ms_eager = timed(step, min(args.steps, 50))
+    # 3) headline: the step as one CUDA graph (single rank; the multi-rank
+    #    step keeps its all-reduce eager)
+    run = step
+    graphed = world == 1
+    if graphed:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cs = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+            for L in layers:
+                L.run(cs)
+        run = graph.replay
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    ms = timed(run, args.steps)
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    assert sfa.get_device_status() == 0
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    launches = int(sum(c for _, c in kt.values()))
+    per_step_launches = sum(c for _, c in kt.values()) / n_k
+    launches = int(round(per_step_launches * args.steps))
+    kt = {k: (v[0] / n_k * args.steps, v[1] / n_k * args.steps) for k, v in kt.items()}
 
     # roofline of the dominant kernel (largest summed device time), HBM view:
     # algorithmic bytes per launch / mean launch time vs the measured copy peak
@@ -306,7 +339,10 @@ def gpu_arm(args, rank, world, dev):
                 "peak_source": src, "algorithmic_bytes_per_launch": bytes_per_launch,
                 "per_launch_ms": round(per_launch_ms, 4),
                 "useful_tflops": round(useful_tflops, 2),
-                "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kt.items() if v[1]}}
+                "kernel_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kt.items() if v[1]},
+                "kernel_times": f"CUDA events around each launch, eager pass of {n_k} steps"}
+    roofline["step_modes"] = {"headline": "CUDA graph of the 16-layer step" if graphed else "eager",
+                              "eager_ms_per_step": round(ms_eager, 4)}
     return layers, ms, clk, launches, roofline
 
 
