@@ -218,10 +218,16 @@ class Layer:
         self.dk = torch.empty_like(x["k"])
         self.dv = torch.empty_like(x["v"])
         self.dadt = torch.zeros((2,), dtype=torch.float64, device=dev)
-        self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha, base=FIB, rope_theta=ROPE)
-        self.nws = max(sfa.workspace_size(self.desc, True, True), sfa.workspace_size(self.desc, True, False))
+        # the layer's rotated keys: one rotation per step serves forward and
+        # backward (kept like a saved activation)
+        self.k_rot = torch.empty_like(x["k"])
+        self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha, base=FIB, rope_theta=ROPE,
+                                  k_rot=self.k_rot)
+        self.nws = max(1, sfa.workspace_size(self.desc, True, True),
+                       sfa.workspace_size(self.desc, True, False))
         self.ws = torch.empty((self.nws,), dtype=torch.uint8, device=dev)
         P = lambda t: C.c_void_p(t.data_ptr())  # noqa: E731
+        self.rargs = (C.byref(self.desc), P(x["k"]), P(self.k_rot))
         self.fargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse),
                       P(self.ws), self.nws)
         self.bargs = (C.byref(self.desc), P(x["q"]), P(x["k"]), P(x["v"]), P(self.o), P(self.lse),
@@ -230,7 +236,8 @@ class Layer:
         self.lib = lib
 
     def run(self, stream):
-        rc = self.lib.sfa_forward(*self.fargs, stream)
+        rc = self.lib.sfa_rope_keys(*self.rargs, stream)
+        rc = rc or self.lib.sfa_forward(*self.fargs, stream)
         rc = rc or self.lib.sfa_backward(*self.bargs, stream)
         if rc:
             raise RuntimeError(f"libsfa status {rc}")

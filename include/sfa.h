@@ -75,6 +75,12 @@ typedef struct {
   /* RoPE: device table written by sfa_rope_table for at least T positions
    * with D = 64, or NULL for no rotation. */
   const float* rope;
+  /* Optional device [B, Hkv, T, 64] bf16: the rotated keys sfa_rope_keys wrote
+   * for this k and this rope table, or NULL.  Calls that run the tensor-core
+   * kernels (bf16 I/O, G = 4, no negative distance) then read it instead of
+   * rotating K into their workspace (which shrinks accordingly), so one
+   * rotation serves a layer's forward and backward.  Ignored otherwise. */
+  const void* k_rot;
 } sfa_desc;
 
 /* ---- host builders (no GPU needed) ---------------------------------- */
@@ -165,6 +171,11 @@ int sfa_rope_table_bytes(int32_t T, size_t* bytes);
  * stored fp32, laid out [T][32][2] = (cos, sin).  Rotation pairs are
  * (j, j + 32) ("rotate half").  theta > 0. */
 int sfa_rope_table(int32_t T, double theta, float* table, void* stream);
+
+/* RoPE-rotated keys for d->k_rot: writes k_rot [B, Hkv, T, 64] = k rotated
+ * at each row's position by d->rope (fp32 rotation, one bf16 rounding).
+ * bf16 only (SFA_ERR_UNSUPPORTED otherwise); d->rope must be set. */
+int sfa_rope_keys(const sfa_desc* d, const void* k, void* k_rot, void* stream);
 
 /* Workspace bytes a call needs: interp != 0 for sfa_forward / sfa_backward,
  * 0 for the integer path; backward != 0 for the backward calls.  The forward

@@ -8,7 +8,7 @@ from ._lib import (LIB_PATH, MAX_RUNGS, SCHED_COPRIME, SCHED_FIXED, SCHED_LINEAR
 from .api import (alpha_schedule, backward, backward_int, decode_int, forward, forward_int,
                   get_device_status, int_distances, make_desc, offset_histogram,
                   offsets_christoffel, offsets_fib, offsets_pow2, offsets_powerlaw, reach,
-                  residue_classes, rope_table, rung_table, status_string, timing_enable,
+                  residue_classes, rope_keys, rope_table, rung_table, status_string, timing_enable,
                   timing_read, workspace_size)
 
 __all__ = [
@@ -16,6 +16,6 @@ __all__ = [
     "SFA_F32", "SfaError", "alpha_schedule", "backward", "backward_int", "decode_int", "forward",
     "forward_int", "get_device_status", "int_distances", "make_desc", "offsets_christoffel",
     "offset_histogram", "offsets_fib", "offsets_pow2", "offsets_powerlaw", "reach",
-    "residue_classes", "rope_table", "rung_table", "status_string",
+    "residue_classes", "rope_keys", "rope_table", "rung_table", "status_string",
     "workspace_size", "timing_enable", "timing_read",
 ]

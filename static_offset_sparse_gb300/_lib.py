@@ -32,7 +32,7 @@ class Desc(C.Structure):
         ("D", C.c_int32), ("dtype", C.c_int32), ("W", C.c_int32), ("alpha", C.c_double),
         ("base", C.POINTER(C.c_int32)), ("n_base", C.c_int32),
         ("dist", C.POINTER(C.c_int32)), ("n_dist", C.c_int32),
-        ("rope", C.c_void_p),
+        ("rope", C.c_void_p), ("k_rot", C.c_void_p),
     ]
 
 
@@ -72,6 +72,7 @@ def _lib():
                 "sfa_get_device_status": [_P, _I32P],
                 "sfa_forward_noalloc": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P],
                 "sfa_decode_int": [C.POINTER(Desc), _P, _P, _P, _P, _P, _P, _P],
+                "sfa_rope_keys": [C.POINTER(Desc), _P, _P, _P],
                 "sfa_reach": [_I32P, _I32P, C.c_int32, C.c_int32, _I32P, C.POINTER(C.c_int64)],
                 "sfa_residue_classes": [_I32P, C.c_int32, C.c_int32, C.POINTER(C.c_int64)],
                 "sfa_offset_histogram": [_I32P, C.c_int32, C.c_int32, C.c_int32,

@@ -156,7 +156,7 @@ def _check_tensor(t, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def make_desc(q, k, *, W=0, alpha=1.0, base=(), dist=(), rope_theta=1e4):
+def make_desc(q, k, *, W=0, alpha=1.0, base=(), dist=(), rope_theta=1e4, k_rot=None):
     """Build the sfa_desc for k [B,Hkv,T,64] and q [B,Hq,...] (Hq and the
     dtype are taken from q).  Keeps the host arrays alive on the returned
     object."""
@@ -178,6 +178,8 @@ def make_desc(q, k, *, W=0, alpha=1.0, base=(), dist=(), rope_theta=1e4):
     else:
         d.rope = None
         d._keep = (barr, darr)
+    d.k_rot = C.c_void_p(k_rot.data_ptr()) if k_rot is not None else None
+    d._keep = d._keep + ((k_rot,) if k_rot is not None else ())
     return d
 
 
@@ -215,15 +217,16 @@ def _fwd(fn, name, interp, q, k, v, desc, o=None, lse=None, ws=None):
 
 
 def forward(q, k, v, *, W: int, alpha: float, base, rope_theta: float = 1e4, o=None, lse=None,
-            ws=None):
-    """Interpolated path: window 0..W plus rungs alpha*f for f in base."""
-    desc = make_desc(q, k, W=W, alpha=alpha, base=base, rope_theta=rope_theta)
+            ws=None, k_rot=None):
+    """Interpolated path: window 0..W plus rungs alpha*f for f in base.  k_rot:
+    optional rotated keys from rope_keys (skips the call's own rotation)."""
+    desc = make_desc(q, k, W=W, alpha=alpha, base=base, rope_theta=rope_theta, k_rot=k_rot)
     return _fwd(_lib().sfa_forward, "sfa_forward", True, q, k, v, desc, o, lse, ws)
 
 
-def forward_int(q, k, v, *, dist, rope_theta: float = 1e4, o=None, lse=None, ws=None):
+def forward_int(q, k, v, *, dist, rope_theta: float = 1e4, o=None, lse=None, ws=None, k_rot=None):
     """Integer path: keys i - s for s in dist (0 required)."""
-    desc = make_desc(q, k, dist=dist, rope_theta=rope_theta)
+    desc = make_desc(q, k, dist=dist, rope_theta=rope_theta, k_rot=k_rot)
     return _fwd(_lib().sfa_forward_int, "sfa_forward_int", False, q, k, v, desc, o, lse, ws)
 
 
@@ -249,15 +252,25 @@ def _bwd(interp, q, k, v, o, lse, do, desc, dq=None, dk=None, dv=None, ws=None, 
     return dq, dk, dv
 
 
-def backward(q, k, v, o, lse, do, *, W: int, alpha: float, base, rope_theta: float = 1e4, **out):
+def backward(q, k, v, o, lse, do, *, W: int, alpha: float, base, rope_theta: float = 1e4,
+             k_rot=None, **out):
     """Returns dq, dk, dv and a device float64 [2] tensor (dL/dalpha, dL/dtheta)."""
-    desc = make_desc(q, k, W=W, alpha=alpha, base=base, rope_theta=rope_theta)
+    desc = make_desc(q, k, W=W, alpha=alpha, base=base, rope_theta=rope_theta, k_rot=k_rot)
     return _bwd(True, q, k, v, o, lse, do, desc, **out)
 
 
-def backward_int(q, k, v, o, lse, do, *, dist, rope_theta: float = 1e4, **out):
-    desc = make_desc(q, k, dist=dist, rope_theta=rope_theta)
+def backward_int(q, k, v, o, lse, do, *, dist, rope_theta: float = 1e4, k_rot=None, **out):
+    desc = make_desc(q, k, dist=dist, rope_theta=rope_theta, k_rot=k_rot)
     return _bwd(False, q, k, v, o, lse, do, desc, **out)
+
+
+def rope_keys(k, rope_theta: float = 1e4, out=None):
+    """Rotated keys for the k_rot argument (sfa_rope_keys; bf16)."""
+    _check_tensor(k, "k")
+    desc = make_desc(k, k, rope_theta=rope_theta)
+    out = _torch().empty_like(k) if out is None else out
+    check(_lib().sfa_rope_keys(C.byref(desc), _ptr(k), _ptr(out), _stream()), "sfa_rope_keys")
+    return out
 
 
 def decode_int(q, k_cache, v_cache, pos, *, dist, rope_theta: float = 1e4, o=None, lse=None):

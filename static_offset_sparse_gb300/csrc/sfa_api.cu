@@ -113,6 +113,7 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
   a->rope = d->rope;
   a->alpha = d->alpha;
   if (d->rope && !aligned16(d->rope)) return SFA_ERR_INVALID_ARG;
+  if (d->k_rot && !aligned16(d->k_rot)) return SFA_ERR_INVALID_ARG;
   return status_ptr(&a->status);
 }
 
@@ -148,7 +149,9 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   a.out_lse = lse;
   if (!tc_path(d, p)) return launch_forward(a, p, d->dtype, stream);
   const void* kr = k;
-  if (d->rope) {
+  if (d->rope && d->k_rot) {
+    kr = d->k_rot;
+  } else if (d->rope) {
     LaunchTimer tm(SFA_KERNEL_PREP, stream);
     rc = launch_rope_prep(k, d->rope, ws, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
     if (rc != SFA_OK) return rc;
@@ -195,7 +198,9 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
     size_t okr, oqt, oco;
     backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco);
     const void* kr = k;
-    if (d->rope) {
+    if (d->rope && d->k_rot) {
+      kr = d->k_rot;
+    } else if (d->rope) {
       LaunchTimer tm(SFA_KERNEL_PREP, stream);
       rc = launch_rope_prep(k, d->rope, w + okr, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
       if (rc != SFA_OK) return rc;
@@ -259,6 +264,16 @@ int sfa_backward_int(const sfa_desc* d, const void* q, const void* k, const void
                      const void* o, const float* lse, const void* dO, void* dq, void* dk,
                      void* dv, void* ws, size_t ws_bytes, void* stream) {
   return backward_common(d, 0, q, k, v, o, lse, dO, dq, dk, dv, nullptr, ws, ws_bytes, stream);
+}
+
+int sfa_rope_keys(const sfa_desc* d, const void* k, void* k_rot, void* stream) {
+  int rc = validate_shape(d);
+  if (rc != SFA_OK) return rc;
+  if (d->dtype != SFA_BF16) return SFA_ERR_UNSUPPORTED;
+  if (!k || !k_rot || !d->rope || !aligned16(k) || !aligned16(k_rot) || !aligned16(d->rope))
+    return SFA_ERR_INVALID_ARG;
+  LaunchTimer tm(SFA_KERNEL_PREP, stream);
+  return launch_rope_prep(k, d->rope, k_rot, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
 }
 
 int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const void* v_cache,

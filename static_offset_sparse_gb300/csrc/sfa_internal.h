@@ -54,8 +54,10 @@ struct AttnArgs {
 // fp32 SIMT kernels.
 inline bool use_tc(const sfa_desc* d) { return d->dtype == SFA_BF16 && d->Hq == 4 * d->Hkv; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+// Workspace for the rotated keys the tensor-core kernels read (none when the
+// caller supplies them in d->k_rot, or without RoPE).
 inline size_t kr_bytes(const sfa_desc* d) {
-  return d->rope ? align256((size_t)d->B * d->Hkv * d->T * 64 * 2) : 0;
+  return d->rope && !d->k_rot ? align256((size_t)d->B * d->Hkv * d->T * 64 * 2) : 0;
 }
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream);
 int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream);

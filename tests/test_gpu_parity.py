@@ -173,3 +173,26 @@ def test_errors_leave_outputs_untouched(sfa):
         sfa.forward(q, k, k, W=-1, alpha=1.0, base=[1, 2], o=o_)
     torch.cuda.synchronize()
     assert (o_ == 3.0).all()
+
+
+def test_k_rot_reuse_is_bit_identical(sfa):
+    """Passing the rotated keys of rope_keys (one rotation per layer) gives the
+    same bits as the calls' own rotation, and shrinks their workspaces."""
+    import torch
+
+    x = si.make_qkvdo(2, 150, 8, 2, 64, "bf16", seed=61)
+    d = {n: t.cuda() for n, t in x.items()}
+    base = o.fib_offsets(12)
+    kr = sfa.rope_keys(d["k"])
+    O1, L1 = sfa.forward(d["q"], d["k"], d["v"], W=8, alpha=0.9, base=base)
+    O2, L2 = sfa.forward(d["q"], d["k"], d["v"], W=8, alpha=0.9, base=base, k_rot=kr)
+    g1 = sfa.backward(d["q"], d["k"], d["v"], O1, L1, d["do"], W=8, alpha=0.9, base=base)
+    g2 = sfa.backward(d["q"], d["k"], d["v"], O2, L2, d["do"], W=8, alpha=0.9, base=base, k_rot=kr)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    d1 = sfa.make_desc(d["q"], d["k"], W=8, alpha=0.9, base=base)
+    d2 = sfa.make_desc(d["q"], d["k"], W=8, alpha=0.9, base=base, k_rot=kr)
+    assert sfa.workspace_size(d2, True, False) == 0 < sfa.workspace_size(d1, True, False)
+    assert sfa.workspace_size(d2, True, True) < sfa.workspace_size(d1, True, True)
