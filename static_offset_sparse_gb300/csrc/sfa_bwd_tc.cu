@@ -12,9 +12,9 @@
 //   the pair (P, dS) as a key-side-ready record (bf16 hi + lo; a rung gets
 //   one record per role: weight 1 - w for key i - c, w for key i - c + 1).
 // bwd_kv_tc (per key tile): dK^T and dV^T accumulate as [64 dims x 8 keys]
-//   mma tiles per warp: A = q~^T or dO^T of the (query, head) pairs that
-//   (staged by TMA)
-//   read the warp's 8 key rows, B = their (dS, P) coefficients: a window
+//   mma tiles per warp: A = q~^T or dO^T (TMA-staged slabs) of the (query,
+//   head) pairs that read the warp's 8 key rows, B = their (dS, P)
+//   coefficients (the records, also TMA-staged): a window
 //   slot s reaches key i - s; a rung (c, w) reaches key i - c with weight
 //   1 - w and key i - c + 1 with weight w.  Each key row is written by one
 //   warp: no atomics.
@@ -487,14 +487,17 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   cudaStream_t s = (cudaStream_t)stream;
   const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
-  CUtensorMap mk, mv, mq, md, mqr, mdr, mcw, mcr, mq36, mdo36, mo36, mqt32, mdq32;
+  // query side: Q / dO / O tile loads (20-row boxes), q~ and dQ tile stores
+  // (16-row boxes); key side: q~ and dO slabs (42 rows for a window chunk,
+  // 34 for a rung) and the record boxes
+  CUtensorMap mk, mv, mq, md, mqr, mdr, mcw, mcr, tq, tdo, to, sqt, sdq;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
-      make_rows_map(&mq36, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
-      make_rows_map(&mdo36, a.dO, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
-      make_rows_map(&mo36, a.o, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
-      make_rows_map(&mqt32, qt, qplanes, a.T, kTcORows, 4) != SFA_OK ||
-      make_rows_map(&mdq32, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
+      make_rows_map(&tq, a.q, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&tdo, a.dO, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&to, a.o, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
+      make_rows_map(&sqt, qt, qplanes, a.T, kTcORows, 4) != SFA_OK ||
+      make_rows_map(&sdq, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&mqr, qt, qplanes, a.T, kKvQR, 4) != SFA_OK ||
@@ -515,7 +518,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   if (cudaMemsetAsync(ticket, 0, sizeof(unsigned), s) != cudaSuccess) return SFA_ERR_CUDA;
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
-    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, mq36, mdo36, mo36, mqt32, mdq32,
+    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, tq, tdo, to, sqt, sdq,
                                            static_cast<uint4*>(coef), NS, ticket, p);
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));

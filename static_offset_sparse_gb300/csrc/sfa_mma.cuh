@@ -1,4 +1,4 @@
-// Warp-level tensor-core and async-copy helpers (inline PTX, sm_103a).
+// Warp-level tensor-core helpers (inline PTX, sm_103a).
 //
 // mma.sync m16n8k16 bf16 -> fp32 fragment layouts used throughout (lane =
 // 4 * gid + tig, gid = lane >> 2, tig = lane & 3):
@@ -20,16 +20,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // 16-byte async global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"

@@ -28,51 +28,6 @@ constexpr int kTcStageB = 2 * kTcRegionB;
 constexpr int kTcStages = 2;
 constexpr int kTcWC = 12;                     // window distances per chunk
 
-// q' fragments of a warp's 16 rows: rows gid (head gid>>2) and gid+8 (head
-// 2 + (gid>>2)), position i, scaled by `scale`; RoPE pairs (d, d + 32) sit in
-// k-steps kk and kk + 2 of the same lane.
-__device__ __forceinline__ void load_q_frags(const bf16* q0, const bf16* q1, const float2* rope,
-                                             int i, float scale, uint32_t (*qa)[4]) {
-  const int tig = threadIdx.x & 3;
-  float x[2][4][4];  // [row][kk][e]: e = dims 2tig, 2tig+1, 2tig+8, 2tig+9 of k-step kk
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const bf16* q = rr ? q1 : q0;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const float2 u = unpack_bf16(*reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig));
-      const float2 v = unpack_bf16(*reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig + 8));
-      x[rr][kk][0] = u.x;
-      x[rr][kk][1] = u.y;
-      x[rr][kk][2] = v.x;
-      x[rr][kk][3] = v.y;
-    }
-  }
-  if (rope) {
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig + 8));
-      const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float lo = x[rr][kk][e], hi = x[rr][kk + 2][e];
-          x[rr][kk][e] = lo * cs[e] - hi * sn[e];
-          x[rr][kk + 2][e] = lo * sn[e] + hi * cs[e];
-        }
-    }
-  }
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    qa[kk][0] = pack_bf16(x[0][kk][0] * scale, x[0][kk][1] * scale);
-    qa[kk][1] = pack_bf16(x[1][kk][0] * scale, x[1][kk][1] * scale);
-    qa[kk][2] = pack_bf16(x[0][kk][2] * scale, x[0][kk][3] * scale);
-    qa[kk][3] = pack_bf16(x[1][kk][2] * scale, x[1][kk][3] * scale);
-  }
-}
-
 // S[16 x 8] += q' . K'^T for the 8 key rows of a region; lane l supplies
 // row `row` (its key column l & 7).
 __device__ __forceinline__ void qk_tile(const uint32_t (*qa)[4], uint32_t region, int row, float* s) {
