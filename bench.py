@@ -708,6 +708,75 @@ def dec_reference_arm(args):
                     "d2h_bytes_per_step": 0}}
 
 
+# ---- configs mode (--mode configs): the pages' five configurations ---------
+def configs_arm(args, dev):
+    """Device time of one fwd(+bwd) call of each configuration (the pages'
+    setups; synthetic N(0, 1) inputs, seeded), CUDA events over K calls after
+    3 warm-ups.  One JSON object per configuration."""
+    import torch
+
+    import sfa_inputs as si
+    import static_offset_sparse_gb300 as sfa
+
+    pow2 = [1 << j for j in range(11)]
+
+    def int_set(alpha, W):
+        return sorted(set(range(W + 1)) | {round(alpha * f) for f in FIB})
+
+    def chris():
+        S = sfa.offsets_christoffel(128, 1024, True)
+        return S
+
+    cases = [  # name, B, T, Hq, Hkv, dtype, kind, params, backward
+        ("1: fp32 interp, alpha=1", 1, 1024, 8, 2, "f32", "interp", (FIB, 1.0, 8), True),
+        ("2: bf16 interp, one layer, alpha=0.9667", 32, 1024, 8, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
+        ("3: bf16 pow2 K=11, alpha=1", 32, 1024, 8, 2, "bf16", "interp", (pow2, 1.0, 8), True),
+        ("4: bf16 integer forward, T=2048, alpha=1", 4, 2048, 8, 2, "bf16", "int", (int_set(1.0, 8),), False),
+        ("4: bf16 integer forward, T=16384, alpha=1.5", 4, 16384, 8, 2, "bf16", "int", (int_set(1.5, 8),), False),
+        ("5: bf16 Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int", (chris(),), True),
+    ]
+    out = []
+    for name, Bc, Tc, Hq, Hkv, dt, kind, par, bwd in cases:
+        x = si.make_qkvdo_device(Bc, Tc, Hq, Hkv, D, dt, SEED, dev, layer=7)
+        if kind == "interp":
+            base, alpha, W = par
+            f = lambda: sfa.forward(x["q"], x["k"], x["v"], W=W, alpha=alpha, base=base)  # noqa: E731
+            b = lambda O, L: sfa.backward(x["q"], x["k"], x["v"], O, L, x["do"], W=W,  # noqa: E731
+                                          alpha=alpha, base=base)
+            keys = round(pair_counts(alpha, W)[0] / T, 2) if base is FIB else None  # mean over T=1024
+        else:
+            dist = par[0]
+            f = lambda: sfa.forward_int(x["q"], x["k"], x["v"], dist=dist)  # noqa: E731
+            b = lambda O, L: sfa.backward_int(x["q"], x["k"], x["v"], O, L, x["do"], dist=dist)  # noqa: E731
+            keys = len(dist)
+
+        def call():
+            O, L = f()
+            if bwd:
+                b(O, L)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = max(3, min(args.steps, 20))
+        ev0.record()
+        for _ in range(n):
+            call()
+        ev1.record()
+        torch.cuda.synchronize()
+        assert sfa.get_device_status() == 0
+        ms = ev0.elapsed_time(ev1) / n
+        path = "tensor cores" if dt == "bf16" and Hq == 4 * Hkv and not (kind == "int" and min(par[0]) < 0) else "SIMT"
+        out.append({"config": name, "B": Bc, "T": Tc, "heads": f"{Hq}/{Hkv}", "dtype": dt,
+                    "direction": "fwd+bwd" if bwd else "fwd", "path": path,
+                    "ms_per_call": round(ms, 4), "tokens_per_s": round(Bc * Tc / (ms * 1e-3), 1),
+                    "keys_per_query": keys})
+        del x
+        torch.cuda.empty_cache()
+    return out
+
+
 def config(args):
     return {"workload": f"interp {args.schedule} schedule, W={args.W}: B={B} T={T} Hq={HQ} Hkv={HKV} "
                         f"D={D}, {LAYERS} layers, Fibonacci K=15, RoPE 1e4, fwd+bwd+dtheta",
@@ -727,8 +796,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
-    ap.add_argument("--mode", default="train", choices=["train", "decode"],
-                    help="train: the fwd+bwd step (default); decode: one token per sequence")
+    ap.add_argument("--mode", default="train", choices=["train", "decode", "configs"],
+                    help="train: the fwd+bwd step (default); decode: one token per sequence; "
+                         "configs: one line per configuration of the pages")
     ap.add_argument("--decode-batch", type=int, default=32)
     args = ap.parse_args()
     global LAYERS
@@ -759,6 +829,11 @@ def main():
     if args.mode == "decode":  # one process per GPU, independent replicas
         if rank == 0:
             print(json.dumps(decode_arm(args, dev)), flush=True)
+        return
+    if args.mode == "configs":
+        if rank == 0:
+            for line in configs_arm(args, dev):
+                print(json.dumps(line), flush=True)
         return
     layers, ms, clk, launches, roofline = gpu_arm(args, rank, world, dev)
     value = world * B * T / (ms * 1e-3)
