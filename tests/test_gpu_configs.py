@@ -119,3 +119,18 @@ def test_config5_christoffel(sfa):
     fwd = lambda d: sfa.forward_int(d["q"], d["k"], d["v"], dist=dist)
     bwd = lambda d, O, L: sfa.backward_int(d["q"], d["k"], d["v"], O, L, d["do"], dist=dist)
     _sampled(sfa, x, [(9, 2)], o.dist_slots(dist), 1e4, fwd, bwd, True)
+
+
+def test_long_sequence_backward(sfa):
+    """Interpolated forward and backward at T = 8192 (one sequence; many rung
+    slabs far from the tile), checked on one (batch, KV head) unit; dL/dalpha
+    over the whole call."""
+    alpha = 1.37
+    x = si.make_qkvdo(1, 8192, 8, 2, 64, "bf16", seed=si.mix_seed(0, 8), layer=8192)
+    slots = o.interp_slots(FIB, alpha, 8)
+    fwd = lambda d: sfa.forward(d["q"], d["k"], d["v"], W=8, alpha=alpha, base=FIB)
+    bwd = lambda d, O, L: sfa.backward(d["q"], d["k"], d["v"], O, L, d["do"], W=8, alpha=alpha, base=FIB)
+    _, _, g = _sampled(sfa, x, [(0, 1)], slots, 1e4, fwd, bwd, True)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4, alpha=alpha)
+    da, dt = _np(g[3])
+    check_dalpha_dtheta(da, dt, gw, alpha, True)
