@@ -60,6 +60,8 @@ def _lib():
                 "sfa_rung_table": [_I32P, C.c_int32, C.c_double, C.c_int32, _I32P,
                                    C.POINTER(C.c_float), C.POINTER(C.c_float), C.c_int32, _I32P],
                 "sfa_int_distances": [_I32P, C.c_int32, _I32P, C.c_int32, _I32P],
+                "sfa_band_plan": [_I32P, C.c_int32, C.c_int32, C.c_int32, _I32P, _I32P, _I32P,
+                                  C.c_int32, _I32P],
                 "sfa_rope_table_bytes": [C.c_int32, C.POINTER(C.c_size_t)],
                 "sfa_rope_table": [C.c_int32, C.c_double, _P, _P],
                 "sfa_workspace_size": [C.POINTER(Desc), C.c_int, C.c_int, C.POINTER(C.c_size_t)],

@@ -63,6 +63,21 @@ def int_distances(dist) -> list[int]:
     return list(out[: nout.value])
 
 
+def band_plan(dist, T: int, G: int):
+    """How the integer path lays a bf16 distance set out for the band
+    kernels (sfa_band_plan): (delta, [(start, length), ...]); delta = 0 when
+    the set runs the rung or SIMT kernels instead."""
+    arr, n = i32_array(dist)
+    cap = 256
+    starts = (C.c_int32 * cap)()
+    lens = (C.c_int32 * cap)()
+    delta = C.c_int32(0)
+    nruns = C.c_int32(0)
+    check(_lib().sfa_band_plan(arr, n, T, G, C.byref(delta), starts, lens, cap, C.byref(nruns)),
+          "sfa_band_plan")
+    return delta.value, [(starts[m], lens[m]) for m in range(nruns.value)]
+
+
 def reach(dist_sets, T: int):
     """Reachability through a stack of layers (sfa_reach): returns hops (list
     of T ints, -1 = never) and covered (one count per layer)."""

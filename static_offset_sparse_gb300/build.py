@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libsfa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["sfa_host.cpp", "sfa_api.cu", "sfa_fwd.cu", "sfa_bwd.cu", "sfa_fwd_tc.cu", "sfa_bwd_tc.cu",
-           "sfa_noalloc.cu", "sfa_decode.cu", "sfa_schedule.cpp"]
+           "sfa_noalloc.cu", "sfa_decode.cu", "sfa_schedule.cpp", "sfa_band.cu"]
 
 
 def _nvcc() -> str:

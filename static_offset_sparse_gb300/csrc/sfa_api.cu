@@ -40,6 +40,21 @@ int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int b
              : SFA_ERR_CUDA;
 }
 
+int make_band_map(CUtensorMap* m, const void* base, int64_t planes, int T, int delta, int box_rows,
+                  int box_planes) {
+  auto fn = encode_fn();
+  if (!fn || delta <= 0 || T % delta) return SFA_ERR_CUDA;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)delta, (cuuint64_t)(T / delta), (cuuint64_t)planes};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)delta * 128, (cuuint64_t)T * 128};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
+
 int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int box_slots,
                   int box_q) {
   auto fn = encode_fn();
@@ -123,8 +138,42 @@ static bool tc_path(const sfa_desc* d, const Plan& p) {
   return use_tc(d) && (p.n == 0 || p.c[0] >= 0);
 }
 
-static size_t forward_workspace_bytes(const sfa_desc* d, const Plan& p) {
-  return tc_path(d, p) ? kr_bytes(d) : 0;
+static size_t forward_workspace_bytes(const sfa_desc* d, const Plan& p, const BandPlan& bp) {
+  return bp.delta > 0 || tc_path(d, p) ? kr_bytes(d) : 0;
+}
+
+// The plans of a call: an integer bf16 set with a band plan runs the band
+// kernels (bp.delta > 0; p is then unused), anything else the rung plan p.
+static int plan_call(const sfa_desc* d, int interp, Plan* p, BandPlan* bp) {
+  bp->delta = 0;
+  bp->nruns = 0;
+  if (!interp) {
+    int rc = build_band_plan(d, bp);
+    if (rc != SFA_OK) return rc;
+    if (bp->delta > 0) {
+      p->W = -1;
+      p->n = 0;
+      p->interp = 0;
+      return SFA_OK;
+    }
+  }
+  return interp ? build_interp_plan(d, p) : build_int_plan(d, p);
+}
+
+// Rotated keys for the tensor-core kernels: the caller's k_rot, the raw keys
+// without RoPE, else K' written into scratch by the prep kernel.
+static int rotated_keys(const sfa_desc* d, const void* k, void* scratch, void* stream,
+                        const void** kr) {
+  *kr = k;
+  if (!d->rope) return SFA_OK;
+  if (d->k_rot) {
+    *kr = d->k_rot;
+    return SFA_OK;
+  }
+  LaunchTimer tm(SFA_KERNEL_PREP, stream);
+  int rc = launch_rope_prep(k, d->rope, scratch, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
+  *kr = scratch;
+  return rc;
 }
 
 static int forward_common(const sfa_desc* d, int interp, const void* q, const void* k,
@@ -135,9 +184,9 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   if (!q || !k || !v || !o || !lse) return SFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SFA_ERR_INVALID_ARG;
   Plan p;
-  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
-  if (rc != SFA_OK) return rc;
-  const size_t need = forward_workspace_bytes(d, p);
+  BandPlan bp;
+  if ((rc = plan_call(d, interp, &p, &bp)) != SFA_OK) return rc;
+  const size_t need = forward_workspace_bytes(d, p, bp);
   if (need && (!ws || !aligned16(ws))) return SFA_ERR_INVALID_ARG;
   if (ws_bytes < need) return SFA_ERR_CAPACITY;
   AttnArgs a;
@@ -147,21 +196,15 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
   a.v = v;
   a.out_o = o;
   a.out_lse = lse;
-  if (!tc_path(d, p)) return launch_forward(a, p, d->dtype, stream);
-  const void* kr = k;
-  if (d->rope && d->k_rot) {
-    kr = d->k_rot;
-  } else if (d->rope) {
-    LaunchTimer tm(SFA_KERNEL_PREP, stream);
-    rc = launch_rope_prep(k, d->rope, ws, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
-    if (rc != SFA_OK) return rc;
-    kr = ws;
-  }
-  return launch_forward_tc(a, p, kr, stream);
+  if (bp.delta == 0 && !tc_path(d, p)) return launch_forward(a, p, d->dtype, stream);
+  const void* kr = nullptr;
+  if ((rc = rotated_keys(d, k, ws, stream, &kr)) != SFA_OK) return rc;
+  return bp.delta > 0 ? launch_band_forward(a, bp, kr, stream) : launch_forward_tc(a, p, kr, stream);
 }
 
-static size_t backward_bytes(const sfa_desc* d, const Plan& p) {
+static size_t backward_bytes(const sfa_desc* d, const Plan& p, const BandPlan& bp) {
   size_t a, b, c;
+  if (bp.delta > 0) return band_backward_workspace_bytes(d, &a, &b, &c);
   return tc_path(d, p) ? backward_tc_workspace_bytes(d, p, &a, &b, &c) : backward_workspace_bytes(d, p);
 }
 
@@ -177,9 +220,9 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
   for (const void* x : ptrs)
     if (!aligned16(x)) return SFA_ERR_INVALID_ARG;
   Plan p;
-  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
-  if (rc != SFA_OK) return rc;
-  if (ws_bytes < backward_bytes(d, p)) return SFA_ERR_CAPACITY;
+  BandPlan bp;
+  if ((rc = plan_call(d, interp, &p, &bp)) != SFA_OK) return rc;
+  if (ws_bytes < backward_bytes(d, p, bp)) return SFA_ERR_CAPACITY;
   AttnArgs a;
   if ((rc = fill_args(d, &a)) != SFA_OK) return rc;
   a.q = q;
@@ -194,18 +237,18 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
   a.dalpha_out = interp ? dadt : nullptr;
   a.dalpha_part = static_cast<double*>(ws);
   char* w = static_cast<char*>(ws);
+  if (bp.delta > 0) {
+    size_t okr, oqt, ost;
+    band_backward_workspace_bytes(d, &okr, &oqt, &ost);
+    const void* kr = nullptr;
+    if ((rc = rotated_keys(d, k, w + okr, stream, &kr)) != SFA_OK) return rc;
+    return launch_band_backward(a, bp, kr, w + oqt, w + ost, stream);
+  }
   if (tc_path(d, p)) {
     size_t okr, oqt, oco;
     backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco);
-    const void* kr = k;
-    if (d->rope && d->k_rot) {
-      kr = d->k_rot;
-    } else if (d->rope) {
-      LaunchTimer tm(SFA_KERNEL_PREP, stream);
-      rc = launch_rope_prep(k, d->rope, w + okr, (int64_t)d->B * d->Hkv * d->T, d->T, stream);
-      if (rc != SFA_OK) return rc;
-      kr = w + okr;
-    }
+    const void* kr = nullptr;
+    if ((rc = rotated_keys(d, k, w + okr, stream, &kr)) != SFA_OK) return rc;
     return launch_backward_tc(a, p, kr, w + oqt, w + oco, stream);
   }
   const int TK = 128 >> a.lgG;
@@ -237,9 +280,9 @@ int sfa_workspace_size(const sfa_desc* d, int interp, int backward, size_t* byte
   int rc = validate_shape(d);
   if (rc != SFA_OK) return rc;
   Plan p;
-  rc = interp ? build_interp_plan(d, &p) : build_int_plan(d, &p);
-  if (rc != SFA_OK) return rc;
-  *bytes = backward ? backward_bytes(d, p) : forward_workspace_bytes(d, p);
+  BandPlan bp;
+  if ((rc = plan_call(d, interp, &p, &bp)) != SFA_OK) return rc;
+  *bytes = backward ? backward_bytes(d, p, bp) : forward_workspace_bytes(d, p, bp);
   return SFA_OK;
 }
 

@@ -1,0 +1,784 @@
+// Tensor-core kernels for integer distance sets made of long arithmetic runs
+// (bf16 I/O, G = 1, 2, 4 or 8 query heads per KV head).
+//
+// "Christoffel-Balanced Sparse Attention" builds its offsets from a carry
+// word with m ones per period k; when m divides k they are 0 and
+// k/m - 1 + t k/m, one arithmetic run, and a dense causal window is one run
+// of step 1.  With delta the runs' common step and i = r + delta u
+// (r = i mod delta), run m (distances a_m + delta t, t < len_m) sends query
+// class r to key class rho = (r - a_m) mod delta at compressed keys
+// v in [u + e - len_m + 1, u + e], e = floor((r - a_m) / delta): a band.  The
+// keys of query i are still exactly i - s for s in the set (the integer path
+// of "Depth-Staggered Fibonacci Spacing for Sparse Attention"); only the
+// order of the work changes.
+//
+// A CTA owns 64 query rows, G heads x 64 / G consecutive compressed positions
+// of one class (row h (64 / G) + u), and walks, run by run, the 64-key tiles
+// of its band.  Rows come in as TMA boxes of a [plane][T / delta][delta][64]
+// view (the class is a coordinate of stride one row, the compressed index
+// one of stride delta rows; rows outside the sequence are zero-filled).
+// Products are mma.sync m16n8k16 (bf16 in, fp32 accumulate) on dense
+// 16 x 64 per-warp tiles, masked only at the band's edges:
+//  * band_fwd:    S = q'.K'^T, online softmax in base 2, O += P.V; O, LSE.
+//  * band_bwd_q:  S and dP = dO.V^T recomputed, P = exp(S - LSE),
+//                 dS = P (dP - delta_i), dQ += dS.K'; writes dQ = R(-phi) dQ'
+//                 / 8, q~ = q'/8 and per row (LSE log2(e), delta_i).
+//  * band_bwd_kv: per 64-key tile, the query tiles of each run that reach
+//                 it, keys on the mma M side: S^T = K'.q~^T, dP^T = V.dO^T,
+//                 dV += P^T.dO, dK' += dS^T.q~; dK = R(-phi) dK'.  Each key
+//                 row is written once (no atomics).
+#include <math.h>
+
+#include "sfa_tc.cuh"
+
+namespace sfa {
+
+constexpr int kBR = 64;                 // rows of every tile: queries (G heads x 64/G) or keys
+constexpr int kBThreads = 128;          // 4 warps x 16 rows
+constexpr int kBTileB = kBR * 128;      // 8 KB, a 1024-byte multiple (128B swizzle)
+constexpr int kBStages = 2;
+constexpr int kBStageB = 2 * kBTileB;   // K' + V, or q~ + dO
+constexpr size_t kBandFwdSmem = (size_t)kBTileB + (size_t)kBStages * kBStageB + 1024;
+constexpr size_t kBandBwdQSmem = (size_t)3 * kBTileB + (size_t)kBStages * kBStageB + 1024;
+constexpr size_t kBandBwdKvSmem = (size_t)2 * kBTileB + (size_t)kBStages * kBStageB + 1024;
+
+// Class and shift of run m for query class r: r - a_m = rho + delta e.
+__device__ __forceinline__ void run_shift(const BandPlan& P, int m, int r, int& rho, int& e) {
+  const int x = r - P.a[m];
+  e = x >= 0 ? x / P.delta : -((P.delta - 1 - x) / P.delta);
+  rho = x - e * P.delta;
+}
+
+// Key tiles of a query tile (class r, compressed positions u0 .. ul): run by
+// run, the band [u0 + e - len + 1, ul + e] clipped at 0, from its low end in
+// steps of 64.
+struct QWalk {
+  int m, vs, vhi, rho, e;
+};
+__device__ __forceinline__ bool qwalk_seek(const BandPlan& P, int r, int u0, int ul, QWalk& w) {
+  for (; w.m < P.nruns; ++w.m) {
+    run_shift(P, w.m, r, w.rho, w.e);
+    const int lo = max(0, u0 + w.e - P.len[w.m] + 1), hi = ul + w.e;
+    if (lo <= hi) {
+      w.vs = lo;
+      w.vhi = hi;
+      return true;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ bool qwalk_next(const BandPlan& P, int r, int u0, int ul, QWalk& w) {
+  w.vs += kBR;
+  if (w.vs <= w.vhi) return true;
+  ++w.m;
+  return qwalk_seek(P, r, u0, ul, w);
+}
+
+// Query tiles that reach a key tile (class rho, compressed keys v0 .. vl):
+// run by run, query class r = (rho + a) mod delta at positions
+// [v0 - e, vl - e + len - 1] (clipped to the sequence), in steps of bu.
+struct KWalk {
+  int m, us, uhi, r, e;
+};
+__device__ __forceinline__ bool kwalk_seek(const BandPlan& P, int rho, int v0, int vl, int Uc,
+                                           KWalk& w) {
+  for (; w.m < P.nruns; ++w.m) {
+    w.r = (rho + P.a[w.m]) % P.delta;
+    int rho2;
+    run_shift(P, w.m, w.r, rho2, w.e);
+    const int lo = v0 - w.e, hi = min(Uc - 1, vl - w.e + P.len[w.m] - 1);
+    if (lo <= hi) {
+      w.us = lo;
+      w.uhi = hi;
+      return true;
+    }
+  }
+  return false;
+}
+__device__ __forceinline__ bool kwalk_next(const BandPlan& P, int rho, int v0, int vl, int Uc, int bu,
+                                           KWalk& w) {
+  w.us += bu;
+  if (w.us <= w.uhi) return true;
+  ++w.m;
+  return kwalk_seek(P, rho, v0, vl, Uc, w);
+}
+
+// A fragments of rows row0 .. row0 + 15 of a 64-row tile for the 4 k-steps.
+// With transform they are unpacked, rotated by RoPE (rows gid and gid + 8 at
+// positions pos[0] and pos[1]; none if rope is nullptr), scaled and repacked.
+__device__ __forceinline__ void band_frags(uint32_t tile, int row0, const float2* rope,
+                                           const int* pos, float scale, bool transform,
+                                           uint32_t (*qa)[4]) {
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    ldsm_x4(tile + swz(row0 + (lane & 15), 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2],
+            qa[kk][3]);
+  if (!transform) return;
+  float x[2][4][4];  // [row gid / gid + 8][kk][dims 2tig, 2tig+1, 2tig+8, 2tig+9]
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const float2 a0 = unpack_bf16(qa[kk][0]), a1 = unpack_bf16(qa[kk][1]);
+    const float2 a2 = unpack_bf16(qa[kk][2]), a3 = unpack_bf16(qa[kk][3]);
+    x[0][kk][0] = a0.x; x[0][kk][1] = a0.y; x[0][kk][2] = a2.x; x[0][kk][3] = a2.y;
+    x[1][kk][0] = a1.x; x[1][kk][1] = a1.y; x[1][kk][2] = a3.x; x[1][kk][3] = a3.y;
+  }
+  if (rope) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const float2* tab = rope + (int64_t)pos[rr] * 32;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(tab + 16 * kk + 2 * tig));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(tab + 16 * kk + 2 * tig + 8));
+        const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = x[rr][kk][e], hi = x[rr][kk + 2][e];
+          x[rr][kk][e] = lo * cs[e] - hi * sn[e];
+          x[rr][kk + 2][e] = lo * sn[e] + hi * cs[e];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    qa[kk][0] = pack_bf16(x[0][kk][0] * scale, x[0][kk][1] * scale);
+    qa[kk][1] = pack_bf16(x[1][kk][0] * scale, x[1][kk][1] * scale);
+    qa[kk][2] = pack_bf16(x[0][kk][2] * scale, x[0][kk][3] * scale);
+    qa[kk][3] = pack_bf16(x[1][kk][2] * scale, x[1][kk][3] * scale);
+  }
+}
+
+// Byte address of the bf16 pair (dims 8 nd + 2 tig, + 1) of tile row `row`.
+__device__ __forceinline__ uint32_t band_out_addr(uint32_t tile, int row, int nd) {
+  return tile + swz(row, nd) + 4 * (threadIdx.x & 3);
+}
+
+// Rows gid (x = 0) and gid + 8 (x = 1) of a warp's accumulator v[8][4]
+// (dims 8 nd + 2 tig, + 1), scaled, optionally rotated back by RoPE
+// (R(-phi) at positions pos[x]), into a 64-row output tile.
+__device__ __forceinline__ void band_store_rows(uint32_t tile, int row0, const float (*v)[4],
+                                                const float* scale, const float2* rope,
+                                                const int* pos) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    float w[8][2];
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd) {
+      w[nd][0] = v[nd][2 * x] * scale[x];
+      w[nd][1] = v[nd][2 * x + 1] * scale[x];
+    }
+    if (rope) {
+#pragma unroll
+      for (int nd = 0; nd < 4; ++nd) {
+        const float4 cs =
+            __ldg(reinterpret_cast<const float4*>(rope + (int64_t)pos[x] * 32 + 8 * nd + 2 * tig));
+        const float c2[2] = {cs.x, cs.z}, s2[2] = {cs.y, cs.w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float lo = w[nd][e], hi = w[nd + 4][e];
+          w[nd][e] = lo * c2[e] + hi * s2[e];
+          w[nd + 4][e] = hi * c2[e] - lo * s2[e];
+        }
+      }
+    }
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd)
+      st_shared_u32(band_out_addr(tile, row0 + gid + 8 * x, nd), pack_bf16(w[nd][0], w[nd][1]));
+  }
+}
+
+// Barriers: kBStages stage barriers, then one for the CTA's own tiles.
+__device__ __forceinline__ void band_init_bars(uint64_t* bars) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s <= kBStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+}
+
+// Bounded wait on a barrier, uniform across the CTA (false: timed out, the
+// status word holds SFA_ERR_TIMEOUT).
+__device__ __forceinline__ bool band_wait(uint64_t* bar, uint32_t parity, int* status) {
+  const bool ok = mbar_wait_bounded(smem_u32(bar), parity);
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) record_status(status, SFA_ERR_TIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+// The staged loop: tile t waits on stage t % kBStages; once every thread has
+// passed the barrier of tile t, the stage of tile t - 1 is refilled with tile
+// t - 1 + kBStages by issue(stage) (thread 0, in tile order).  compute(t,
+// stage address) runs on every thread.  False (uniformly) on a timeout,
+// after thread 0 has waited out the loads still in flight.
+template <typename IssueFn, typename ComputeFn>
+__device__ __forceinline__ bool band_loop(int NT, uint32_t stages, uint64_t* bars, int* status,
+                                          IssueFn issue, ComputeFn compute) {
+  for (int t = 0; t < NT; ++t) {
+    const int s = t % kBStages;
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (t / kBStages) & 1);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        record_status(status, SFA_ERR_TIMEOUT);
+        for (int t2 = t; t2 < NT && t2 < t + kBStages - 1; ++t2)
+          mbar_wait_bounded(smem_u32(&bars[t2 % kBStages]), (t2 / kBStages) & 1);
+      }
+      return false;
+    }
+    if (threadIdx.x == 0 && t > 0 && t - 1 + kBStages < NT) issue((t - 1) % kBStages);
+    compute(t, stages + s * kBStageB);
+  }
+  __syncthreads();  // every stage is consumed: shared memory may be reused
+  return true;
+}
+
+// Thread 0 waits out the first stages' loads after the CTA's own tiles timed
+// out (nothing may land in shared memory after the CTA has left).
+__device__ __forceinline__ void band_drain(uint64_t* bars, int NT) {
+  if (threadIdx.x == 0)
+    for (int s = 0; s < kBStages && s < NT; ++s) mbar_wait_bounded(smem_u32(&bars[s]), 0);
+}
+
+// Online softmax over one 64-key tile for rows gid (x = 0) and gid + 8 of a
+// lane: s[x][16] holds base-2 logits (invalid = -inf) and comes back as
+// p = 2^(s - m).  The running maximum m is refreshed only when some logit
+// of the warp exceeds it by more than 8: between refreshes p stays below
+// 2^8, and O = sum p v / sum p and LSE = m + log2 l hold for any m.  m stays
+// uniform over a row's quad (it changes only through the quad reduction).
+__device__ __forceinline__ void band_softmax(float (*s)[16], float* m, float* l, float (*o)[4]) {
+  constexpr float kMargin = 8.0f;
+  float mx[2];
+  bool need = false;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    mx[x] = s[x][0];
+#pragma unroll
+    for (int e = 1; e < 16; ++e) mx[x] = fmaxf(mx[x], s[x][e]);
+    need |= mx[x] > m[x] + kMargin;  // m = -inf: any valid logit
+  }
+  if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      mx[x] = fmaxf(mx[x], __shfl_xor_sync(0xffffffffu, mx[x], 1));
+      mx[x] = fmaxf(mx[x], __shfl_xor_sync(0xffffffffu, mx[x], 2));
+      if (mx[x] > m[x]) {
+        const float corr = ex2(m[x] - mx[x]);  // 0 while the row had no key
+        m[x] = mx[x];
+        l[x] *= corr;
+#pragma unroll
+        for (int nd = 0; nd < 8; ++nd) {
+          o[nd][2 * x] *= corr;
+          o[nd][2 * x + 1] *= corr;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const float mm = m[x] == -INFINITY ? 0.0f : m[x];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float pe = ex2(s[x][e] - mm);  // ex2(-inf) = 0
+      s[x][e] = pe;
+      l[x] += pe;
+    }
+  }
+}
+
+// Query-tile geometry shared by the forward and the query-side backward.
+template <int G>
+struct QTile {
+  static constexpr int BU = kBR / G;
+  int delta, Uc, r, u0, ul, qplane, bg;
+  int hh[2], uu[2], pos[2];  // rows gid, gid + 8 of the lane's warp: head, position, i
+  __device__ __forceinline__ QTile(const AttnArgs& a, const BandPlan& P) {
+    const int warp = threadIdx.x >> 5, gid = (threadIdx.x & 31) >> 2;
+    delta = P.delta;
+    Uc = a.T / delta;
+    const int nqt = (Uc + BU - 1) / BU;
+    r = blockIdx.x / nqt;
+    u0 = (blockIdx.x - r * nqt) * BU;
+    ul = min(u0 + BU - 1, Uc - 1);
+    bg = blockIdx.y;
+    const int b = bg / a.Hkv, g = bg - b * a.Hkv;
+    qplane = b * a.Hq + g * G;
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int row = 16 * warp + gid + 8 * x;
+      hh[x] = row / BU;
+      uu[x] = u0 + row % BU;
+      pos[x] = r + delta * min(uu[x], Uc - 1);
+    }
+  }
+  __device__ __forceinline__ int count(const BandPlan& P) const {
+    int n = 0;
+    QWalk w{0, 0, 0, 0, 0};
+    if (qwalk_seek(P, r, u0, ul, w)) do ++n; while (qwalk_next(P, r, u0, ul, w));
+    return n;
+  }
+  // Tile columns [lo, hi] of row x that are keys of the current run.
+  __device__ __forceinline__ void cols(const BandPlan& P, const QWalk& w, int* lo, int* hi) const {
+    const int len = P.len[w.m];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      lo[x] = uu[x] + w.e - len + 1 - w.vs;
+      hi[x] = uu[x] < Uc ? uu[x] + w.e - w.vs : -1;  // rows past the sequence take no key
+    }
+  }
+};
+
+template <int G>
+__global__ void __launch_bounds__(kBThreads, 3)
+    band_fwd_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
+                    const __grid_constant__ CUtensorMap mo, const __grid_constant__ BandPlan P) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kBStages + 1];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tig = lane & 3;
+  const QTile<G> q(a, P);
+  const uint32_t qtile = sbase, stages = sbase + kBTileB;
+  const int NT = q.count(P);
+  band_init_bars(bars);
+  QWalk iw{0, 0, 0, 0, 0};
+  auto issue = [&](int s) {
+    const uint32_t st = stages + s * kBStageB, bar = smem_u32(&bars[s]);
+    mbar_expect_tx(bar, kBStageB);
+    tma_load_4d(st, &mk, 0, iw.rho, iw.vs, q.bg, bar);
+    tma_load_4d(st + kBTileB, &mv, 0, iw.rho, iw.vs, q.bg, bar);
+    qwalk_next(P, q.r, q.u0, q.ul, iw);
+  };
+  if (threadIdx.x == 0) {
+    const uint32_t qb = smem_u32(&bars[kBStages]);
+    mbar_expect_tx(qb, kBTileB);
+    tma_load_4d(qtile, &mq, 0, q.r, q.u0, q.qplane, qb);
+    qwalk_seek(P, q.r, q.u0, q.ul, iw);
+    for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
+  }
+  if (!band_wait(&bars[kBStages], 0, a.status)) {
+    band_drain(bars, NT);
+    return;
+  }
+  uint32_t qa[4][4];
+  band_frags(qtile, 16 * warp, static_cast<const float2*>(a.rope), q.pos, 0.125f * kLog2e, true, qa);
+  float o[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+  QWalk cw{0, 0, 0, 0, 0};
+  qwalk_seek(P, q.r, q.u0, q.ul, cw);
+
+  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+      qk_tile(qa, kst, 8 * nt + (lane & 7), acc[nt]);
+    }
+    int lo[2], hi[2];
+    q.cols(P, cw, lo, hi);
+    float s[2][16];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int x = e >> 1, col = 8 * nt + 2 * tig + (e & 1);
+        s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] : -INFINITY;
+      }
+    band_softmax(s, m, l, o);
+    const uint32_t vst = kst + kBTileB;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t pa[4] = {pack_bf16(s[0][4 * kk], s[0][4 * kk + 1]),
+                              pack_bf16(s[1][4 * kk], s[1][4 * kk + 1]),
+                              pack_bf16(s[0][4 * kk + 2], s[0][4 * kk + 3]),
+                              pack_bf16(s[1][4 * kk + 2], s[1][4 * kk + 3])};
+      pv_tile(pa, vst, 16 * kk + (lane & 7), 16 * kk + 8 + (lane & 7), o);
+    }
+    qwalk_next(P, q.r, q.u0, q.ul, cw);
+  });
+  if (!ok) return;
+
+  float inv[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    l[x] += __shfl_xor_sync(0xffffffffu, l[x], 1);
+    l[x] += __shfl_xor_sync(0xffffffffu, l[x], 2);
+    inv[x] = 1.0f / l[x];
+    if (tig == 0 && q.uu[x] < q.Uc)
+      a.out_lse[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] = (m[x] + log2f(l[x])) * kLn2;
+  }
+  band_store_rows(qtile, 16 * warp, o, inv, nullptr, q.pos);
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tma_store_4d(&mo, 0, q.r, q.u0, q.qplane, qtile);
+    bulk_commit();
+    bulk_wait_read();
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kBThreads, 3)
+    band_bwd_q_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
+                      const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mo,
+                      const __grid_constant__ CUtensorMap mqt,
+                      const __grid_constant__ CUtensorMap mdq, float2* __restrict__ stat,
+                      const __grid_constant__ BandPlan P) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kBStages + 1];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
+  const QTile<G> q(a, P);
+  const uint32_t qtile = sbase, dotile = sbase + kBTileB, otile = sbase + 2 * kBTileB;
+  const uint32_t stages = sbase + 3 * kBTileB;
+  const float2* rope = static_cast<const float2*>(a.rope);
+  const int NT = q.count(P);
+  band_init_bars(bars);
+  QWalk iw{0, 0, 0, 0, 0};
+  auto issue = [&](int s) {
+    const uint32_t st = stages + s * kBStageB, bar = smem_u32(&bars[s]);
+    mbar_expect_tx(bar, kBStageB);
+    tma_load_4d(st, &mk, 0, iw.rho, iw.vs, q.bg, bar);
+    tma_load_4d(st + kBTileB, &mv, 0, iw.rho, iw.vs, q.bg, bar);
+    qwalk_next(P, q.r, q.u0, q.ul, iw);
+  };
+  if (threadIdx.x == 0) {
+    const uint32_t qb = smem_u32(&bars[kBStages]);
+    mbar_expect_tx(qb, 3 * kBTileB);
+    tma_load_4d(qtile, &mq, 0, q.r, q.u0, q.qplane, qb);
+    tma_load_4d(dotile, &mdo, 0, q.r, q.u0, q.qplane, qb);
+    tma_load_4d(otile, &mo, 0, q.r, q.u0, q.qplane, qb);
+    qwalk_seek(P, q.r, q.u0, q.ul, iw);
+    for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
+  }
+  float lse2[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) lse2[x] = a.lse[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] * kLog2e;
+  if (!band_wait(&bars[kBStages], 0, a.status)) {
+    band_drain(bars, NT);
+    return;
+  }
+  uint32_t qa[4][4], da[4][4];
+  band_frags(qtile, 16 * warp, rope, q.pos, 0.125f, true, qa);
+  band_frags(dotile, 16 * warp, nullptr, q.pos, 1.0f, false, da);
+  float dlt[2];
+  {  // delta_i = dO . O per row from this lane's 16 dims of each, then the quad
+    uint32_t oa[4][4];
+    band_frags(otile, 16 * warp, nullptr, q.pos, 1.0f, false, oa);
+    float acc[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float2 u = unpack_bf16(da[kk][x]), v = unpack_bf16(oa[kk][x]);
+        acc[x & 1] = fmaf(u.x, v.x, fmaf(u.y, v.y, acc[x & 1]));  // x even: row gid, odd: gid + 8
+      }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      acc[x] += __shfl_xor_sync(0xffffffffu, acc[x], 1);
+      acc[x] += __shfl_xor_sync(0xffffffffu, acc[x], 2);
+      dlt[x] = acc[x];
+      if (tig == 0 && q.uu[x] < q.Uc)
+        stat[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] = make_float2(lse2[x], dlt[x]);
+    }
+  }
+  __syncthreads();  // the O tile is read: it now carries q~ = q'/8 out for the key side
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    st_shared_u32(band_out_addr(otile, 16 * warp + gid, 2 * kk), qa[kk][0]);
+    st_shared_u32(band_out_addr(otile, 16 * warp + gid + 8, 2 * kk), qa[kk][1]);
+    st_shared_u32(band_out_addr(otile, 16 * warp + gid, 2 * kk + 1), qa[kk][2]);
+    st_shared_u32(band_out_addr(otile, 16 * warp + gid + 8, 2 * kk + 1), qa[kk][3]);
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tma_store_4d(&mqt, 0, q.r, q.u0, q.qplane, otile);
+    bulk_commit();
+  }
+  float dq[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
+  QWalk cw{0, 0, 0, 0, 0};
+  qwalk_seek(P, q.r, q.u0, q.ul, cw);
+
+  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
+    const uint32_t vst = kst + kBTileB;
+    int lo[2], hi[2];
+    q.cols(P, cw, lo, hi);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {  // keys 32 hf .. 32 hf + 31 of the tile
+      float sc[4][4], dp[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
+        dp[nt][0] = dp[nt][1] = dp[nt][2] = dp[nt][3] = 0.0f;
+        const int row = 32 * hf + 8 * nt + (lane & 7);
+        qk_tile(qa, kst, row, sc[nt]);
+        qk_tile(da, vst, row, dp[nt]);
+      }
+      float ds[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
+          const float pr =
+              (col >= lo[x] && col <= hi[x]) ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x])) : 0.0f;
+          ds[nt][e] = pr * (dp[nt][e] - dlt[x]);
+        }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t sa[4] = {pack_bf16(ds[2 * ks][0], ds[2 * ks][1]),
+                                pack_bf16(ds[2 * ks][2], ds[2 * ks][3]),
+                                pack_bf16(ds[2 * ks + 1][0], ds[2 * ks + 1][1]),
+                                pack_bf16(ds[2 * ks + 1][2], ds[2 * ks + 1][3])};
+        const int rl = 32 * hf + 16 * ks + (lane & 7);
+        pv_tile(sa, kst, rl, rl + 8, dq);
+      }
+    }
+    qwalk_next(P, q.r, q.u0, q.ul, cw);
+  });
+  if (!ok) {
+    if (threadIdx.x == 0) bulk_wait_read();
+    return;
+  }
+  const float eighth[2] = {0.125f, 0.125f};
+  band_store_rows(qtile, 16 * warp, dq, eighth, rope, q.pos);  // dQ = R(-phi) dQ' / 8
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tma_store_4d(&mdq, 0, q.r, q.u0, q.qplane, qtile);
+    bulk_commit();
+    bulk_wait_read();  // the q~ and dQ tiles have been read
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kBThreads, 2)
+    band_bwd_kv_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                       const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mqt,
+                       const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
+                       const __grid_constant__ CUtensorMap mdv, const float2* __restrict__ stat,
+                       const __grid_constant__ BandPlan P) {
+  constexpr int BU = kBR / G;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kBStages + 1];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
+  const int T = a.T, delta = P.delta, Uc = T / delta;
+  const int nkt = (Uc + kBR - 1) / kBR;
+  const int rho = blockIdx.x / nkt, v0 = (blockIdx.x - rho * nkt) * kBR;
+  const int vl = min(v0 + kBR - 1, Uc - 1);
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  const int qplane = b * a.Hq + g * G;
+  const int kv[2] = {v0 + 16 * warp + gid, v0 + 16 * warp + gid + 8};  // this lane's key rows
+  const uint32_t ktile = sbase, vtile = sbase + kBTileB, stages = sbase + 2 * kBTileB;
+  int NT = 0;
+  {
+    KWalk w{0, 0, 0, 0, 0};
+    if (kwalk_seek(P, rho, v0, vl, Uc, w)) do ++NT; while (kwalk_next(P, rho, v0, vl, Uc, BU, w));
+  }
+  band_init_bars(bars);
+  KWalk iw{0, 0, 0, 0, 0};
+  auto issue = [&](int s) {
+    const uint32_t st = stages + s * kBStageB, bar = smem_u32(&bars[s]);
+    mbar_expect_tx(bar, kBStageB);
+    tma_load_4d(st, &mqt, 0, iw.r, iw.us, qplane, bar);
+    tma_load_4d(st + kBTileB, &mdo, 0, iw.r, iw.us, qplane, bar);
+    kwalk_next(P, rho, v0, vl, Uc, BU, iw);
+  };
+  if (threadIdx.x == 0) {
+    const uint32_t kb = smem_u32(&bars[kBStages]);
+    mbar_expect_tx(kb, 2 * kBTileB);
+    tma_load_4d(ktile, &mk, 0, rho, v0, bg, kb);
+    tma_load_4d(vtile, &mv, 0, rho, v0, bg, kb);
+    kwalk_seek(P, rho, v0, vl, Uc, iw);
+    for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
+  }
+  if (!band_wait(&bars[kBStages], 0, a.status)) {
+    band_drain(bars, NT);
+    return;
+  }
+  uint32_t ka[4][4], va[4][4];
+  band_frags(ktile, 16 * warp, nullptr, nullptr, 1.0f, false, ka);
+  band_frags(vtile, 16 * warp, nullptr, nullptr, 1.0f, false, va);
+  float dk[8][4], dv[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) {
+    dk[nd][0] = dk[nd][1] = dk[nd][2] = dk[nd][3] = 0.0f;
+    dv[nd][0] = dv[nd][1] = dv[nd][2] = dv[nd][3] = 0.0f;
+  }
+  KWalk cw{0, 0, 0, 0, 0};
+  kwalk_seek(P, rho, v0, vl, Uc, cw);
+
+  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t qst) {
+    const uint32_t dst = qst + kBTileB;
+    const int len = P.len[cw.m];
+    // query u of column n reaches key v of row x iff t = u - v + e is in [0, len)
+    int tb[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) tb[x] = kv[x] < Uc ? cw.e - kv[x] : -(1 << 30);
+#pragma unroll
+    for (int hq = 0; hq < 2; ++hq) {  // query rows 32 hq .. 32 hq + 31 of the tile
+      float2 sd[4][2];
+      int uq[4][2];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int n = 32 * hq + 8 * nt + 2 * tig + c;
+          const int u = cw.us + n % BU;
+          uq[nt][c] = u < Uc ? u : -(1 << 30);
+          sd[nt][c] = __ldg(stat + (int64_t)(qplane + n / BU) * T + cw.r + delta * min(u, Uc - 1));
+        }
+      float st[4][4], dpt[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.0f;
+        dpt[nt][0] = dpt[nt][1] = dpt[nt][2] = dpt[nt][3] = 0.0f;
+        const int row = 32 * hq + 8 * nt + (lane & 7);
+        qk_tile(ka, qst, row, st[nt]);
+        qk_tile(va, dst, row, dpt[nt]);
+      }
+      float pp[4][4], ds[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int x = e >> 1, c = e & 1;
+          const bool valid = (unsigned)(uq[nt][c] + tb[x]) < (unsigned)len;
+          const float pr = valid ? ex2(fmaf(st[nt][e], kLog2e, -sd[nt][c].x)) : 0.0f;
+          pp[nt][e] = pr;
+          ds[nt][e] = pr * (dpt[nt][e] - sd[nt][c].y);
+        }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t pa[4] = {pack_bf16(pp[2 * ks][0], pp[2 * ks][1]),
+                                pack_bf16(pp[2 * ks][2], pp[2 * ks][3]),
+                                pack_bf16(pp[2 * ks + 1][0], pp[2 * ks + 1][1]),
+                                pack_bf16(pp[2 * ks + 1][2], pp[2 * ks + 1][3])};
+        const uint32_t sa[4] = {pack_bf16(ds[2 * ks][0], ds[2 * ks][1]),
+                                pack_bf16(ds[2 * ks][2], ds[2 * ks][3]),
+                                pack_bf16(ds[2 * ks + 1][0], ds[2 * ks + 1][1]),
+                                pack_bf16(ds[2 * ks + 1][2], ds[2 * ks + 1][3])};
+        const int rl = 32 * hq + 16 * ks + (lane & 7);
+        pv_tile(pa, dst, rl, rl + 8, dv);
+        pv_tile(sa, qst, rl, rl + 8, dk);
+      }
+    }
+    kwalk_next(P, rho, v0, vl, Uc, BU, cw);
+  });
+  if (!ok) return;
+  // dK = R(-phi_j) dK' at j = rho + delta v; dV as accumulated
+  const int kpos[2] = {rho + delta * min(kv[0], Uc - 1), rho + delta * min(kv[1], Uc - 1)};
+  const float one[2] = {1.0f, 1.0f};
+  band_store_rows(ktile, 16 * warp, dk, one, static_cast<const float2*>(a.rope), kpos);
+  band_store_rows(vtile, 16 * warp, dv, one, nullptr, kpos);
+  fence_async_smem();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tma_store_4d(&mdk, 0, rho, v0, bg, ktile);
+    tma_store_4d(&mdv, 0, rho, v0, bg, vtile);
+    bulk_commit();
+    bulk_wait_read();
+  }
+}
+
+// ---- launchers ---------------------------------------------------------------
+
+template <int G>
+static int band_fwd_launch(const AttnArgs& a, const BandPlan& p, const void* kr, cudaStream_t s) {
+  constexpr int BU = kBR / G;
+  CUtensorMap mk, mv, mq, mo;
+  const int64_t planes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
+  if (make_band_map(&mk, kr, planes, a.T, p.delta, kBR, 1) != SFA_OK ||
+      make_band_map(&mv, a.v, planes, a.T, p.delta, kBR, 1) != SFA_OK ||
+      make_band_map(&mq, a.q, qplanes, a.T, p.delta, BU, G) != SFA_OK ||
+      make_band_map(&mo, a.out_o, qplanes, a.T, p.delta, BU, G) != SFA_OK)
+    return SFA_ERR_CUDA;
+  if (cudaFuncSetAttribute(band_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kBandFwdSmem) != cudaSuccess)
+    return SFA_ERR_CUDA;
+  const int Uc = a.T / p.delta;
+  dim3 grid((unsigned)(p.delta * ((Uc + BU - 1) / BU)), (unsigned)(a.B * a.Hkv));
+  LaunchTimer tm(SFA_KERNEL_FWD, s);
+  band_fwd_kernel<G><<<grid, kBThreads, kBandFwdSmem, s>>>(a, mk, mv, mq, mo, p);
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+int launch_band_forward(const AttnArgs& a, const BandPlan& p, const void* kr, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (a.lgG) {
+    case 0: return band_fwd_launch<1>(a, p, kr, s);
+    case 1: return band_fwd_launch<2>(a, p, kr, s);
+    case 2: return band_fwd_launch<4>(a, p, kr, s);
+    case 3: return band_fwd_launch<8>(a, p, kr, s);
+    default: return SFA_ERR_UNSUPPORTED;
+  }
+}
+
+size_t band_backward_workspace_bytes(const sfa_desc* d, size_t* off_kr, size_t* off_qt,
+                                     size_t* off_stat) {
+  const size_t qrows = (size_t)d->B * d->Hq * d->T;
+  *off_kr = 0;
+  *off_qt = kr_bytes(d);
+  *off_stat = *off_qt + align256(qrows * 64 * 2);
+  return *off_stat + align256(qrows * sizeof(float2));
+}
+
+template <int G>
+static int band_bwd_launch(const AttnArgs& a, const BandPlan& p, const void* kr, void* qt,
+                           void* stat, cudaStream_t s) {
+  constexpr int BU = kBR / G;
+  CUtensorMap mk, mv, mq, mdo, mo, mqt, mdq, mdk, mdv;
+  const int64_t planes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
+  const int T = a.T, dl = p.delta;
+  if (make_band_map(&mk, kr, planes, T, dl, kBR, 1) != SFA_OK ||
+      make_band_map(&mv, a.v, planes, T, dl, kBR, 1) != SFA_OK ||
+      make_band_map(&mq, a.q, qplanes, T, dl, BU, G) != SFA_OK ||
+      make_band_map(&mdo, a.dO, qplanes, T, dl, BU, G) != SFA_OK ||
+      make_band_map(&mo, a.o, qplanes, T, dl, BU, G) != SFA_OK ||
+      make_band_map(&mqt, qt, qplanes, T, dl, BU, G) != SFA_OK ||
+      make_band_map(&mdq, a.dq, qplanes, T, dl, BU, G) != SFA_OK ||
+      make_band_map(&mdk, a.dk, planes, T, dl, kBR, 1) != SFA_OK ||
+      make_band_map(&mdv, a.dv, planes, T, dl, kBR, 1) != SFA_OK)
+    return SFA_ERR_CUDA;
+  if (cudaFuncSetAttribute(band_bwd_q_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kBandBwdQSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(band_bwd_kv_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kBandBwdKvSmem) != cudaSuccess)
+    return SFA_ERR_CUDA;
+  const int Uc = T / dl;
+  float2* st = static_cast<float2*>(stat);
+  {
+    dim3 grid((unsigned)(dl * ((Uc + BU - 1) / BU)), (unsigned)(a.B * a.Hkv));
+    LaunchTimer tm(SFA_KERNEL_BWD_Q, s);
+    band_bwd_q_kernel<G><<<grid, kBThreads, kBandBwdQSmem, s>>>(a, mk, mv, mq, mdo, mo, mqt, mdq, st, p);
+    if (cudaGetLastError() != cudaSuccess) return SFA_ERR_CUDA;
+  }
+  dim3 grid((unsigned)(dl * ((Uc + kBR - 1) / kBR)), (unsigned)(a.B * a.Hkv));
+  LaunchTimer tm(SFA_KERNEL_BWD_KV, s);
+  band_bwd_kv_kernel<G><<<grid, kBThreads, kBandBwdKvSmem, s>>>(a, mk, mv, mqt, mdo, mdk, mdv, st, p);
+  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+int launch_band_backward(const AttnArgs& a, const BandPlan& p, const void* kr, void* qt,
+                         void* stat, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (a.lgG) {
+    case 0: return band_bwd_launch<1>(a, p, kr, qt, stat, s);
+    case 1: return band_bwd_launch<2>(a, p, kr, qt, stat, s);
+    case 2: return band_bwd_launch<4>(a, p, kr, qt, stat, s);
+    case 3: return band_bwd_launch<8>(a, p, kr, qt, stat, s);
+    default: return SFA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace sfa

@@ -122,6 +122,26 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
   return SFA_OK;
 }
 
+int sfa_band_plan(const int32_t* dist, int32_t n_dist, int32_t T, int32_t G, int32_t* delta,
+                  int32_t* run_start, int32_t* run_len, int32_t cap, int32_t* n_runs) {
+  if (!delta || !n_runs || T <= 0 || G <= 0 || cap < 0) return SFA_ERR_INVALID_ARG;
+  std::vector<int32_t> s((size_t)(n_dist > 0 ? n_dist : 0));
+  int32_t n = 0;
+  int rc = sfa_int_distances(dist, n_dist, s.data(), n_dist, &n);
+  if (rc != SFA_OK) return rc;
+  sfa::BandPlan p;
+  sfa::band_plan_of(s.data(), n, T, G, &p);
+  *delta = p.delta;
+  *n_runs = p.nruns;
+  if (p.nruns > cap) return SFA_ERR_CAPACITY;
+  if (p.nruns > 0 && (!run_start || !run_len)) return SFA_ERR_INVALID_ARG;
+  for (int32_t m = 0; m < p.nruns; ++m) {
+    run_start[m] = p.a[m];
+    run_len[m] = p.len[m];
+  }
+  return SFA_OK;
+}
+
 const char* sfa_status_string(int s) {
   switch (s) {
     case SFA_OK: return "ok";
@@ -195,6 +215,68 @@ int build_int_plan(const sfa_desc* d, Plan* p) {
     p->f[r] = 0.0f;
   }
   return SFA_OK;
+}
+
+// Band plan.  For each step delta <= 64 dividing T, the set splits into runs
+// of step delta (a distance extends the run of s - delta when that is in the
+// set); a query tile of 64 / G positions then meets ceil((64 / G + len - 1) /
+// 64) key tiles of 64 rows per run.  The step with the fewest tiles wins
+// (the smallest on ties); the plan is used when at least one product in
+// eight is a wanted (query, key) pair, i.e. n >= 8 x tiles.  Distances >= T
+// reach no key and are left out.
+int band_plan_of(const int32_t* s, int n, int T, int G, BandPlan* p) {
+  p->delta = 0;
+  p->nruns = 0;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return SFA_OK;
+  if (n <= 0 || s[0] != 0) return SFA_OK;  // signed sets, or no distance 0
+  int m = n;
+  while (m > 0 && s[m - 1] >= T) --m;
+  const int BU = 64 / G;
+  int64_t best = -1;
+  std::vector<int32_t> ra, rl, run_of((size_t)m);
+  for (int delta = 1; delta <= kMaxBandDelta && delta <= T; ++delta) {
+    if (T % delta) continue;
+    ra.clear();
+    rl.clear();
+    for (int x = 0; x < m; ++x) {
+      const int32_t prev = s[x] - delta;
+      const int32_t* it = std::lower_bound(s, s + x, prev);
+      if (prev >= 0 && it != s + x && *it == prev) {
+        run_of[(size_t)x] = run_of[(size_t)(it - s)];
+        ++rl[(size_t)run_of[(size_t)x]];
+      } else {
+        run_of[(size_t)x] = (int32_t)ra.size();
+        ra.push_back(s[x]);
+        rl.push_back(1);
+      }
+    }
+    if (ra.size() > (size_t)kMaxRuns) continue;
+    int64_t cost = 0;
+    for (int32_t len : rl) cost += (BU + len - 1 + 63) / 64;
+    if (best < 0 || cost < best) {
+      best = cost;
+      p->delta = delta;
+      p->nruns = (int32_t)ra.size();
+      std::copy(ra.begin(), ra.end(), p->a);
+      std::copy(rl.begin(), rl.end(), p->len);
+    }
+  }
+  if (best < 0 || (int64_t)m < 8 * best) {
+    p->delta = 0;
+    p->nruns = 0;
+  }
+  return SFA_OK;
+}
+
+int build_band_plan(const sfa_desc* d, BandPlan* p) {
+  p->delta = 0;
+  p->nruns = 0;
+  if (d->dtype != SFA_BF16 || d->n_dist <= 0 || !d->dist) return SFA_OK;
+  std::vector<int32_t> s((size_t)d->n_dist);
+  int32_t n = 0;
+  int rc = sfa_int_distances(d->dist, d->n_dist, s.data(), d->n_dist, &n);
+  if (rc != SFA_OK) return rc;
+  return band_plan_of(s.data(), n, d->T, d->Hq / d->Hkv, p);
 }
 
 }  // namespace sfa

@@ -25,6 +25,21 @@ struct Plan {
   float f[kMaxRungs];
 };
 
+// A distance set written as runs of one step delta (delta divides T): run m
+// holds the distances a[m] + delta * t, 0 <= t < len[m].  With i = r + delta u
+// (r = i mod delta), run m sends the queries of residue class r to the keys
+// of class rho = (r - a[m]) mod delta at compressed indices
+// v in [u + e - len[m] + 1, u + e], e = floor((r - a[m]) / delta): a band, so
+// a tile of queries meets a contiguous tile of keys (the band kernels).
+constexpr int kMaxRuns = 128;
+constexpr int kMaxBandDelta = 64;
+struct BandPlan {
+  int32_t delta;  // 0: the set is not served by the band kernels
+  int32_t nruns;
+  int32_t a[kMaxRuns];
+  int32_t len[kMaxRuns];
+};
+
 // Pointers and sizes of one call, passed by value to every kernel.
 // Tensor element type is bf16 or fp32 (a template parameter of the kernels).
 struct AttnArgs {
@@ -69,6 +84,12 @@ int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 int launch_decode_int(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 int launch_backward(const AttnArgs& a, const Plan& p, int dtype, void* stream);
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p);
+// Band kernels (bf16 I/O, G in {1, 2, 4, 8}, integer sets with a band plan).
+int launch_band_forward(const AttnArgs& a, const BandPlan& p, const void* kr, void* stream);
+size_t band_backward_workspace_bytes(const sfa_desc* d, size_t* off_kr, size_t* off_qt,
+                                     size_t* off_stat);
+int launch_band_backward(const AttnArgs& a, const BandPlan& p, const void* kr, void* qt,
+                         void* stat, void* stream);
 
 // Optional launch timing (sfa_api.cu): returns a record id or -1 when off.
 int timing_start(int kind, void* stream);
@@ -85,6 +106,10 @@ struct LaunchTimer {
 // Host helpers (sfa_host.cpp).
 int build_interp_plan(const sfa_desc* d, Plan* p);
 int build_int_plan(const sfa_desc* d, Plan* p);
+// Band plan of a sorted, distinct, non-negative distance set for G query heads
+// per KV head; p->delta = 0 when the band kernels would not pay.
+int band_plan_of(const int32_t* s, int n, int T, int G, BandPlan* p);
+int build_band_plan(const sfa_desc* d, BandPlan* p);
 int validate_shape(const sfa_desc* d);
 
 }  // namespace sfa

@@ -80,6 +80,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];\n" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Wait until the committed stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() {

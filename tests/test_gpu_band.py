@@ -1,0 +1,183 @@
+"""GPU parity of the band kernels: integer bf16 distance sets that split into
+long arithmetic runs of one step delta (the Christoffel carry-word offsets
+of "Christoffel-Balanced Sparse Attention" with m | k, dense windows, the
+full causal set, and mixed windows with a strided tail), for G = 1, 2, 4
+and 8 query heads per KV head.  Forward and backward against the fp64
+oracle on the same seeded inputs, with the bounds of the other parity
+tests; ragged tails (T / delta not a multiple of the tile) included."""
+import numpy as np
+import pytest
+
+import oracle as o
+import sfa_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sfa(sfa_lib):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import static_offset_sparse_gb300 as s
+
+    return s
+
+
+def _check(name, got, want):
+    lim = 2e-2 + 2.0 ** -8 * np.abs(want)
+    err = np.abs(got - want)
+    assert np.isfinite(got).all(), f"{name}: non-finite"
+    assert (err <= lim).all(), f"{name}: max err {err.max():.3g}"
+
+
+SETS = {
+    "christoffel32_256": o.christoffel_offsets(32, 256, include_zero=True),
+    "christoffel128_1024": o.christoffel_offsets(128, 1024, include_zero=True),
+    "window64": list(range(64)),
+    "window_stride4": list(range(16)) + [19 + 4 * t for t in range(80)],
+}
+# (B, T, Hq, Hkv): G = 1, 2, 4, 8; T / delta leaves a ragged last tile
+SHAPES = [(1, 200, 2, 2), (2, 456, 4, 2), (1, 1000, 8, 2), (1, 456, 8, 1)]
+CASES = [(n, s) for n in sorted(SETS) for s in SHAPES
+         if not (n == "window_stride4" and s[1] == 200)]
+
+
+def _run(sfa, x, dist, theta, k_rot=False):
+    import torch
+
+    dev = {n: t.cuda() for n, t in x.items()}
+    kw = {}
+    if k_rot:
+        kw["k_rot"] = sfa.rope_keys(dev["k"], rope_theta=theta)
+    O, L = sfa.forward_int(dev["q"], dev["k"], dev["v"], dist=dist, rope_theta=theta, **kw)
+    g = sfa.backward_int(dev["q"], dev["k"], dev["v"], O, L, dev["do"], dist=dist,
+                         rope_theta=theta, **kw)
+    torch.cuda.synchronize()
+    assert sfa.get_device_status() == 0
+    return O, L, g
+
+
+def _f64(t):
+    import torch
+
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@pytest.mark.parametrize("name,shape", CASES)
+def test_band_forward_backward(sfa, name, shape):
+    B, T, Hq, Hkv = shape
+    dist = SETS[name]
+    delta, runs = sfa.band_plan(dist, T, Hq // Hkv)
+    assert delta > 0, "the set must take the band kernels"
+    x = si.make_qkvdo(B, T, Hq, Hkv, 64, "bf16", seed=1300 + T + len(dist))
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    _check("O", _f64(O), Ow)
+    assert np.abs(_f64(L) - Lw).max() <= 2e-2
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_band_full_causal(sfa, shape):
+    """Every distance 0..T-1: dense causal attention as one run of step 1."""
+    B, T, Hq, Hkv = shape
+    dist = list(range(T))
+    assert sfa.band_plan(dist, T, Hq // Hkv) == (1, [(0, T)])
+    x = si.make_qkvdo(B, T, Hq, Hkv, 64, "bf16", seed=1400 + T)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    _check("O", _f64(O), Ow)
+    assert np.abs(_f64(L) - Lw).max() <= 2e-2
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_band_no_rope(sfa, G):
+    dist = SETS["christoffel32_256"]
+    B, T, Hkv = 1, 512, 2
+    x = si.make_qkvdo(B, T, G * Hkv, Hkv, 64, "bf16", seed=1500 + G)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 0.0)
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 0.0)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 0.0)
+    _check("O", _f64(O), Ow)
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
+
+
+def test_band_k_rot_reuse_is_bit_identical(sfa):
+    """Rotated keys handed in (one rotation shared by forward and backward)
+    give the same bits as rotating inside each call."""
+    import torch
+
+    dist = SETS["christoffel128_1024"]
+    x = si.make_qkvdo(2, 1024, 4, 4, 64, "bf16", seed=1600)
+    a = _run(sfa, x, dist, 1e4)
+    b = _run(sfa, x, dist, 1e4, k_rot=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for u, w in zip(a[2], b[2]):
+        assert torch.equal(u, w)
+
+
+def test_band_is_deterministic(sfa):
+    import torch
+
+    dist = SETS["window_stride4"]
+    x = si.make_qkvdo(1, 1000, 8, 2, 64, "bf16", seed=1700)
+    a = _run(sfa, x, dist, 1e4)
+    b = _run(sfa, x, dist, 1e4)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for u, w in zip(a[2], b[2]):
+        assert torch.equal(u, w)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_band_fallback_when_delta_does_not_divide_T(sfa, G):
+    """T = 201 is not a multiple of the Christoffel step 8: no band plan; the
+    set runs the rung (G = 4) or SIMT (G = 1) kernels with the same result."""
+    dist = SETS["christoffel32_256"]
+    B, T, Hkv = 1, 201, 2
+    assert sfa.band_plan(dist, T, G)[0] == 0
+    x = si.make_qkvdo(B, T, G * Hkv, Hkv, 64, "bf16", seed=1800 + G)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    slots = o.dist_slots(dist)
+    Ow, _ = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    _check("O", _f64(O), Ow)
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
+
+
+def test_band_christoffel_gqa_full_size_sampled(sfa):
+    """The Christoffel 128/1024 set with 8 query heads over 2 KV heads (G = 4,
+    formerly the rung kernels) at B = 4, T = 2048; one (batch, KV head) unit
+    against the oracle."""
+    import torch
+
+    dist = SETS["christoffel128_1024"]
+    x = si.make_qkvdo(4, 2048, 8, 2, 64, "bf16", seed=1900)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    rows = [(3, 1)]
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4, rows=rows)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4, rows=rows)
+    b, g = rows[0]
+    hs = slice(4 * g, 4 * g + 4)
+    _check("O", _f64(O)[b, hs], Ow[b, hs])
+    assert np.abs(_f64(L)[b, hs] - Lw[b, hs]).max() <= 2e-2
+    _check("dQ", _f64(dq)[b, hs], gw["dq"][b, hs])
+    _check("dK", _f64(dk)[b, g], gw["dk"][b, g])
+    _check("dV", _f64(dv)[b, g], gw["dv"][b, g])
+    assert torch.isfinite(dk).all() and torch.isfinite(dv).all()
