@@ -19,10 +19,11 @@
 // one of stride delta rows; rows outside the sequence are zero-filled).
 // Products are mma.sync m16n8k16 (bf16 in, fp32 accumulate) on dense
 // 16 x 64 per-warp tiles, masked only at the band's edges:
-//  * band_fwd:    S = q'.K'^T, online softmax in base 2, O += P.V; O, LSE.
+//  * band_fwd:    S = q~.K'^T (q~ = q'/8 in bf16, as the backward has it),
+//                 online softmax in base 2, O += P.V; O, LSE.
 //  * band_bwd_q:  S and dP = dO.V^T recomputed, P = exp(S - LSE),
 //                 dS = P (dP - delta_i), dQ += dS.K'; writes dQ = R(-phi) dQ'
-//                 / 8, q~ = q'/8 and per row (LSE log2(e), delta_i).
+//                 / 8, q~ = q'/8 and per row (LSE log2(e), sum_j P dP).
 //  * band_bwd_kv: per 64-key tile, the query tiles of each run that reach
 //                 it, keys on the mma M side: S^T = K'.q~^T, dP^T = V.dO^T,
 //                 dV += P^T.dO, dK' += dS^T.q~; dK = R(-phi) dK'.  Each key
@@ -187,6 +188,31 @@ __device__ __forceinline__ void band_store_rows(uint32_t tile, int row0, const f
 #pragma unroll
     for (int nd = 0; nd < 8; ++nd)
       st_shared_u32(band_out_addr(tile, row0 + gid + 8 * x, nd), pack_bf16(w[nd][0], w[nd][1]));
+  }
+}
+
+// x as bf16 hi + lo pairs (hi = bf16(x), lo = bf16(x - hi)): about 16
+// mantissa bits for the key side's sums over many queries.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  const float2 h = unpack_bf16(hi);
+  lo = pack_bf16(x0 - h.x, x1 - h.y);
+}
+
+// acc[16 x 64] += (A_hi + A_lo)[16 x 16] . rows[16 x 64] (as pv_tile, one set
+// of B loads for both parts).
+__device__ __forceinline__ void pv_tile2(const uint32_t* ah, const uint32_t* al, uint32_t region,
+                                         int row_lo, int row_hi, float (*acc)[4]) {
+  const int mi = (threadIdx.x & 31) >> 3;
+  const int row = (mi & 1) ? row_hi : row_lo;
+#pragma unroll
+  for (int nd = 0; nd < 8; nd += 2) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(region + swz(row, nd + (mi >> 1)), b0, b1, b2, b3);
+    mma_bf16(acc[nd], ah, b0, b1);
+    mma_bf16(acc[nd + 1], ah, b2, b3);
+    mma_bf16(acc[nd], al, b0, b1);
+    mma_bf16(acc[nd + 1], al, b2, b3);
   }
 }
 
@@ -363,8 +389,11 @@ __global__ void __launch_bounds__(kBThreads, 3)
     band_drain(bars, NT);
     return;
   }
+  // q~ = q'/8 rounded exactly as the backward rounds it, log2(e) applied to
+  // the fp32 logits: the backward's P = exp(S - LSE) then recomputes this
+  // kernel's logits bit for bit and stays normalised
   uint32_t qa[4][4];
-  band_frags(qtile, 16 * warp, static_cast<const float2*>(a.rope), q.pos, 0.125f * kLog2e, true, qa);
+  band_frags(qtile, 16 * warp, static_cast<const float2*>(a.rope), q.pos, 0.125f, true, qa);
   float o[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
@@ -387,7 +416,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int x = e >> 1, col = 8 * nt + 2 * tig + (e & 1);
-        s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] : -INFINITY;
+        s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
       }
     band_softmax(s, m, l, o);
     const uint32_t vst = kst + kBTileB;
@@ -484,8 +513,6 @@ __global__ void __launch_bounds__(kBThreads, 3)
       acc[x] += __shfl_xor_sync(0xffffffffu, acc[x], 1);
       acc[x] += __shfl_xor_sync(0xffffffffu, acc[x], 2);
       dlt[x] = acc[x];
-      if (tig == 0 && q.uu[x] < q.Uc)
-        stat[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] = make_float2(lse2[x], dlt[x]);
     }
   }
   __syncthreads();  // the O tile is read: it now carries q~ = q'/8 out for the key side
@@ -505,6 +532,10 @@ __global__ void __launch_bounds__(kBThreads, 3)
   float dq[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
+  // delta_i again as sum_j P_ij dP_ij in fp32 (equal to dO . O in exact
+  // arithmetic, free of the rounding of the stored O) for the key side,
+  // whose sums over many queries would collect that rounding
+  float psum[2] = {0.0f, 0.0f};
   QWalk cw{0, 0, 0, 0, 0};
   qwalk_seek(P, q.r, q.u0, q.ul, cw);
 
@@ -532,6 +563,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
           const float pr =
               (col >= lo[x] && col <= hi[x]) ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x])) : 0.0f;
           ds[nt][e] = pr * (dp[nt][e] - dlt[x]);
+          psum[x] = fmaf(pr, dp[nt][e], psum[x]);
         }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
@@ -548,6 +580,13 @@ __global__ void __launch_bounds__(kBThreads, 3)
   if (!ok) {
     if (threadIdx.x == 0) bulk_wait_read();
     return;
+  }
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    psum[x] += __shfl_xor_sync(0xffffffffu, psum[x], 1);
+    psum[x] += __shfl_xor_sync(0xffffffffu, psum[x], 2);
+    if (tig == 0 && q.uu[x] < q.Uc)
+      stat[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] = make_float2(lse2[x], psum[x]);
   }
   const float eighth[2] = {0.125f, 0.125f};
   band_store_rows(qtile, 16 * warp, dq, eighth, rope, q.pos);  // dQ = R(-phi) dQ' / 8
@@ -658,19 +697,20 @@ __global__ void __launch_bounds__(kBThreads, 2)
           pp[nt][e] = pr;
           ds[nt][e] = pr * (dpt[nt][e] - sd[nt][c].y);
         }
+      // a key row sums P and dS over up to G x len (query, head) pairs, with
+      // sum P above 1 for the early keys: both go in as bf16 hi + lo
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t pa[4] = {pack_bf16(pp[2 * ks][0], pp[2 * ks][1]),
-                                pack_bf16(pp[2 * ks][2], pp[2 * ks][3]),
-                                pack_bf16(pp[2 * ks + 1][0], pp[2 * ks + 1][1]),
-                                pack_bf16(pp[2 * ks + 1][2], pp[2 * ks + 1][3])};
-        const uint32_t sa[4] = {pack_bf16(ds[2 * ks][0], ds[2 * ks][1]),
-                                pack_bf16(ds[2 * ks][2], ds[2 * ks][3]),
-                                pack_bf16(ds[2 * ks + 1][0], ds[2 * ks + 1][1]),
-                                pack_bf16(ds[2 * ks + 1][2], ds[2 * ks + 1][3])};
+        uint32_t ph[4], pl[4], sh[4], sl[4];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const int nt = 2 * ks + (y >> 1), e = 2 * (y & 1);
+          split_bf16(pp[nt][e], pp[nt][e + 1], ph[y], pl[y]);
+          split_bf16(ds[nt][e], ds[nt][e + 1], sh[y], sl[y]);
+        }
         const int rl = 32 * hq + 16 * ks + (lane & 7);
-        pv_tile(pa, dst, rl, rl + 8, dv);
-        pv_tile(sa, qst, rl, rl + 8, dk);
+        pv_tile2(ph, pl, dst, rl, rl + 8, dv);
+        pv_tile2(sh, sl, qst, rl, rl + 8, dk);
       }
     }
     kwalk_next(P, rho, v0, vl, Uc, BU, cw);

@@ -6,8 +6,8 @@
 // accumulate):
 //
 //  * A warp owns 4 consecutive query positions x the 4 heads of one KV
-//    group = 16 rows (row r = 4 h + p).  Its q' (rotated, scaled by
-//    log2(e)/8) stays in registers as bf16 A fragments.
+//    group = 16 rows (row r = 4 h + p).  Its q~ = q'/8 (rotated, scaled)
+//    stays in registers as bf16 A fragments; logits take log2(e) in fp32.
 //  * Keys are the raw rotated rows K' (bf16, written by the prep kernel) and
 //    raw V rows, staged per CTA as contiguous shifted slabs by TMA (rows
 //    outside the sequence are zero-filled by the copy engine).
@@ -99,7 +99,10 @@ __global__ void __launch_bounds__(kTcThreads, 5)
   tc_start(&mk, &mv, qmaps, 1, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
   if (!tc_wait_qtiles(bars, a.status)) return;
   uint32_t qa[4][4];
-  tile_frags(qtile, warp, rope, min(i, T - 1), 0.125f * kLog2e, true, qa);
+  // q~ = q'/8 rounded exactly as the query-side backward rounds it, log2(e)
+  // applied to the fp32 logits: the backward's P = exp(S - LSE) recomputes
+  // this kernel's logits bit for bit and stays normalised
+  tile_frags(qtile, warp, rope, min(i, T - 1), 0.125f, true, qa);
   float o[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kTcThreads, 5)
         for (int e = 0; e < 4; ++e) {
           const int dist = p + 12 + s_lo - (8 * nt + 2 * tig + (e & 1));
           const bool v = dist >= s_lo && dist <= s_hi && dist <= i;
-          s[e >> 1][2 * nt + (e & 1)] = v ? acc[nt][e] : -INFINITY;
+          s[e >> 1][2 * nt + (e & 1)] = v ? acc[nt][e] * kLog2e : -INFINITY;
         }
       softmax_step(s, std::integral_constant<int, 4>());
       pa[0] = pack_bf16(s[0][0], s[0][1]);
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, 5)
         const bool v = rg < nr && p == tig && i >= P.c[rg];
         const float w = (INTERP && rg < nr) ? P.w[rg] : 0.0f;
         wgt[x] = w;
-        s[0][x] = v ? fmaf(w, acc[1], (1.0f - w) * acc[0]) : -INFINITY;
-        s[1][x] = v ? fmaf(w, acc[3], (1.0f - w) * acc[2]) : -INFINITY;
+        s[0][x] = v ? fmaf(w, acc[1], (1.0f - w) * acc[0]) * kLog2e : -INFINITY;
+        s[1][x] = v ? fmaf(w, acc[3], (1.0f - w) * acc[2]) * kLog2e : -INFINITY;
       }
       softmax_step(s, std::integral_constant<int, 2>());
       pa[0] = pack_bf16(s[0][0] * (1.0f - wgt[0]), s[0][0] * wgt[0]);
