@@ -216,6 +216,23 @@ __device__ __forceinline__ void pv_tile2(const uint32_t* ah, const uint32_t* al,
   }
 }
 
+// acc0 += A0 . rows and acc1 += A1 . rows for one set of B loads.
+__device__ __forceinline__ void pv_tile2(const uint32_t* a0, const uint32_t* a1, uint32_t region,
+                                         int row_lo, int row_hi, float (*acc0)[4],
+                                         float (*acc1)[4]) {
+  const int mi = (threadIdx.x & 31) >> 3;
+  const int row = (mi & 1) ? row_hi : row_lo;
+#pragma unroll
+  for (int nd = 0; nd < 8; nd += 2) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(region + swz(row, nd + (mi >> 1)), b0, b1, b2, b3);
+    mma_bf16(acc0[nd], a0, b0, b1);
+    mma_bf16(acc0[nd + 1], a0, b2, b3);
+    mma_bf16(acc1[nd], a1, b0, b1);
+    mma_bf16(acc1[nd + 1], a1, b2, b3);
+  }
+}
+
 // Barriers: kBStages stage barriers, then one for the CTA's own tiles.
 __device__ __forceinline__ void band_init_bars(uint64_t* bars) {
   if (threadIdx.x == 0) {
@@ -532,10 +549,16 @@ __global__ void __launch_bounds__(kBThreads, 3)
   float dq[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
-  // delta_i again as sum_j P_ij dP_ij in fp32 (equal to dO . O in exact
-  // arithmetic, free of the rounding of the stored O) for the key side,
-  // whose sums over many queries would collect that rounding
+  // delta_i is dO . O from the stored (bf16) O; the exact value is
+  // sum_j P_ij dP_ij (fp32 here), and with |dP| in the tens the difference
+  // shifts dS visibly.  The loop uses the O value and also sums
+  // psum = sum_j P_ij dP_ij and kbar = sum_j P_ij K'_j; at the end
+  // dQ' += (delta - psum) kbar makes dQ' = sum_j P_ij (dP_ij - psum) K'_j, and
+  // the key side reads psum.
   float psum[2] = {0.0f, 0.0f};
+  float kbar[8][4];
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) kbar[nd][0] = kbar[nd][1] = kbar[nd][2] = kbar[nd][3] = 0.0f;
   QWalk cw{0, 0, 0, 0, 0};
   qwalk_seek(P, q.r, q.u0, q.ul, cw);
 
@@ -554,7 +577,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
         qk_tile(qa, kst, row, sc[nt]);
         qk_tile(da, vst, row, dp[nt]);
       }
-      float ds[4][4];
+      float ds[4][4], pp[4][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -563,6 +586,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
           const float pr =
               (col >= lo[x] && col <= hi[x]) ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x])) : 0.0f;
           ds[nt][e] = pr * (dp[nt][e] - dlt[x]);
+          pp[nt][e] = pr;
           psum[x] = fmaf(pr, dp[nt][e], psum[x]);
         }
 #pragma unroll
@@ -571,8 +595,12 @@ __global__ void __launch_bounds__(kBThreads, 3)
                                 pack_bf16(ds[2 * ks][2], ds[2 * ks][3]),
                                 pack_bf16(ds[2 * ks + 1][0], ds[2 * ks + 1][1]),
                                 pack_bf16(ds[2 * ks + 1][2], ds[2 * ks + 1][3])};
+        const uint32_t pa[4] = {pack_bf16(pp[2 * ks][0], pp[2 * ks][1]),
+                                pack_bf16(pp[2 * ks][2], pp[2 * ks][3]),
+                                pack_bf16(pp[2 * ks + 1][0], pp[2 * ks + 1][1]),
+                                pack_bf16(pp[2 * ks + 1][2], pp[2 * ks + 1][3])};
         const int rl = 32 * hf + 16 * ks + (lane & 7);
-        pv_tile(sa, kst, rl, rl + 8, dq);
+        pv_tile2(sa, pa, kst, rl, rl + 8, dq, kbar);
       }
     }
     qwalk_next(P, q.r, q.u0, q.ul, cw);
@@ -587,6 +615,12 @@ __global__ void __launch_bounds__(kBThreads, 3)
     psum[x] += __shfl_xor_sync(0xffffffffu, psum[x], 2);
     if (tig == 0 && q.uu[x] < q.Uc)
       stat[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] = make_float2(lse2[x], psum[x]);
+    const float corr = dlt[x] - psum[x];
+#pragma unroll
+    for (int nd = 0; nd < 8; ++nd) {
+      dq[nd][2 * x] = fmaf(corr, kbar[nd][2 * x], dq[nd][2 * x]);
+      dq[nd][2 * x + 1] = fmaf(corr, kbar[nd][2 * x + 1], dq[nd][2 * x + 1]);
+    }
   }
   const float eighth[2] = {0.125f, 0.125f};
   band_store_rows(qtile, 16 * warp, dq, eighth, rope, q.pos);  // dQ = R(-phi) dQ' / 8
