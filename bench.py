@@ -734,6 +734,7 @@ def configs_arm(args, dev):
         ("4: bf16 integer forward, T=2048, alpha=1", 4, 2048, 8, 2, "bf16", "int", (int_set(1.0, 8),), False),
         ("4: bf16 integer forward, T=16384, alpha=1.5", 4, 16384, 8, 2, "bf16", "int", (int_set(1.5, 8),), False),
         ("5: bf16 Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int", (chris(),), True),
+        ("5 with 8/2 heads (G = 4)", 16, 2048, 8, 2, "bf16", "int", (chris(),), True),
     ]
     out = []
     for name, Bc, Tc, Hq, Hkv, dt, kind, par, bwd in cases:
@@ -767,11 +768,25 @@ def configs_arm(args, dev):
         torch.cuda.synchronize()
         assert sfa.get_device_status() == 0
         ms = ev0.elapsed_time(ev1) / n
-        path = "tensor cores" if dt == "bf16" and Hq == 4 * Hkv and not (kind == "int" and min(par[0]) < 0) else "SIMT"
+        # per-kernel device time: one more timed pass with the library's launch events
+        sfa.timing_enable(True)
+        for _ in range(n):
+            call()
+        torch.cuda.synchronize()
+        rec = sfa.timing_read()
+        sfa.timing_enable(False)
+        kernels = {k: round(t / n * 1e3, 2) for k, (t, c) in rec.items() if c}
+        band = kind == "int" and dt == "bf16" and sfa.band_plan(par[0], Tc, Hq // Hkv)[0] > 0
+        if band:
+            path = "band (tensor cores)"
+        elif dt == "bf16" and Hq == 4 * Hkv and not (kind == "int" and min(par[0]) < 0):
+            path = "rung (tensor cores)"
+        else:
+            path = "SIMT"
         out.append({"config": name, "B": Bc, "T": Tc, "heads": f"{Hq}/{Hkv}", "dtype": dt,
                     "direction": "fwd+bwd" if bwd else "fwd", "path": path,
                     "ms_per_call": round(ms, 4), "tokens_per_s": round(Bc * Tc / (ms * 1e-3), 1),
-                    "keys_per_query": keys})
+                    "keys_per_query": keys, "kernel_us_per_call": kernels})
         del x
         torch.cuda.empty_cache()
     return out

@@ -286,13 +286,14 @@ __device__ __forceinline__ void band_drain(uint64_t* bars, int NT) {
     for (int s = 0; s < kBStages && s < NT; ++s) mbar_wait_bounded(smem_u32(&bars[s]), 0);
 }
 
-// Online softmax over one 64-key tile for rows gid (x = 0) and gid + 8 of a
-// lane: s[x][16] holds base-2 logits (invalid = -inf) and comes back as
+// Online softmax over N keys of a tile for rows gid (x = 0) and gid + 8 of a
+// lane: s[x][N] holds base-2 logits (invalid = -inf) and comes back as
 // p = 2^(s - m).  The running maximum m is refreshed only when some logit
 // of the warp exceeds it by more than 8: between refreshes p stays below
 // 2^8, and O = sum p v / sum p and LSE = m + log2 l hold for any m.  m stays
 // uniform over a row's quad (it changes only through the quad reduction).
-__device__ __forceinline__ void band_softmax(float (*s)[16], float* m, float* l, float (*o)[4]) {
+template <int N>
+__device__ __forceinline__ void band_softmax(float (*s)[N], float* m, float* l, float (*o)[4]) {
   constexpr float kMargin = 8.0f;
   float mx[2];
   bool need = false;
@@ -300,7 +301,7 @@ __device__ __forceinline__ void band_softmax(float (*s)[16], float* m, float* l,
   for (int x = 0; x < 2; ++x) {
     mx[x] = s[x][0];
 #pragma unroll
-    for (int e = 1; e < 16; ++e) mx[x] = fmaxf(mx[x], s[x][e]);
+    for (int e = 1; e < N; ++e) mx[x] = fmaxf(mx[x], s[x][e]);
     need |= mx[x] > m[x] + kMargin;  // m = -inf: any valid logit
   }
   if (__any_sync(0xffffffffu, need)) {
@@ -324,7 +325,7 @@ __device__ __forceinline__ void band_softmax(float (*s)[16], float* m, float* l,
   for (int x = 0; x < 2; ++x) {
     const float mm = m[x] == -INFINITY ? 0.0f : m[x];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
+    for (int e = 0; e < N; ++e) {
       const float pe = ex2(s[x][e] - mm);  // ex2(-inf) = 0
       s[x][e] = pe;
       l[x] += pe;
@@ -363,6 +364,21 @@ struct QTile {
     if (qwalk_seek(P, r, u0, ul, w)) do ++n; while (qwalk_next(P, r, u0, ul, w));
     return n;
   }
+  // Positions of this warp's 16 rows: one head's 16 consecutive positions
+  // (64 / G >= 16) or the same 8 positions of two heads (G = 8).
+  __device__ __forceinline__ void warp_span(int& umin, int& umax) const {
+    const int warp = threadIdx.x >> 5;
+    umin = u0 + (BU >= 16 ? (16 * warp) % BU : 0);
+    umax = min(umin + (BU >= 16 ? 15 : BU - 1), Uc - 1);
+  }
+  // The n-tiles (8 key columns each) of the current tile that hold a key of
+  // some row of the warp (bit nt); warp-uniform, 0 when none does.
+  __device__ __forceinline__ unsigned ntmask(const BandPlan& P, const QWalk& w, int umin,
+                                             int umax) const {
+    const int cl = max(0, umin + w.e - P.len[w.m] + 1 - w.vs), ch = min(kBR - 1, umax + w.e - w.vs);
+    if (umin > umax || cl > ch) return 0u;
+    return ((2u << (ch >> 3)) - 1u) & ~((1u << (cl >> 3)) - 1u);
+  }
   // Tile columns [lo, hi] of row x that are keys of the current run.
   __device__ __forceinline__ void cols(const BandPlan& P, const QWalk& w, int* lo, int* hi) const {
     const int len = P.len[w.m];
@@ -375,7 +391,7 @@ struct QTile {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kBThreads, 3)
+__global__ void __launch_bounds__(kBThreads, 4)
     band_fwd_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mo, const __grid_constant__ BandPlan P) {
@@ -419,31 +435,39 @@ __global__ void __launch_bounds__(kBThreads, 3)
   qwalk_seek(P, q.r, q.u0, q.ul, cw);
 
   const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
-    float acc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-      qk_tile(qa, kst, 8 * nt + (lane & 7), acc[nt]);
-    }
+    // every warp computes the whole tile (skipping the n-tiles outside its
+    // rows' bands measured slower: it breaks up the load and product batches
+    // the scheduler overlaps), in two halves of 32 keys with one softmax step
+    // each, which keeps four CTAs per SM within the register file
     int lo[2], hi[2];
     q.cols(P, cw, lo, hi);
-    float s[2][16];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int x = e >> 1, col = 8 * nt + 2 * tig + (e & 1);
-        s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
-      }
-    band_softmax(s, m, l, o);
     const uint32_t vst = kst + kBTileB;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint32_t pa[4] = {pack_bf16(s[0][4 * kk], s[0][4 * kk + 1]),
-                              pack_bf16(s[1][4 * kk], s[1][4 * kk + 1]),
-                              pack_bf16(s[0][4 * kk + 2], s[0][4 * kk + 3]),
-                              pack_bf16(s[1][4 * kk + 2], s[1][4 * kk + 3])};
-      pv_tile(pa, vst, 16 * kk + (lane & 7), 16 * kk + 8 + (lane & 7), o);
+    for (int hf = 0; hf < 2; ++hf) {
+      float acc[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        qk_tile(qa, kst, 32 * hf + 8 * nt + (lane & 7), acc[nt]);
+      }
+      float s[2][8];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
+          s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
+        }
+      band_softmax<8>(s, m, l, o);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t pa[4] = {pack_bf16(s[0][4 * kk], s[0][4 * kk + 1]),
+                                pack_bf16(s[1][4 * kk], s[1][4 * kk + 1]),
+                                pack_bf16(s[0][4 * kk + 2], s[0][4 * kk + 3]),
+                                pack_bf16(s[1][4 * kk + 2], s[1][4 * kk + 3])};
+        const int rl = 32 * hf + 16 * kk + (lane & 7);
+        pv_tile(pa, vst, rl, rl + 8, o);
+      }
     }
     qwalk_next(P, q.r, q.u0, q.ul, cw);
   });
@@ -561,18 +585,24 @@ __global__ void __launch_bounds__(kBThreads, 3)
   for (int nd = 0; nd < 8; ++nd) kbar[nd][0] = kbar[nd][1] = kbar[nd][2] = kbar[nd][3] = 0.0f;
   QWalk cw{0, 0, 0, 0, 0};
   qwalk_seek(P, q.r, q.u0, q.ul, cw);
+  int umin, umax;
+  q.warp_span(umin, umax);
 
   const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
     const uint32_t vst = kst + kBTileB;
     int lo[2], hi[2];
     q.cols(P, cw, lo, hi);
+    const unsigned msk = q.ntmask(P, cw, umin, umax);  // n-tiles the warp's rows read
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {  // keys 32 hf .. 32 hf + 31 of the tile
+      const unsigned mh = (msk >> (4 * hf)) & 15u;
+      if (!mh) continue;
       float sc[4][4], dp[4][4];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
         dp[nt][0] = dp[nt][1] = dp[nt][2] = dp[nt][3] = 0.0f;
+        if (!((mh >> nt) & 1u)) continue;
         const int row = 32 * hf + 8 * nt + (lane & 7);
         qk_tile(qa, kst, row, sc[nt]);
         qk_tile(da, vst, row, dp[nt]);
@@ -583,14 +613,16 @@ __global__ void __launch_bounds__(kBThreads, 3)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
-          const float pr =
-              (col >= lo[x] && col <= hi[x]) ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x])) : 0.0f;
+          const float pr = ((mh >> nt) & 1u) && col >= lo[x] && col <= hi[x]
+                               ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x]))
+                               : 0.0f;
           ds[nt][e] = pr * (dp[nt][e] - dlt[x]);
           pp[nt][e] = pr;
           psum[x] = fmaf(pr, dp[nt][e], psum[x]);
         }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
+        if (!((mh >> (2 * ks)) & 3u)) continue;
         const uint32_t sa[4] = {pack_bf16(ds[2 * ks][0], ds[2 * ks][1]),
                                 pack_bf16(ds[2 * ks][2], ds[2 * ks][3]),
                                 pack_bf16(ds[2 * ks + 1][0], ds[2 * ks + 1][1]),
@@ -634,7 +666,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
 }
 
 template <int G>
-__global__ void __launch_bounds__(kBThreads, 2)
+__global__ void __launch_bounds__(kBThreads, 3)
     band_bwd_kv_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                        const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mqt,
                        const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mdk,
@@ -679,9 +711,6 @@ __global__ void __launch_bounds__(kBThreads, 2)
     band_drain(bars, NT);
     return;
   }
-  uint32_t ka[4][4], va[4][4];
-  band_frags(ktile, 16 * warp, nullptr, nullptr, 1.0f, false, ka);
-  band_frags(vtile, 16 * warp, nullptr, nullptr, 1.0f, false, va);
   float dk[8][4], dv[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) {
@@ -690,6 +719,8 @@ __global__ void __launch_bounds__(kBThreads, 2)
   }
   KWalk cw{0, 0, 0, 0, 0};
   kwalk_seek(P, rho, v0, vl, Uc, cw);
+  // keys of this warp's 16 rows (none past the sequence)
+  const int vmin = v0 + 16 * warp, vmax = min(vmin + 15, Uc - 1);
 
   const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t qst) {
     const uint32_t dst = qst + kBTileB;
@@ -698,8 +729,23 @@ __global__ void __launch_bounds__(kBThreads, 2)
     int tb[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) tb[x] = kv[x] < Uc ? cw.e - kv[x] : -(1 << 30);
+    // n-tiles (8 columns = 8 positions of one head) holding a query that reads
+    // one of the warp's keys: positions [vmin - e, vmax - e + len - 1]; whole
+    // halves of 32 columns are skipped
+    unsigned msk = 0u;
+    {
+      const int ua = max(vmin - cw.e, 0) - cw.us, ub = min(vmax - cw.e + len - 1, Uc - 1) - cw.us;
+      if (vmin <= vmax && ua <= ub)
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const int c0 = (8 * g8) % BU;
+          if (c0 <= ub && c0 + 7 >= ua) msk |= 1u << g8;
+        }
+    }
 #pragma unroll
     for (int hq = 0; hq < 2; ++hq) {  // query rows 32 hq .. 32 hq + 31 of the tile
+      const unsigned mh = (msk >> (4 * hq)) & 15u;
+      if (!mh) continue;
       float2 sd[4][2];
       int uq[4][2];
 #pragma unroll
@@ -712,13 +758,20 @@ __global__ void __launch_bounds__(kBThreads, 2)
           sd[nt][c] = __ldg(stat + (int64_t)(qplane + n / BU) * T + cw.r + delta * min(u, Uc - 1));
         }
       float st[4][4], dpt[4][4];
+      {
+        // the warp's K' and V rows as A fragments, from the CTA's tiles (kept
+        // in shared memory rather than in 32 registers for the whole CTA)
+        uint32_t ka[4][4], va[4][4];
+        band_frags(ktile, 16 * warp, nullptr, nullptr, 1.0f, false, ka);
+        band_frags(vtile, 16 * warp, nullptr, nullptr, 1.0f, false, va);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.0f;
-        dpt[nt][0] = dpt[nt][1] = dpt[nt][2] = dpt[nt][3] = 0.0f;
-        const int row = 32 * hq + 8 * nt + (lane & 7);
-        qk_tile(ka, qst, row, st[nt]);
-        qk_tile(va, dst, row, dpt[nt]);
+        for (int nt = 0; nt < 4; ++nt) {
+          st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.0f;
+          dpt[nt][0] = dpt[nt][1] = dpt[nt][2] = dpt[nt][3] = 0.0f;
+          const int row = 32 * hq + 8 * nt + (lane & 7);
+          qk_tile(ka, qst, row, st[nt]);
+          qk_tile(va, dst, row, dpt[nt]);
+        }
       }
       float pp[4][4], ds[4][4];
 #pragma unroll
