@@ -191,6 +191,26 @@ __device__ __forceinline__ void band_store_rows(uint32_t tile, int row0, const f
   }
 }
 
+// acc[nt] += A . rows(row0 + 8 nt .. + 7)^T for four n-tiles, k-step outer:
+// consecutive products go to different accumulators (qk_tile's four
+// products chain on one).  B fragments of two k-steps are live at a time.
+__device__ __forceinline__ void qk_tiles4(const uint32_t (*qa)[4], uint32_t region, int row0,
+                                          float (*acc)[4]) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3;
+#pragma unroll
+  for (int hk = 0; hk < 2; ++hk) {  // dims 32 hk .. 32 hk + 31: k-steps 2 hk, 2 hk + 1
+    uint32_t b[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+      ldsm_x4(region + swz(row0 + 8 * nt + (lane & 7), 4 * hk + mi), b[nt][0], b[nt][1], b[nt][2],
+              b[nt][3]);
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) mma_bf16(acc[nt], qa[2 * hk + k2], b[nt][2 * k2], b[nt][2 * k2 + 1]);
+  }
+}
+
 // x as bf16 hi + lo pairs (hi = bf16(x), lo = bf16(x - hi)): about 16
 // mantissa bits for the key side's sums over many queries.
 __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -446,10 +466,8 @@ __global__ void __launch_bounds__(kBThreads, 4)
     for (int hf = 0; hf < 2; ++hf) {
       float acc[4][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-        qk_tile(qa, kst, 32 * hf + 8 * nt + (lane & 7), acc[nt]);
-      }
+      for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+      qk_tiles4(qa, kst, 32 * hf, acc);
       float s[2][8];
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
@@ -768,10 +786,9 @@ __global__ void __launch_bounds__(kBThreads, 3)
         for (int nt = 0; nt < 4; ++nt) {
           st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.0f;
           dpt[nt][0] = dpt[nt][1] = dpt[nt][2] = dpt[nt][3] = 0.0f;
-          const int row = 32 * hq + 8 * nt + (lane & 7);
-          qk_tile(ka, qst, row, st[nt]);
-          qk_tile(va, dst, row, dpt[nt]);
         }
+        qk_tiles4(ka, qst, 32 * hq, st);
+        qk_tiles4(va, dst, 32 * hq, dpt);
       }
       float pp[4][4], ds[4][4];
 #pragma unroll
