@@ -736,6 +736,8 @@ def configs_arm(args, dev):
         ("5: bf16 Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int", (chris(),), True),
         ("5 with 8/2 heads (G = 4)", 16, 2048, 8, 2, "bf16", "int", (chris(),), True),
     ]
+    if args.only:
+        cases = [c for c in cases if c[0].startswith(args.only)]
     out = []
     for name, Bc, Tc, Hq, Hkv, dt, kind, par, bwd in cases:
         x = si.make_qkvdo_device(Bc, Tc, Hq, Hkv, D, dt, SEED, dev, layer=7)
@@ -811,6 +813,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
+    ap.add_argument("--only", default="", help="configs mode: run the configurations whose name "
+                    "starts with this (e.g. '5:')")
     ap.add_argument("--mode", default="train", choices=["train", "decode", "configs"],
                     help="train: the fwd+bwd step (default); decode: one token per sequence; "
                          "configs: one line per configuration of the pages")
