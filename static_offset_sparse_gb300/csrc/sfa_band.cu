@@ -253,13 +253,16 @@ __device__ __forceinline__ void pv_tile2(const uint32_t* a0, const uint32_t* a1,
   }
 }
 
-// Barriers: kBStages stage barriers, then one for the CTA's own tiles.
+// Barriers: kBStages stage barriers, then one for the CTA's own tiles; the
+// dependent-launch handshake (no global access before it).
 __device__ __forceinline__ void band_init_bars(uint64_t* bars) {
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s <= kBStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's outputs are complete from here on
 }
 
 // Bounded wait on a barrier, uniform across the CTA (false: timed out, the
@@ -853,8 +856,10 @@ static int band_fwd_launch(const AttnArgs& a, const BandPlan& p, const void* kr,
   const int Uc = a.T / p.delta;
   dim3 grid((unsigned)(p.delta * ((Uc + BU - 1) / BU)), (unsigned)(a.B * a.Hkv));
   LaunchTimer tm(SFA_KERNEL_FWD, s);
-  band_fwd_kernel<G><<<grid, kBThreads, kBandFwdSmem, s>>>(a, mk, mv, mq, mo, p);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+  return launch_pdl(band_fwd_kernel<G>, grid, dim3(kBThreads), kBandFwdSmem, s, a, mk, mv, mq, mo,
+                    p) == cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
 }
 
 int launch_band_forward(const AttnArgs& a, const BandPlan& p, const void* kr, void* stream) {
@@ -904,13 +909,16 @@ static int band_bwd_launch(const AttnArgs& a, const BandPlan& p, const void* kr,
   {
     dim3 grid((unsigned)(dl * ((Uc + BU - 1) / BU)), (unsigned)(a.B * a.Hkv));
     LaunchTimer tm(SFA_KERNEL_BWD_Q, s);
-    band_bwd_q_kernel<G><<<grid, kBThreads, kBandBwdQSmem, s>>>(a, mk, mv, mq, mdo, mo, mqt, mdq, st, p);
-    if (cudaGetLastError() != cudaSuccess) return SFA_ERR_CUDA;
+    if (launch_pdl(band_bwd_q_kernel<G>, grid, dim3(kBThreads), kBandBwdQSmem, s, a, mk, mv, mq, mdo,
+                   mo, mqt, mdq, st, p) != cudaSuccess)
+      return SFA_ERR_CUDA;
   }
   dim3 grid((unsigned)(dl * ((Uc + kBR - 1) / kBR)), (unsigned)(a.B * a.Hkv));
   LaunchTimer tm(SFA_KERNEL_BWD_KV, s);
-  band_bwd_kv_kernel<G><<<grid, kBThreads, kBandBwdKvSmem, s>>>(a, mk, mv, mqt, mdo, mdk, mdv, st, p);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+  return launch_pdl(band_bwd_kv_kernel<G>, grid, dim3(kBThreads), kBandBwdKvSmem, s, a, mk, mv, mqt,
+                    mdo, mdk, mdv, static_cast<const float2*>(st), p) == cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
 }
 
 int launch_band_backward(const AttnArgs& a, const BandPlan& p, const void* kr, void* qt,

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mo,
                     const __grid_constant__ CUtensorMap mqt,
-                    const __grid_constant__ CUtensorMap mdq, uint4* coef, int NS, unsigned* ticket,
+                    const __grid_constant__ CUtensorMap mdq, uint4* coef, int NS,
                     const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bars[kTcStages + 1];
@@ -203,38 +203,17 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   if (!ok) return;
 
   if (INTERP && a.dalpha_out) {
-    // per-CTA partial of dL/dalpha; the last CTA to finish sums all partials
-    // in a fixed order (deterministic) and writes dL/dalpha and dL/dtheta
-    __shared__ bool last;
+    // per-CTA partial of dL/dalpha; the key-side kernel, which runs after this
+    // one, sums the partials in a fixed order (deterministic)
     double d = (double)dacc;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_down_sync(0xffffffffu, d, off);
     if (lane == 0) red[warp] = d;
     __syncthreads();
-    const unsigned nblk = gridDim.x * gridDim.y;
     if (threadIdx.x == 0) {
-      double s = 0.0;
-      for (int x = 0; x < kTcWarps; ++x) s += red[x];
-      a.dalpha_part[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = s;
-      __threadfence();
-      last = atomicAdd(ticket, 1u) == nblk - 1;
-    }
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      const volatile double* part = a.dalpha_part;
-      double s = 0.0;
-      for (unsigned x = threadIdx.x; x < nblk; x += kTcThreads) s += part[x];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xffffffffu, s, off);
-      if (lane == 0) red[warp] = s;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int x = 0; x < kTcWarps; ++x) t += red[x];
-        a.dalpha_out[0] = t;
-        a.dalpha_out[1] = t * (a.alpha - 0.5) * (1.5 - a.alpha);
-      }
+      double sum = 0.0;
+      for (int x = 0; x < kTcWarps; ++x) sum += red[x];
+      a.dalpha_part[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = sum;
     }
   }
   // dQ = R(-phi) dq / 8 (dims d in tile nd and d + 32 in tile nd + 4 share a
@@ -394,11 +373,13 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     }
   };
 
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kKvStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the query side's q~, records and partials are complete from here on
   if (tid == 0)
     for (int s = 0; s < kKvStages && s < NG; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
   for (int grp = 0; grp < NG; ++grp) {
@@ -466,12 +447,31 @@ __global__ void __launch_bounds__(kKvThreads, 2)
       *reinterpret_cast<uint4*>(static_cast<bf16*>(a.dv) + row) = *reinterpret_cast<const uint4*>(tv + n * 72 + 8 * ch);
     }
   }
+  if (INTERP && a.dalpha_out && blockIdx.x == 0 && blockIdx.y == 0) {
+    // dL/dalpha = the query side's per-CTA partials summed in a fixed order
+    // (strided per thread, then the warp tree, then the warps in order), and
+    // dL/dtheta = dL/dalpha (alpha - 0.5)(1.5 - alpha)
+    __shared__ double red[kKvThreads / 32];
+    const int nblk = ((T + kTcTQ - 1) / kTcTQ) * a.B * a.Hkv;
+    double sum = 0.0;
+    for (int x = tid; x < nblk; x += kKvThreads) sum += a.dalpha_part[x];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_down_sync(0xffffffffu, sum, off);
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int x = 0; x < kKvThreads / 32; ++x) t += red[x];
+      a.dalpha_out[0] = t;
+      a.dalpha_out[1] = t * (a.alpha - 0.5) * (1.5 - a.alpha);
+    }
+  }
 }
 
 size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
                                    size_t* off_coef) {
   const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * d->Hkv;
-  size_t o = align256(nparts * sizeof(double)) + 256;  // partials, then the ticket counter
+  size_t o = align256(nparts * sizeof(double));  // per-CTA dL/dalpha partials
   *off_kr = o;
   o += kr_bytes(d);
   *off_qt = o;
@@ -513,18 +513,18 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
           cudaSuccess)
     return SFA_ERR_CUDA;
   dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
-  unsigned* ticket = reinterpret_cast<unsigned*>(
-      reinterpret_cast<char*>(a.dalpha_part) + align256((size_t)gq.x * gq.y * sizeof(double)));
-  if (cudaMemsetAsync(ticket, 0, sizeof(unsigned), s) != cudaSuccess) return SFA_ERR_CUDA;
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
-    kq<<<gq, kTcThreads, kBwdQTcSmem, s>>>(a, mk, mv, tq, tdo, to, sqt, sdq,
-                                           static_cast<uint4*>(coef), NS, ticket, p);
+    if (launch_pdl(kq, gq, dim3(kTcThreads), kBwdQTcSmem, s, a, mk, mv, tq, tdo, to, sqt, sdq,
+                   static_cast<uint4*>(coef), NS, p) != cudaSuccess)
+      return SFA_ERR_CUDA;
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
-    kkv<<<gkv, kKvThreads, kBwdKvTcSmem, s>>>(a, mq, md, mqr, mdr, mcw, mcr, p);
+    if (launch_pdl(kkv, gkv, dim3(kKvThreads), kBwdKvTcSmem, s, a, mq, md, mqr, mdr, mcw, mcr, p) !=
+        cudaSuccess)
+      return SFA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
 }

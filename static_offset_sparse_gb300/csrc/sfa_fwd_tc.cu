@@ -37,6 +37,8 @@ constexpr int kPrepPlanes = 2;
 __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__ k,
                                                         const float2* __restrict__ rope,
                                                         bf16* __restrict__ kr, int64_t planes, int T) {
+  pdl_launch_dependents();
+  pdl_wait();  // K may be the previous kernel's output
   const int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (it >= (int64_t)T * 4) return;
   const int pos = (int)(it >> 2), pc = (int)(it & 3);
@@ -65,9 +67,11 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream) {
   const int64_t planes = rows / T;
   dim3 grid((unsigned)(((int64_t)T * 4 + 255) / 256), (unsigned)((planes + kPrepPlanes - 1) / kPrepPlanes < 65535 ? (planes + kPrepPlanes - 1) / kPrepPlanes : 65535));
-  rope_prep_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
-      static_cast<const bf16*>(k), static_cast<const float2*>(rope), static_cast<bf16*>(kr), planes, T);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+  return launch_pdl(rope_prep_kernel, grid, dim3(256), 0, (cudaStream_t)stream,
+                    static_cast<const bf16*>(k), static_cast<const float2*>(rope),
+                    static_cast<bf16*>(kr), planes, T) == cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
 }
 
 template <bool INTERP>
@@ -248,8 +252,9 @@ int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* st
     return SFA_ERR_CUDA;
   dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
   LaunchTimer tm(SFA_KERNEL_FWD, stream);
-  kern<<<grid, kTcThreads, kFwdTcSmem, s>>>(a, mk, mv, mq, mo, p);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+  return launch_pdl(kern, grid, dim3(kTcThreads), kFwdTcSmem, s, a, mk, mv, mq, mo, p) == cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
 }
 
 }  // namespace sfa

@@ -13,6 +13,7 @@
 #pragma once
 
 #include "sfa_device.cuh"
+#include "sfa_launch.cuh"
 #include "sfa_mma.cuh"
 #include "sfa_tma.cuh"
 
@@ -95,11 +96,13 @@ __device__ __forceinline__ void tc_start(const CUtensorMap* mk, const CUtensorMa
                                          const CUtensorMap* const* qmaps, int nq, uint32_t qtile,
                                          int qplane, const Plan& P, int bg, int i0, int nwc, int nr,
                                          int NG, uint32_t sbase, uint64_t* bars) {
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s <= kTcStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's outputs (K', Q, ...) are complete from here on
   if (threadIdx.x == 0) {
     const uint32_t qb = smem_u32(&bars[kTcStages]);
     mbar_expect_tx(qb, nq * kTcQTileB);

@@ -105,6 +105,19 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
   return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream drains:
+// pdl_launch_dependents lets the next kernel's CTAs launch once every CTA of
+// this grid has executed it (so all of this grid is resident first), and
+// pdl_wait blocks until the previous grid has completed and its memory
+// operations are visible (it returns at once when there is none).  Every
+// kernel launched this way calls pdl_wait before its first global memory
+// access, reads and writes alike.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Record a timeout in the device status word (first error wins).
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
