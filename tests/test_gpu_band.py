@@ -181,3 +181,38 @@ def test_band_christoffel_gqa_full_size_sampled(sfa):
     _check("dK", _f64(dk)[b, g], gw["dk"][b, g])
     _check("dV", _f64(dv)[b, g], gw["dv"][b, g])
     assert torch.isfinite(dk).all() and torch.isfinite(dv).all()
+
+
+@pytest.mark.parametrize("T,Hq,Hkv", [(16, 2, 2), (16, 8, 1), (65, 4, 4), (65, 8, 2), (130, 4, 2)])
+def test_band_tiny_and_ragged(sfa, T, Hq, Hkv):
+    """Whole sequence in one partial tile (T = 16), one row past a tile (T = 65),
+    full causal sets; results against the oracle."""
+    dist = list(range(T))
+    delta, runs = sfa.band_plan(dist, T, Hq // Hkv)
+    assert delta == 1 and runs == [(0, T)]
+    x = si.make_qkvdo(2, T, Hq, Hkv, 64, "bf16", seed=2000 + T + Hq)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    _check("O", _f64(O), Ow)
+    assert np.abs(_f64(L) - Lw).max() <= 2e-2
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
+
+
+def test_band_distances_past_T_are_ignored(sfa):
+    """Distances >= T reach no key: the set with them gives the same bits as
+    the set without them."""
+    import torch
+
+    ch = SETS["christoffel32_256"]
+    T = 192
+    assert sfa.band_plan(ch, T, 1) == (8, [(0, 1), (7, 24)])
+    x = si.make_qkvdo(1, T, 4, 4, 64, "bf16", seed=2100)
+    a = _run(sfa, x, [d for d in ch if d < T], 1e4)
+    b = _run(sfa, x, ch, 1e4)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for u, w in zip(a[2], b[2]):
+        assert torch.equal(u, w)
