@@ -135,8 +135,8 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
  * tiles per query tile of 64 / G positions, sum over runs of
  * ceil((64 / G + len - 1) / 64), is kept (smallest delta on ties), and the
  * plan is used when the distance count is at least 8 times that tile count.
- * Writes *delta (0: no band plan; the set runs the rung kernels for G = 4,
- * the SIMT kernels otherwise), *n_runs, and run_start / run_len (cap
+ * Writes *delta (0: no band plan; the set runs the rung kernels for G = 4, 8
+ * or 16, the SIMT kernels otherwise), *n_runs, and run_start / run_len (cap
  * entries; SFA_ERR_CAPACITY if more runs).  G must be 1, 2, 4 or 8 for a
  * plan; a set with a negative distance or without 0 has none. */
 int sfa_band_plan(const int32_t* dist, int32_t n_dist, int32_t T, int32_t G, int32_t* delta,
@@ -231,8 +231,8 @@ int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v,
  * with 0 <= i - s < T.  A negative s reads the future row i + |s| (signed
  * offsets for bidirectional attention, same page); sets with negative
  * distances run the fp32 SIMT kernels.  bf16 sets with a band plan
- * (sfa_band_plan) run the band kernels, other bf16 sets with G = 4 the rung
- * kernels.  Same outputs as sfa_forward / sfa_backward without the alpha
+ * (sfa_band_plan) run the band kernels, other bf16 sets with G = 4, 8 or 16 the
+ * rung kernels.  Same outputs as sfa_forward / sfa_backward without the alpha
  * gradient. */
 int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
                     float* lse, void* ws, size_t ws_bytes, void* stream);

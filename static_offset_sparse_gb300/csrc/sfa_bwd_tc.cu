@@ -1,4 +1,5 @@
-// Tensor-core backward (bf16 I/O, G = 4): gradients of L = sum(O * dO) for
+// Tensor-core backward (bf16 I/O, G = 4, 8 or 16 in groups of 4 query heads;
+// the key side sums the groups of its KV head): gradients of L = sum(O * dO) for
 // the key set of "Depth-Staggered Fibonacci Spacing for Sparse Attention"
 // (method section), the same quantities as the SIMT backward.
 //
@@ -52,7 +53,10 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  // blockIdx.y = (batch, group g of 4 query heads); with G = 4m query heads per
+  // KV head the group reads KV head g / m; its records form plane blockIdx.y
+  const int ng4 = a.Hq >> 2, b = blockIdx.y / ng4, g = blockIdx.y - b * ng4;
+  const int bg = b * a.Hkv + (g >> (a.lgG - 2));
   const int T = a.T;
   const int i0 = blockIdx.x * kTcTQ, i0w = i0 + 4 * warp;
   const int p = gid & 3, i = i0w + p;
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   float dacc = 0.0f;
   // records of query i: [slot][2 x uint4]; this lane's rows gid, gid + 8 are
   // heads hA, hA + 2 of position p, i.e. half gid >> 2 of each record
-  uint4* crow = coef + ((int64_t)bg * T + ic) * NS * 2 + (gid >> 2);
+  uint4* crow = coef + ((int64_t)blockIdx.y * T + ic) * NS * 2 + (gid >> 2);
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
   const int colrow2 = 4 * warp + ((((lane & 7) >> 1) + 2) & 3) + (lane & 1);
@@ -326,7 +330,8 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
   }
 }
 
-template <bool INTERP>
+// MULTI: G > 4, the key side loops over the G / 4 query-head groups of its KV head
+template <bool INTERP, bool MULTI>
 __global__ void __launch_bounds__(kKvThreads, 2)
     bwd_kv_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mqr,
@@ -343,7 +348,12 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   const int T = a.T;
   const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * kw;
   const int j = j0w + gid;  // key row of B column gid
-  const int hplane = b * a.Hq + g * 4;
+  // the m = G / 4 groups of 4 query heads that read this KV head, one after
+  // the other: group s has query heads 4 (g m + s) .. + 3 and record plane
+  // b (Hq / 4) + g m + s
+  const int msub = MULTI ? 1 << (a.lgG - 2) : 1;
+  auto hplane_of = [&](int sg) { return b * a.Hq + (g * msub + sg) * 4; };
+  auto rplane_of = [&](int sg) { return b * (a.Hq >> 2) + g * msub + sg; };
 
   float dk[2][4], dv[2][4];
 #pragma unroll
@@ -354,22 +364,25 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   const int nwc = wmax >= 0 ? wmax / kKvWC + 1 : 0;
   int nr = 0;
   while (nr < P.n && P.c[nr] <= T - j0) ++nr;
-  const int NG = nwc + nr;
+  const int NG = nwc + nr;       // groups per query-head group
+  const int NGt = MULTI ? NG * msub : NG;  // all groups: query-head group gt / NG, group gt % NG
   // group -> first staged query: window chunk s_lo = 9 grp, or rung grp - nwc
   auto qb_of = [&](int grp) { return grp < nwc ? j0 + kKvWC * grp : j0 + P.c[grp - nwc] - 1; };
-  auto issue = [&](int grp, uint32_t st, uint32_t bar) {
+  auto issue = [&](int gt, uint32_t st, uint32_t bar) {
+    const int sg = MULTI ? gt / NG : 0, grp = MULTI ? gt - sg * NG : gt;
+    const int hplane = hplane_of(sg), rp = rplane_of(sg);
     const bool win = grp < nwc;
     const int qb = qb_of(grp);
     if (win) {
       mbar_expect_tx(bar, 2 * kKvPlaneB + kKvCoefB);
       tma_load_3d(st, &mq, 0, qb, hplane, bar);
       tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, bg, bar);
+      tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, rp, bar);
     } else {
       mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * 32);
       tma_load_3d(st, &mqr, 0, qb, hplane, bar);
       tma_load_3d(st + kKvPlaneB, &mdr, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, bg, bar);
+      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, rp, bar);
     }
   };
 
@@ -381,14 +394,16 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   __syncthreads();
   pdl_wait();  // the query side's q~, records and partials are complete from here on
   if (tid == 0)
-    for (int s = 0; s < kKvStages && s < NG; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
-  for (int grp = 0; grp < NG; ++grp) {
-    const int st = grp % kKvStages;
-    const bool okw = mbar_wait_bounded(smem_u32(&bars[st]), (grp / kKvStages) & 1);
+    for (int s = 0; s < kKvStages && s < NGt; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
+  int grpm = 0;  // with MULTI: gt mod NG, kept by a counter (no division per group)
+  for (int gt = 0; gt < NGt; ++gt) {
+    const int grp = MULTI ? grpm : gt;
+    const int st = gt % kKvStages;
+    const bool okw = mbar_wait_bounded(smem_u32(&bars[st]), (gt / kKvStages) & 1);
     if (__syncthreads_or(!okw)) {
       if (tid == 0) {
         record_status(a.status, SFA_ERR_TIMEOUT);
-        for (int g2 = grp; g2 < NG && g2 < grp + kKvStages; ++g2)
+        for (int g2 = gt; g2 < NGt && g2 < gt + kKvStages; ++g2)
           mbar_wait_bounded(smem_u32(&bars[g2 % kKvStages]), (g2 / kKvStages) & 1);
       }
       return;
@@ -405,7 +420,8 @@ __global__ void __launch_bounds__(kKvThreads, 2)
                   kKvQR, qoff, j, T, dh, dk, dv);
     }
     __syncthreads();
-    if (tid == 0 && grp + kKvStages < NG) issue(grp + kKvStages, qst, smem_u32(&bars[st]));
+    if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
+    if (MULTI && ++grpm == NG) grpm = 0;
   }
 
   // dK = R(-phi) dk' at key positions; transpose through shared memory for
@@ -452,7 +468,7 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     // (strided per thread, then the warp tree, then the warps in order), and
     // dL/dtheta = dL/dalpha (alpha - 0.5)(1.5 - alpha)
     __shared__ double red[kKvThreads / 32];
-    const int nblk = ((T + kTcTQ - 1) / kTcTQ) * a.B * a.Hkv;
+    const int nblk = ((T + kTcTQ - 1) / kTcTQ) * a.B * (a.Hq >> 2);
     double sum = 0.0;
     for (int x = tid; x < nblk; x += kKvThreads) sum += a.dalpha_part[x];
 #pragma unroll
@@ -470,7 +486,7 @@ __global__ void __launch_bounds__(kKvThreads, 2)
 
 size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
                                    size_t* off_coef) {
-  const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * d->Hkv;
+  const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * (d->Hq / 4);
   size_t o = align256(nparts * sizeof(double));  // per-CTA dL/dalpha partials
   *off_kr = o;
   o += kr_bytes(d);
@@ -478,7 +494,7 @@ size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off
   o += align256((size_t)d->B * d->Hq * d->T * kD * 2);
   *off_coef = o;
   const size_t NS = (size_t)p.W + 1 + 2 * p.n;  // records per query: window slots, 2 per rung
-  o += align256((size_t)d->B * d->Hkv * d->T * NS * 32);
+  o += align256((size_t)d->B * (d->Hq / 4) * d->T * NS * 32);  // one plane per group of 4 heads
   return o;
 }
 
@@ -502,17 +518,19 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&mqr, qt, qplanes, a.T, kKvQR, 4) != SFA_OK ||
       make_rows_map(&mdr, a.dO, qplanes, a.T, kKvQR, 4) != SFA_OK ||
-      make_coef_map(&mcw, coef, kvplanes, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
-      make_coef_map(&mcr, coef, kvplanes, a.T, NS, 2, kKvQR) != SFA_OK)
+      make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
+      make_coef_map(&mcr, coef, qplanes / 4, a.T, NS, 2, kKvQR) != SFA_OK)
     return SFA_ERR_CUDA;
   auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
-  auto kkv = p.interp ? bwd_kv_tc_kernel<true> : bwd_kv_tc_kernel<false>;
+  const bool multi = a.lgG > 2;
+  auto kkv = p.interp ? (multi ? bwd_kv_tc_kernel<true, true> : bwd_kv_tc_kernel<true, false>)
+                      : (multi ? bwd_kv_tc_kernel<false, true> : bwd_kv_tc_kernel<false, false>);
   if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdQTcSmem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdKvTcSmem) !=
           cudaSuccess)
     return SFA_ERR_CUDA;
-  dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
+  dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * (a.Hq / 4)));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
     if (launch_pdl(kq, gq, dim3(kTcThreads), kBwdQTcSmem, s, a, mk, mv, tq, tdo, to, sqt, sdq,

@@ -1,4 +1,5 @@
-// Tensor-core forward (bf16 I/O, G = 4 query heads per KV head).
+// Tensor-core forward (bf16 I/O, G = 4, 8 or 16 query heads per KV head, taken
+// in groups of 4).
 //
 // Same result as the SIMT forward ("Depth-Staggered Fibonacci Spacing for
 // Sparse Attention", method section: window 0..W plus rungs read by two-row
@@ -84,7 +85,10 @@ __global__ void __launch_bounds__(kTcThreads, 5)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
+  // blockIdx.y = (batch, group g of 4 query heads); with G = 4m query heads per
+  // KV head the group reads KV head g / m
+  const int ng4 = a.Hq >> 2, b = blockIdx.y / ng4, g = blockIdx.y - b * ng4;
+  const int bg = b * a.Hkv + (g >> (a.lgG - 2));
   const int T = a.T;
   const int i0 = blockIdx.x * kTcTQ, i0w = i0 + 4 * warp;
   const int p = gid & 3, i = i0w + p;  // position of rows gid and gid + 8
@@ -250,7 +254,7 @@ int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* st
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFwdTcSmem) !=
       cudaSuccess)
     return SFA_ERR_CUDA;
-  dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * a.Hkv));
+  dim3 grid((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * (a.Hq / 4)));
   LaunchTimer tm(SFA_KERNEL_FWD, stream);
   return launch_pdl(kern, grid, dim3(kTcThreads), kFwdTcSmem, s, a, mk, mv, mq, mo, p) == cudaSuccess
              ? SFA_OK

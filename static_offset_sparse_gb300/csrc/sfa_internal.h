@@ -65,9 +65,13 @@ struct AttnArgs {
 };
 
 // Kernel launchers (stream is a cudaStream_t).
-// The tensor-core kernels serve bf16 I/O with G = 4; everything else runs the
-// fp32 SIMT kernels.
-inline bool use_tc(const sfa_desc* d) { return d->dtype == SFA_BF16 && d->Hq == 4 * d->Hkv; }
+// The rung tensor-core kernels serve bf16 I/O with G = 4m (m = 1, 2, 4: groups
+// of 4 query heads, m of them per KV head); everything else runs the fp32
+// SIMT kernels (or the band kernels, for integer sets with a band plan).
+inline bool use_tc(const sfa_desc* d) {
+  const int G = d->Hq / d->Hkv;
+  return d->dtype == SFA_BF16 && (G == 4 || G == 8 || G == 16);
+}
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Workspace for the rotated keys the tensor-core kernels read (none when the
 // caller supplies them in d->k_rot, or without RoPE).

@@ -1,4 +1,5 @@
-// Shared pieces of the tensor-core kernels (bf16 I/O, G = 4).
+// Shared pieces of the rung tensor-core kernels (bf16 I/O, G = 4, 8 or 16: the
+// query heads of a KV head in groups of 4).
 //
 // A warp owns 4 consecutive query positions x the 4 query heads of one KV
 // group = 16 mma rows (row r = 4 h + p).  Keys are raw RoPE-rotated K' rows

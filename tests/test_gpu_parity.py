@@ -70,7 +70,7 @@ def _check(name, got, want, tol, bf16=None):
 
 SHAPES = [  # B, T, Hq, Hkv
     (1, 1, 8, 2), (1, 2, 4, 1), (2, 3, 1, 1), (1, 17, 8, 2), (2, 65, 4, 1),
-    (1, 130, 8, 2), (1, 300, 2, 2), (1, 70, 16, 1), (1, 40, 2, 1),
+    (1, 130, 8, 2), (1, 300, 2, 2), (1, 70, 16, 1), (1, 40, 2, 1), (1, 90, 8, 1),
 ]
 
 
@@ -196,3 +196,34 @@ def test_k_rot_reuse_is_bit_identical(sfa):
     d2 = sfa.make_desc(d["q"], d["k"], W=8, alpha=0.9, base=base, k_rot=kr)
     assert sfa.workspace_size(d2, True, False) == 0 < sfa.workspace_size(d1, True, False)
     assert sfa.workspace_size(d2, True, True) < sfa.workspace_size(d1, True, True)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv", [(2, 200, 16, 2), (1, 256, 8, 1), (1, 333, 32, 8)])
+def test_rung_kernels_groups_of_four_heads(sfa, B, T, Hq, Hkv):
+    """G = 8 and 16: the rung kernels run one CTA row per group of four query
+    heads (reading KV head group / (G / 4)) and the key side sums the groups;
+    interpolated (with dL/dalpha) and integer paths against the oracle."""
+    base = o.fib_offsets(15)
+    x = si.make_qkvdo(B, T, Hq, Hkv, 64, "bf16", seed=300 + Hq + T)
+    alpha = 0.83
+    O, L, g = _run_interp(sfa, x, 8, alpha, base, 1e4)
+    slots = o.interp_slots(base, alpha, 8)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4, alpha=alpha)
+    _check("O", O, Ow, 2e-2)
+    _check("LSE", L, Lw, 2e-2, bf16=False)
+    for name, got, key in (("dQ", g[0], "dq"), ("dK", g[1], "dk"), ("dV", g[2], "dv")):
+        _check(name, got, gw[key], 2e-2)
+    da, dt = _np(g[3])
+    check_dalpha_dtheta(da, dt, gw, alpha, True)
+    dist = sorted(set(range(9)) | set(o.fib_offsets(15)))
+    q, k, v, do = (_dev(x[n]) for n in ("q", "k", "v", "do"))
+    Oi, Li = sfa.forward_int(q, k, v, dist=dist)
+    gi = sfa.backward_int(q, k, v, Oi, Li, do, dist=dist)
+    si_ = o.dist_slots(dist)
+    Ow, _ = o.forward(x["q"], x["k"], x["v"], si_, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], si_, 1e4)
+    _check("O int", Oi, Ow, 2e-2)
+    for name, got, key in (("dQ int", gi[0], "dq"), ("dK int", gi[1], "dk"), ("dV int", gi[2], "dv")):
+        _check(name, got, gw[key], 2e-2)
+    assert sfa.get_device_status() == 0
