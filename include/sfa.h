@@ -77,7 +77,8 @@ typedef struct {
   const float* rope;
   /* Optional device [B, Hkv, T, 64] bf16: the rotated keys sfa_rope_keys wrote
    * for this k and this rope table, or NULL.  Calls that run the tensor-core
-   * kernels (bf16 I/O, G = 4, no negative distance) then read it instead of
+   * kernels (bf16 I/O: the rung kernels for G = 4, 8, 16 and the band kernels,
+   * no negative distance) then read it instead of
    * rotating K into their workspace (which shrinks accordingly), so one
    * rotation serves a layer's forward and backward.  Ignored otherwise. */
   const void* k_rot;
