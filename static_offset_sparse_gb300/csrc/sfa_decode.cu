@@ -15,6 +15,7 @@
 #include <math.h>
 
 #include "sfa_device.cuh"
+#include "sfa_launch.cuh"
 #include "sfa_tma.cuh"
 
 namespace sfa {
@@ -24,6 +25,8 @@ constexpr int kDecHeadsPerCta = 4;
 template <typename TIO>
 __global__ void __launch_bounds__(32 * kDecHeadsPerCta)
     decode_int_kernel(const AttnArgs a, const __grid_constant__ Plan P) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's outputs (this layer's q, the cache) are complete
   const int lane = threadIdx.x & 31;
   const int64_t gh = (int64_t)blockIdx.x * kDecHeadsPerCta + (threadIdx.x >> 5);  // b * Hq + h
   if (gh >= (int64_t)a.B * a.Hq) return;
@@ -131,10 +134,15 @@ int launch_decode_int(const AttnArgs& a, const Plan& p, int dtype, void* stream)
   if (grid == 0) return SFA_OK;
   LaunchTimer tm(SFA_KERNEL_DECODE, stream);
   if (dtype == SFA_BF16)
-    decode_int_kernel<bf16><<<grid, 32 * kDecHeadsPerCta, 0, (cudaStream_t)stream>>>(a, p);
+    return launch_pdl(decode_int_kernel<bf16>, grid, dim3(32 * kDecHeadsPerCta), 0,
+                      (cudaStream_t)stream, a, p) == cudaSuccess
+               ? SFA_OK
+               : SFA_ERR_CUDA;
   else
-    decode_int_kernel<float><<<grid, 32 * kDecHeadsPerCta, 0, (cudaStream_t)stream>>>(a, p);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+    return launch_pdl(decode_int_kernel<float>, grid, dim3(32 * kDecHeadsPerCta), 0,
+                      (cudaStream_t)stream, a, p) == cudaSuccess
+               ? SFA_OK
+               : SFA_ERR_CUDA;
 }
 
 }  // namespace sfa
