@@ -82,12 +82,14 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   float delta[2], lse2[2];
   lse2[0] = a.lse[rowA] * kLog2e;
   lse2[1] = a.lse[rowB] * kLog2e;
+  float4 rp[4];
+  if (rope) load_frag_rope(rope, ic, rp);  // while the query tiles are in flight
   if (!tc_wait_qtiles(bars, a.status)) return;
-  tile_frags(qtile, warp, rope, ic, 0.125f, true, qa);
-  tile_frags(dotile, warp, nullptr, ic, 1.0f, false, da);
+  tile_frags(qtile, warp, rope ? rp : nullptr, 0.125f, true, qa);
+  tile_frags(dotile, warp, nullptr, 1.0f, false, da);
   {  // delta = dO . O per row, from the dO and O fragments of this lane (16 dims), then the quad
     uint32_t oa[4][4];
-    tile_frags(otile, warp, nullptr, ic, 1.0f, false, oa);
+    tile_frags(otile, warp, nullptr, 1.0f, false, oa);
     float acc[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)

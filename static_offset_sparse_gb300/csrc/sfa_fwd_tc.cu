@@ -105,12 +105,14 @@ __global__ void __launch_bounds__(kTcThreads, 5)
   const int qplane = b * a.Hq + g * 4;
   const CUtensorMap* qmaps[1] = {&mq};
   tc_start(&mk, &mv, qmaps, 1, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+  float4 rp[4];
+  if (rope) load_frag_rope(rope, min(i, T - 1), rp);  // while the Q tile is in flight
   if (!tc_wait_qtiles(bars, a.status)) return;
   uint32_t qa[4][4];
   // q~ = q'/8 rounded exactly as the query-side backward rounds it, log2(e)
   // applied to the fp32 logits: the backward's P = exp(S - LSE) recomputes
   // this kernel's logits bit for bit and stays normalised
-  tile_frags(qtile, warp, rope, min(i, T - 1), 0.125f, true, qa);
+  tile_frags(qtile, warp, rope ? rp : nullptr, 0.125f, true, qa);
   float o[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;

@@ -157,11 +157,24 @@ __device__ __forceinline__ bool tc_run(const CUtensorMap* mk, const CUtensorMap*
   return true;
 }
 
+// The RoPE (cos, sin) pairs a lane's fragments need at position i (pairs
+// 16 kk + 2 tig + {0, 1, 8, 9}, kk = 0, 1), as four float4: loaded while the
+// query tile is still in flight.
+__device__ __forceinline__ void load_frag_rope(const float2* rope, int i, float4* rp) {
+  const int tig = threadIdx.x & 3;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    rp[2 * kk] = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig));
+    rp[2 * kk + 1] = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig + 8));
+  }
+}
+
 // A fragments of a warp's 16 rows (row r = 4 h + p: head h, position 4w + p)
-// for the 4 k-steps, from a query tile; with RoPE at position i (rope !=
-// nullptr) and a scale they are unpacked, rotated, scaled and repacked.
-__device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float2* rope, int i,
-                                           float scale, bool transform, uint32_t (*qa)[4]) {
+// for the 4 k-steps, from a query tile; with transform they are unpacked,
+// rotated by the RoPE pairs rp of load_frag_rope (none if rp is nullptr),
+// scaled and repacked.
+__device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float4* rp, float scale,
+                                           bool transform, uint32_t (*qa)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3;
   const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
   const int srow = (r >> 2) * kTcQRows + 4 * warp + (r & 3);
@@ -177,11 +190,10 @@ __device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float2
     x[0][kk][0] = a0.x; x[0][kk][1] = a0.y; x[0][kk][2] = a2.x; x[0][kk][3] = a2.y;
     x[1][kk][0] = a1.x; x[1][kk][1] = a1.y; x[1][kk][2] = a3.x; x[1][kk][3] = a3.y;
   }
-  if (rope) {
+  if (rp) {
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)i * 32 + 16 * kk + 2 * tig + 8));
+      const float4 a = rp[2 * kk], b = rp[2 * kk + 1];
       const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
