@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
     if (rope) {
 #pragma unroll
       for (int nd = 0; nd < 4; ++nd) {
-        const float4 cs = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)ic * 32 + 8 * nd + 2 * tig));
+        const float4 cs = rp[nd];  // the pairs 8 nd + 2 tig (+1) loaded for the fragments
         const float c2[2] = {cs.x, cs.z}, s2[2] = {cs.y, cs.w};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -397,6 +397,17 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   pdl_wait();  // the query side's q~, records and partials are complete from here on
   if (tid == 0)
     for (int s = 0; s < kKvStages && s < NGt; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
+  // the RoPE pairs of the dK epilogue (keys 2 tig (+1) of the warp's group,
+  // pairs 16 dh + gid (+8)), loaded now so their latency hides under the loop
+  const float2* rope = static_cast<const float2*>(a.rope);
+  float2 kcs[2][2];
+  if (rope)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int jj = min(j0w + 2 * tig + e, T - 1);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) kcs[e][hh] = __ldg(rope + (int64_t)jj * 32 + 16 * dh + gid + 8 * hh);
+    }
   int grpm = 0;  // with MULTI: gt mod NG, kept by a counter (no division per group)
   for (int gt = 0; gt < NGt; ++gt) {
     const int grp = MULTI ? grpm : gt;
@@ -429,14 +440,12 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   // dK = R(-phi) dk' at key positions; transpose through shared memory for
   // row-contiguous stores.  Lane holds dims 16 mt + gid (+8) for mt = dh,
   // dh + 2, keys 2 tig (+1) of its key group.
-  const float2* rope = static_cast<const float2*>(a.rope);
   if (rope) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int jj = min(j0w + 2 * tig + e, T - 1);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const float2 cs = __ldg(rope + (int64_t)jj * 32 + 16 * dh + gid + 8 * hh);
+        const float2 cs = kcs[e][hh];
         const float lo = dk[0][2 * hh + e], hi = dk[1][2 * hh + e];
         dk[0][2 * hh + e] = lo * cs.x + hi * cs.y;
         dk[1][2 * hh + e] = hi * cs.x - lo * cs.y;
