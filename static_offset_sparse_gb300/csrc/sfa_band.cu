@@ -104,12 +104,26 @@ __device__ __forceinline__ bool kwalk_next(const BandPlan& P, int rho, int v0, i
   return kwalk_seek(P, rho, v0, vl, Uc, w);
 }
 
+// The RoPE (cos, sin) pairs of rows gid (x = 0) and gid + 8 at positions
+// pos[x] that band_frags needs (pairs 16 kk + 2 tig + {0, 1, 8, 9}), loaded
+// while the tile is still in flight.
+__device__ __forceinline__ void band_rope_pairs(const float2* rope, const int* pos, float4 (*rp)[4]) {
+  const int tig = threadIdx.x & 3;
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const float2* tab = rope + (int64_t)pos[x] * 32 + 16 * kk + 2 * tig;
+      rp[x][2 * kk] = __ldg(reinterpret_cast<const float4*>(tab));
+      rp[x][2 * kk + 1] = __ldg(reinterpret_cast<const float4*>(tab + 8));
+    }
+}
+
 // A fragments of rows row0 .. row0 + 15 of a 64-row tile for the 4 k-steps.
-// With transform they are unpacked, rotated by RoPE (rows gid and gid + 8 at
-// positions pos[0] and pos[1]; none if rope is nullptr), scaled and repacked.
-__device__ __forceinline__ void band_frags(uint32_t tile, int row0, const float2* rope,
-                                           const int* pos, float scale, bool transform,
-                                           uint32_t (*qa)[4]) {
+// With transform they are unpacked, rotated by the RoPE pairs rp of
+// band_rope_pairs (none if rp is nullptr), scaled and repacked.
+__device__ __forceinline__ void band_frags(uint32_t tile, int row0, const float4 (*rp)[4],
+                                           float scale, bool transform, uint32_t (*qa)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
@@ -124,14 +138,12 @@ __device__ __forceinline__ void band_frags(uint32_t tile, int row0, const float2
     x[0][kk][0] = a0.x; x[0][kk][1] = a0.y; x[0][kk][2] = a2.x; x[0][kk][3] = a2.y;
     x[1][kk][0] = a1.x; x[1][kk][1] = a1.y; x[1][kk][2] = a3.x; x[1][kk][3] = a3.y;
   }
-  if (rope) {
+  if (rp) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const float2* tab = rope + (int64_t)pos[rr] * 32;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(tab + 16 * kk + 2 * tig));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(tab + 16 * kk + 2 * tig + 8));
+        const float4 a = rp[rr][2 * kk], b = rp[rr][2 * kk + 1];
         const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -441,6 +453,9 @@ __global__ void __launch_bounds__(kBThreads, 4)
     qwalk_seek(P, q.r, q.u0, q.ul, iw);
     for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
   }
+  const float2* rope = static_cast<const float2*>(a.rope);
+  float4 rp[2][4];
+  if (rope) band_rope_pairs(rope, q.pos, rp);  // while the Q tile is in flight
   if (!band_wait(&bars[kBStages], 0, a.status)) {
     band_drain(bars, NT);
     return;
@@ -449,7 +464,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
   // the fp32 logits: the backward's P = exp(S - LSE) then recomputes this
   // kernel's logits bit for bit and stays normalised
   uint32_t qa[4][4];
-  band_frags(qtile, 16 * warp, static_cast<const float2*>(a.rope), q.pos, 0.125f, true, qa);
+  band_frags(qtile, 16 * warp, rope ? rp : nullptr, 0.125f, true, qa);
   float o[8][4];
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
@@ -551,17 +566,19 @@ __global__ void __launch_bounds__(kBThreads, 3)
   float lse2[2];
 #pragma unroll
   for (int x = 0; x < 2; ++x) lse2[x] = a.lse[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] * kLog2e;
+  float4 rp[2][4];
+  if (rope) band_rope_pairs(rope, q.pos, rp);  // while the query tiles are in flight
   if (!band_wait(&bars[kBStages], 0, a.status)) {
     band_drain(bars, NT);
     return;
   }
   uint32_t qa[4][4], da[4][4];
-  band_frags(qtile, 16 * warp, rope, q.pos, 0.125f, true, qa);
-  band_frags(dotile, 16 * warp, nullptr, q.pos, 1.0f, false, da);
+  band_frags(qtile, 16 * warp, rope ? rp : nullptr, 0.125f, true, qa);
+  band_frags(dotile, 16 * warp, nullptr, 1.0f, false, da);
   float dlt[2];
   {  // delta_i = dO . O per row from this lane's 16 dims of each, then the quad
     uint32_t oa[4][4];
-    band_frags(otile, 16 * warp, nullptr, q.pos, 1.0f, false, oa);
+    band_frags(otile, 16 * warp, nullptr, 1.0f, false, oa);
     float acc[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
@@ -783,8 +800,8 @@ __global__ void __launch_bounds__(kBThreads, 3)
         // the warp's K' and V rows as A fragments, from the CTA's tiles (kept
         // in shared memory rather than in 32 registers for the whole CTA)
         uint32_t ka[4][4], va[4][4];
-        band_frags(ktile, 16 * warp, nullptr, nullptr, 1.0f, false, ka);
-        band_frags(vtile, 16 * warp, nullptr, nullptr, 1.0f, false, va);
+        band_frags(ktile, 16 * warp, nullptr, 1.0f, false, ka);
+        band_frags(vtile, 16 * warp, nullptr, 1.0f, false, va);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
           st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.0f;
