@@ -216,3 +216,44 @@ def test_band_distances_past_T_are_ignored(sfa):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
     for u, w in zip(a[2], b[2]):
         assert torch.equal(u, w)
+
+
+def _random_band_cases(n, seed):
+    """Seeded run-structured sets that get a band plan with step >= 2 and at
+    least two runs: steps 2, 3, 4, 5, 8, runs starting past the step (several
+    runs in one key class), distances past T, ragged T / delta."""
+    import random
+
+    import static_offset_sparse_gb300 as s
+
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        delta = rng.choice([2, 3, 4, 5, 8])
+        G = rng.choice([1, 2, 4, 8])
+        T = delta * rng.randint(20, 90)
+        dist = {0}
+        for _ in range(rng.randint(1, 3)):
+            a = rng.randrange(0, 3 * delta + 5)
+            dist |= {a + delta * t for t in range(rng.randint(20, 120))}
+        dist = sorted(dist)
+        d, runs = s.band_plan(dist, T, G)
+        if d >= 2 and len(runs) >= 2:
+            out.append((T, G, dist))
+    return out
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_band_random_run_sets(sfa, case):
+    T, G, dist = _random_band_cases(12, 11)[case]
+    Hkv = 2 if G <= 4 else 1
+    x = si.make_qkvdo(1, T, G * Hkv, Hkv, 64, "bf16", seed=2200 + case)
+    O, L, (dq, dk, dv) = _run(sfa, x, dist, 1e4)
+    slots = o.dist_slots(dist)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4)
+    _check("O", _f64(O), Ow)
+    assert np.abs(_f64(L) - Lw).max() <= 2e-2
+    _check("dQ", _f64(dq), gw["dq"])
+    _check("dK", _f64(dk), gw["dk"])
+    _check("dV", _f64(dv), gw["dv"])
