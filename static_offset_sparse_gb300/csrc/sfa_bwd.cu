@@ -402,12 +402,6 @@ __global__ void dalpha_reduce_kernel(const double* part, int64_t n, double alpha
   }
 }
 
-int launch_dalpha_reduce(const double* part, int64_t n, double alpha, double* out, void* stream) {
-  LaunchTimer tm(SFA_KERNEL_DALPHA, stream);
-  dalpha_reduce_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(part, n, alpha, out);
-  return cudaGetLastError() == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
-}
-
 static int kv_grid_x(int T, int lgG) { return (T + (128 >> lgG) - 1) / (128 >> lgG); }
 
 size_t backward_workspace_bytes(const sfa_desc* d, const Plan& p) {
