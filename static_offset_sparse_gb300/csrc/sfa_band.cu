@@ -480,6 +480,38 @@ __global__ void __launch_bounds__(kBThreads, 4)
     int lo[2], hi[2];
     q.cols(P, cw, lo, hi);
     const uint32_t vst = kst + kBTileB;
+    if (P.len[cw.m] == 1) {
+      // a one-distance run (distance 0 in the Christoffel sets): each row reads
+      // one key, and a warp's 16 rows read at most 16 consecutive columns, so
+      // the warp computes the three n-tiles nb .. nb + 2 around them (a
+      // CTA-uniform path: the n-tile base only moves shared-memory addresses)
+      int umin, umax;
+      q.warp_span(umin, umax);
+      const int nb = min(max(0, umin + cw.e - cw.vs) >> 3, 5);
+      float acc[3][4];
+#pragma unroll
+      for (int nt = 0; nt < 3; ++nt) {
+        acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        qk_tile(qa, kst, 8 * (nb + nt) + (lane & 7), acc[nt]);
+      }
+      float s[2][6];
+#pragma unroll
+      for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int x = e >> 1, col = 8 * (nb + nt) + 2 * tig + (e & 1);
+          s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
+        }
+      band_softmax<6>(s, m, l, o);
+      const uint32_t pa0[4] = {pack_bf16(s[0][0], s[0][1]), pack_bf16(s[1][0], s[1][1]),
+                               pack_bf16(s[0][2], s[0][3]), pack_bf16(s[1][2], s[1][3])};
+      const uint32_t pa1[4] = {pack_bf16(s[0][4], s[0][5]), pack_bf16(s[1][4], s[1][5]), 0u, 0u};
+      const int rl = 8 * nb + (lane & 7);
+      pv_tile(pa0, vst, rl, rl + 8, o);
+      pv_tile(pa1, vst, rl + 16, rl + 16, o);  // keys 8 nb + 24 .. are not read (zero P)
+      qwalk_next(P, q.r, q.u0, q.ul, cw);
+      return;
+    }
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       float acc[4][4];
