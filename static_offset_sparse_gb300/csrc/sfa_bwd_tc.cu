@@ -53,9 +53,13 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  // blockIdx.y = (batch, group g of 4 query heads); with G = 4m query heads per
-  // KV head the group reads KV head g / m; its records form plane blockIdx.y
-  const int ng4 = a.Hq >> 2, b = blockIdx.y / ng4, g = blockIdx.y - b * ng4;
+  // qy = (batch, group g of 4 query heads); with G = 4m query heads per KV head
+  // the group reads KV head g / m; its records form plane qy.  Planes run in
+  // reverse launch order: the forward ended on the last planes, whose O and
+  // LSE are the likeliest to be still in L2, and the key side, which starts
+  // on the first planes, finds their records there
+  const int qy = gridDim.y - 1 - blockIdx.y;
+  const int ng4 = a.Hq >> 2, b = qy / ng4, g = qy - b * ng4;
   const int bg = b * a.Hkv + (g >> (a.lgG - 2));
   const int T = a.T;
   const int i0 = blockIdx.x * kTcTQ, i0w = i0 + 4 * warp;
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   float dacc = 0.0f;
   // records of query i: [slot][2 x uint4]; this lane's rows gid, gid + 8 are
   // heads hA, hA + 2 of position p, i.e. half gid >> 2 of each record
-  uint4* crow = coef + ((int64_t)blockIdx.y * T + ic) * NS * 2 + (gid >> 2);
+  uint4* crow = coef + ((int64_t)qy * T + ic) * NS * 2 + (gid >> 2);
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
   const int colrow2 = 4 * warp + ((((lane & 7) >> 1) + 2) & 3) + (lane & 1);
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
     if (threadIdx.x == 0) {
       double sum = 0.0;
       for (int x = 0; x < kTcWarps; ++x) sum += red[x];
-      a.dalpha_part[(int64_t)blockIdx.y * gridDim.x + blockIdx.x] = sum;
+      a.dalpha_part[(int64_t)qy * gridDim.x + blockIdx.x] = sum;
     }
   }
   // dQ = R(-phi) dq / 8 (dims d in tile nd and d + 32 in tile nd + 4 share a
