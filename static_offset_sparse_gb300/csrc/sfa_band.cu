@@ -374,7 +374,10 @@ struct QTile {
   static constexpr int BU = kBR / G;
   int delta, Uc, r, u0, ul, qplane, bg;
   int hh[2], uu[2], pos[2];  // rows gid, gid + 8 of the lane's warp: head, position, i
-  __device__ __forceinline__ QTile(const AttnArgs& a, const BandPlan& P) {
+  // reverse: planes in reverse launch order (the query-side backward starts on
+  // the planes the forward ended on, whose O and LSE are the likeliest to be
+  // in L2, and ends on those the key side starts on)
+  __device__ __forceinline__ QTile(const AttnArgs& a, const BandPlan& P, bool reverse) {
     const int warp = threadIdx.x >> 5, gid = (threadIdx.x & 31) >> 2;
     delta = P.delta;
     Uc = a.T / delta;
@@ -382,7 +385,7 @@ struct QTile {
     r = blockIdx.x / nqt;
     u0 = (blockIdx.x - r * nqt) * BU;
     ul = min(u0 + BU - 1, Uc - 1);
-    bg = blockIdx.y;
+    bg = reverse ? gridDim.y - 1 - blockIdx.y : blockIdx.y;
     const int b = bg / a.Hkv, g = bg - b * a.Hkv;
     qplane = b * a.Hq + g * G;
 #pragma unroll
@@ -434,7 +437,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
   __shared__ uint64_t bars[kBStages + 1];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tig = lane & 3;
-  const QTile<G> q(a, P);
+  const QTile<G> q(a, P, false);
   const uint32_t qtile = sbase, stages = sbase + kBTileB;
   const int NT = q.count(P);
   band_init_bars(bars);
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
   __shared__ uint64_t bars[kBStages + 1];
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gid = lane >> 2, tig = lane & 3;
-  const QTile<G> q(a, P);
+  const QTile<G> q(a, P, true);
   const uint32_t qtile = sbase, dotile = sbase + kBTileB, otile = sbase + 2 * kBTileB;
   const uint32_t stages = sbase + 3 * kBTileB;
   const float2* rope = static_cast<const float2*>(a.rope);
