@@ -175,7 +175,7 @@ __device__ __forceinline__ void load_frag_rope(const float2* rope, int i, float4
 // scaled and repacked.
 __device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float4* rp, float scale,
                                            bool transform, uint32_t (*qa)[4]) {
-  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int lane = threadIdx.x & 31;
   const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
   const int srow = (r >> 2) * kTcQRows + 4 * warp + (r & 3);
 #pragma unroll
