@@ -735,6 +735,8 @@ def configs_arm(args, dev):
         ("4: bf16 integer forward, T=16384, alpha=1.5", 4, 16384, 8, 2, "bf16", "int", (int_set(1.5, 8),), False),
         ("5: bf16 Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int", (chris(),), True),
         ("5 with 8/2 heads (G = 4)", 16, 2048, 8, 2, "bf16", "int", (chris(),), True),
+        ("2 with 16/2 heads (G = 8)", 16, 1024, 16, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
+        ("5 with 8/1 heads (G = 8)", 16, 2048, 8, 1, "bf16", "int", (chris(),), True),
     ]
     if args.only:
         cases = [c for c in cases if c[0].startswith(args.only)]
@@ -781,7 +783,7 @@ def configs_arm(args, dev):
         band = kind == "int" and dt == "bf16" and sfa.band_plan(par[0], Tc, Hq // Hkv)[0] > 0
         if band:
             path = "band (tensor cores)"
-        elif dt == "bf16" and Hq == 4 * Hkv and not (kind == "int" and min(par[0]) < 0):
+        elif dt == "bf16" and Hq // Hkv in (4, 8, 16) and not (kind == "int" and min(par[0]) < 0):
             path = "rung (tensor cores)"
         else:
             path = "SIMT"
