@@ -20,7 +20,7 @@
 
 namespace sfa {
 
-constexpr int kDecHeadsPerCta = 4;
+constexpr int kDecHeadsPerCta = 1;
 
 template <typename TIO>
 __global__ void __launch_bounds__(32 * kDecHeadsPerCta)
