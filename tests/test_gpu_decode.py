@@ -79,6 +79,33 @@ def test_decode_matches_oracle(sfa, dtype, case):
     assert np.abs(f64(L) - Lw).max() <= lse_tol
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_both_kernels(sfa, dtype):
+    """Steps of more than 1024 heads run the register kernel, smaller steps the
+    staged one: B = 130 sequences x 8 heads against the oracle, and its first
+    three sequences bit for bit against a three-sequence call."""
+    import torch
+
+    B, T, Hq, Hkv = 130, 64, 8, 2
+    dist = o.int_distances(FIB, 1.0, 8)
+    x = si.make_qkvdo(B, T, Hq, Hkv, 64, dtype, seed=91, with_do=False)
+    rng = np.random.default_rng(5)
+    pos = [int(p) for p in rng.integers(0, T, size=B)]
+    q_dec = x["q"][:, :, -1].contiguous().cuda()
+    k, v = x["k"].cuda(), x["v"].cuda()
+    posd = torch.tensor(pos, dtype=torch.int32, device="cuda")
+    O, L = sfa.decode_int(q_dec, k, v, posd, dist=dist)
+    O3, L3 = sfa.decode_int(q_dec[:3].contiguous(), k[:3].contiguous(), v[:3].contiguous(),
+                            posd[:3].contiguous(), dist=dist)
+    torch.cuda.synchronize()
+    assert sfa.get_device_status() == 0
+    assert torch.equal(O[:3], O3) and torch.equal(L[:3], L3)
+    f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    Ow, Lw = _expected(f64(q_dec), f64(x["k"]), f64(x["v"]), pos, dist, 1e4)
+    _check("O", f64(O), Ow, dtype == "bf16")
+    assert np.abs(f64(L) - Lw).max() <= (1e-5 if dtype == "f32" else 2e-2)
+
+
 def test_decode_equals_forward_int_row(sfa):
     """Decode at position t reproduces row t of the integer forward (same
     caches, q placed at t)."""
