@@ -431,37 +431,102 @@ def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
     return time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name from /proc/cpuinfo (x86 'model name', Arm
+    implementer/part codes), else the platform's processor string."""
+    import platform
+
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        info = []
+    for line in info:
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    imp = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")]
+    part = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")]
+    if imp and part:
+        return f"{platform.machine()} (CPU implementer {imp[0]}, part {part[0]})"
+    return platform.processor() or platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_unit(job):
+    """Pool worker: one oracle (layer, sequence) unit; returns its seconds."""
+    schedule, W, layer = job
+    return oracle_step_sample(schedule, W, 1, layer)
+
+
 def cpu_baseline(schedule: str, W: int, budget_s: float = 10.0):
-    """The oracle as it stands on this host: one sequence of one layer at a
-    time, cycling through the 16 layers' alphas, until ~budget_s of CPU work;
-    throughput scaled to the 16-layer step (tokens / (16 x seconds per
-    layer-sequence))."""
+    """The oracle as it stands on this host, on a bounded sample of the
+    workload, scaled to the 16-layer step (tokens / (16 x seconds per
+    layer-sequence)).
+
+    Single thread: one sequence of one layer at a time, cycling through the 16
+    layers' alphas, until ~budget_s of CPU work.  All cores: one process per
+    host core (spawned: this process may hold a CUDA context), each running
+    whole (layer, sequence) units, each process's numpy on one thread; after
+    one warm-up unit per process, a batch of 4 units per process is timed by
+    the wall clock."""
     spent, n = 0.0, 0
     while spent < budget_s and n < 16 * 32:
         spent += oracle_step_sample(schedule, W, 1, n % SCHED_L)
         n += 1
     tok_s = n * T / (spent * SCHED_L)
-    return {"value": round(tok_s, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, {n} (layer, sequence) units of {T} tokens cycling over the "
-                      f"16 layers' alphas, W={W}, fwd+bwd incl. dtheta, single thread; {spent:.1f} s; "
-                      "scaled to the 16-layer step"}
+    out = {"value": round(tok_s, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "cpu_model": cpu_model(),
+           "sample": f"fp64 numpy oracle, {n} (layer, sequence) units of {T} tokens cycling over the "
+                     f"16 layers' alphas, W={W}, fwd+bwd incl. dtheta, single thread; {spent:.1f} s; "
+                     "scaled to the 16-layer step"}
+    cores = host_cores()
+    if cores > 1:
+        import multiprocessing as mp
+
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(cores) as pool:
+            pool.map(_oracle_unit, [(schedule, W, l % SCHED_L) for l in range(cores)], chunksize=1)
+            units = 4 * cores
+            t0 = time.perf_counter()
+            pool.map(_oracle_unit, [(schedule, W, l % SCHED_L) for l in range(units)], chunksize=1)
+            wall = time.perf_counter() - t0
+        out["all_cores"] = {
+            "value": round(units * T / (wall * SCHED_L), 3), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "cpu_model": out["cpu_model"],
+            "sample": f"fp64 numpy oracle, {units} (layer, sequence) units over {cores} spawned "
+                      f"processes (one thread each), wall {wall:.2f} s after one warm-up unit per "
+                      "process; scaled to the 16-layer step"}
+    return out
 
 
 def reference_arm(args):
     """--impl reference: the fp64 oracle timed on this host, each step one
-    sequence of one layer (bounded sample), scaled to the 16-layer step."""
+    sequence of one layer (bounded sample).  ms_per_step is that sample's own
+    time, so steps x ms_per_step is the time this arm actually ran; value is
+    the throughput scaled to the workload (B sequences x 16 layers per step),
+    with the scale stated in sample_scale."""
     for _ in range(args.warmup):
         oracle_step_sample(args.schedule, args.W, 1, 7)
     ts = [oracle_step_sample(args.schedule, args.W, 1, 7) for _ in range(args.steps)]
     sec = sum(ts) / len(ts)
     val = T / (sec * LAYERS)
     cb = {"value": round(val, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+          "cpu_model": cpu_model(),
           "sample": f"fp64 numpy oracle, one {T}-token sequence of layer 7 per step, W={args.W}, "
                     "fwd+bwd incl. dtheta, single thread; scaled to 16 layers"}
     return {"metric": METRIC, "impl": "reference", "value": round(val, 3), "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(sec * LAYERS * 1e3 * (B * T) / T, 1), "higher_is_better": True,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "sample_scale": {"per_step": f"1 sequence x 1 layer of the workload's {B} sequences x "
+                                         f"{LAYERS} layers",
+                             "factor": B * LAYERS,
+                             "workload_ms_per_step": round(sec * 1e3 * B * LAYERS, 1)},
             "config": config(args), "cpu_baseline": cb,
             "e2e": {"value": round(val, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -796,6 +861,63 @@ def configs_arm(args, dev):
     return out
 
 
+def grid_arm(args, dev):
+    """The 16-layer step of the interpolated configuration over its whole grid:
+    W in {6, 8, 10, 12} x {linear, coprime} alpha schedules.  Each point builds
+    its 16 layers (own seeded inputs, rotated keys once per layer), captures
+    the step as one CUDA graph and times K replays with CUDA events after the
+    warm-ups; one JSON object per point."""
+    import ctypes as C
+    import torch
+
+    import sfa_inputs as si
+    import static_offset_sparse_gb300 as sfa
+    from static_offset_sparse_gb300._lib import _lib
+
+    lib = _lib()
+    peak, src = hbm_peak()
+    out = []
+    for schedule in ("linear", "coprime"):
+        al = alphas(schedule)
+        for W in (6, 8, 10, 12):
+            layers = [Layer(sfa, lib, si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", rank_seed(0), dev,
+                                                           layer=l), al[l], W, dev)
+                      for l in layer_ids()]
+            stream = torch.cuda.current_stream()
+            sp = C.c_void_p(stream.cuda_stream)
+            for _ in range(args.warmup):
+                for L in layers:
+                    L.run(sp)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cs = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+                for L in layers:
+                    L.run(cs)
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+            n = max(3, min(args.steps, 50))
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(n):
+                graph.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            assert sfa.get_device_status() == 0
+            ms = ev0.elapsed_time(ev1) / n
+            hbm = UNIQUE_BYTES_PER_TOKEN * B * T * len(layers) / (ms * 1e-3) / 1e9
+            keys = sum(pair_counts(L.alpha, W)[0] for L in layers) / len(layers) / T
+            out.append({"config": f"2 grid: {schedule}, W={W}", "B": B, "T": T, "heads": f"{HQ}/{HKV}",
+                        "layers": len(layers), "dtype": "bf16", "direction": "fwd+bwd+dtheta",
+                        "ms_per_step": round(ms, 4), "tokens_per_s": round(B * T / (ms * 1e-3), 1),
+                        "hbm_frac": round(hbm / peak, 4), "hbm_peak_source": src,
+                        "keys_per_query": round(keys, 2), "timing": f"CUDA graph of the step, {n} replays"})
+            del layers, graph
+            torch.cuda.empty_cache()
+    return out
+
+
 def config(args):
     return {"workload": f"interp {args.schedule} schedule, W={args.W}: B={B} T={T} Hq={HQ} Hkv={HKV} "
                         f"D={D}, {LAYERS} layers, Fibonacci K=15, RoPE 1e4, fwd+bwd+dtheta",
@@ -816,7 +938,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
     ap.add_argument("--only", default="", help="configs mode: run the configurations whose name "
-                    "starts with this (e.g. '5:')")
+                    "starts with this (e.g. '5:'; '2 grid' runs only the W x schedule grid)")
     ap.add_argument("--mode", default="train", choices=["train", "decode", "configs"],
                     help="train: the fwd+bwd step (default); decode: one token per sequence; "
                          "configs: one line per configuration of the pages")
@@ -853,8 +975,12 @@ def main():
         return
     if args.mode == "configs":
         if rank == 0:
-            for line in configs_arm(args, dev):
-                print(json.dumps(line), flush=True)
+            if not args.only or args.only.startswith("2 grid"):
+                for line in grid_arm(args, dev):
+                    print(json.dumps(line), flush=True)
+            if args.only != "2 grid":
+                for line in configs_arm(args, dev):
+                    print(json.dumps(line), flush=True)
         return
     layers, ms, clk, launches, roofline = gpu_arm(args, rank, world, dev)
     value = world * B * T / (ms * 1e-3)

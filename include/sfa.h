@@ -269,9 +269,12 @@ int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const 
  * array of SFA_STATIC_WS_BYTES that every GPU loading the library keeps until
  * the process exits.  Calls whose sfa_workspace_size(d, 1, 0) exceeds that
  * return SFA_ERR_CAPACITY and launch nothing (B * Hkv * T <= 65536 rows with
- * RoPE, e.g. B = 32, Hkv = 2, T = 1024).  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress, that device current);
- * make it before any stream capture.  Nothing is allocated or freed.  All
+ * RoPE, e.g. B = 32, Hkv = 2, T = 1024; a call given d->k_rot needs no
+ * scratch and has no such limit).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, that device current); make it
+ * before any stream capture.  The address is kept with the context it belongs
+ * to, and a call from a new context of that device (after cudaDeviceReset,
+ * say) looks it up again, before launching.  Nothing is allocated or freed.  All
  * calls share the one array: calls that overlap on the GPU (other streams,
  * other threads) race on it; serialize them.  The array needs no clearing
  * (each call writes the scratch rows it reads). */
@@ -302,6 +305,20 @@ int sfa_timing_read(double* ms, int64_t* launches, int n);
  * sfa_status recorded by a kernel's bounds check or bounded wait since the
  * last call, SFA_OK if none) and clear it. */
 int sfa_get_device_status(void* stream, int32_t* out);
+
+/* Test injection for the bounded waits (no counterpart on the pages; for
+ * tests of the failure path only).  Every mbarrier wait of the TMA-staged
+ * kernels gives up after `wait_cycles` SM clock cycles (0 restores the
+ * default of 2e9, about 1 s at 2.07 GHz); the CTA then records
+ * SFA_ERR_TIMEOUT in the device status word, waits (bounded) for its own
+ * loads in flight and leaves.  skip_group >= 0 makes CTA (0, 0) of the rung
+ * tensor-core forward and query-side backward issue neither the expect_tx
+ * nor the loads of that staged group (window chunks first, then rung pairs),
+ * so its consumers' wait runs out with nothing in flight; -1 turns this off.
+ * The setting is process-wide and read by every later call until changed;
+ * the outputs of a call that timed out are undefined.  Returns
+ * SFA_ERR_INVALID_ARG for wait_cycles < 0 or skip_group < -1. */
+int sfa_debug_inject(int64_t wait_cycles, int32_t skip_group);
 
 #ifdef __cplusplus
 }

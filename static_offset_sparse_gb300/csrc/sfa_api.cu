@@ -76,16 +76,40 @@ int launch_rope_table(int T, double theta, float* table, void* stream);
 // index checks); sfa_get_device_status reads and clears it.
 static __device__ int g_status;
 
+// The CUDA context current on the calling thread (driver entry point, no
+// libcuda link); nullptr if none is current or it cannot be read.
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of g_status, cached per device together with the context it
+// was looked up in (a new context, e.g. after cudaDeviceReset, looks it up
+// again).
 static int status_ptr(int** out) {
   static std::mutex mu;
   static int* cache[64] = {nullptr};
+  static CUcontext owner[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SFA_ERR_CUDA;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+  if (!ctx || !cache[dev] || owner[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return SFA_ERR_CUDA;
     cache[dev] = static_cast<int*>(p);
+    owner[dev] = current_context();
   }
   *out = cache[dev];
   return SFA_OK;
@@ -118,6 +142,12 @@ void timing_stop(int id, void* stream) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Test injection (sfa_debug_inject): the bounded-wait limit and the group
+// whose loads CTA (0, 0) of a rung tensor-core kernel never issues.
+static std::mutex g_dbg_mu;
+static long long g_dbg_wait = 0;  // 0: kDefaultWaitCycles
+static int g_dbg_skip = -1;
+
 static int fill_args(const sfa_desc* d, AttnArgs* a) {
   *a = AttnArgs{};
   a->B = d->B;
@@ -127,6 +157,11 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
   a->lgG = __builtin_ctz((unsigned)(d->Hq / d->Hkv));
   a->rope = d->rope;
   a->alpha = d->alpha;
+  {
+    std::lock_guard<std::mutex> lock(g_dbg_mu);
+    a->wait_cycles = g_dbg_wait > 0 ? g_dbg_wait : kDefaultWaitCycles;
+    a->debug_skip = g_dbg_skip;
+  }
   if (d->rope && !aligned16(d->rope)) return SFA_ERR_INVALID_ARG;
   if (d->k_rot && !aligned16(d->k_rot)) return SFA_ERR_INVALID_ARG;
   return status_ptr(&a->status);
@@ -339,6 +374,14 @@ int sfa_decode_int(const sfa_desc* d, const void* q, const void* k_cache, const 
   a.out_o = o;
   a.out_lse = lse;
   return launch_decode_int(a, p, d->dtype, stream);
+}
+
+int sfa_debug_inject(int64_t wait_cycles, int32_t skip_group) {
+  if (wait_cycles < 0 || skip_group < -1) return SFA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_dbg_mu);
+  g_dbg_wait = wait_cycles;
+  g_dbg_skip = skip_group;
+  return SFA_OK;
 }
 
 int sfa_timing_enable(int on) {

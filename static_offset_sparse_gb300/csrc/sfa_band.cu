@@ -279,10 +279,10 @@ __device__ __forceinline__ void band_init_bars(uint64_t* bars) {
 
 // Bounded wait on a barrier, uniform across the CTA (false: timed out, the
 // status word holds SFA_ERR_TIMEOUT).
-__device__ __forceinline__ bool band_wait(uint64_t* bar, uint32_t parity, int* status) {
-  const bool ok = mbar_wait_bounded(smem_u32(bar), parity);
+__device__ __forceinline__ bool band_wait(uint64_t* bar, uint32_t parity, const AttnArgs& a) {
+  const bool ok = mbar_wait_bounded(smem_u32(bar), parity, a.wait_cycles);
   if (__syncthreads_or(!ok)) {
-    if (threadIdx.x == 0) record_status(status, SFA_ERR_TIMEOUT);
+    if (threadIdx.x == 0) record_status(a.status, SFA_ERR_TIMEOUT);
     return false;
   }
   return true;
@@ -294,16 +294,16 @@ __device__ __forceinline__ bool band_wait(uint64_t* bar, uint32_t parity, int* s
 // stage address) runs on every thread.  False (uniformly) on a timeout,
 // after thread 0 has waited out the loads still in flight.
 template <typename IssueFn, typename ComputeFn>
-__device__ __forceinline__ bool band_loop(int NT, uint32_t stages, uint64_t* bars, int* status,
+__device__ __forceinline__ bool band_loop(int NT, uint32_t stages, uint64_t* bars, const AttnArgs& a,
                                           IssueFn issue, ComputeFn compute) {
   for (int t = 0; t < NT; ++t) {
     const int s = t % kBStages;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (t / kBStages) & 1);
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (t / kBStages) & 1, a.wait_cycles);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
-        record_status(status, SFA_ERR_TIMEOUT);
+        record_status(a.status, SFA_ERR_TIMEOUT);
         for (int t2 = t; t2 < NT && t2 < t + kBStages - 1; ++t2)
-          mbar_wait_bounded(smem_u32(&bars[t2 % kBStages]), (t2 / kBStages) & 1);
+          mbar_wait_bounded(smem_u32(&bars[t2 % kBStages]), (t2 / kBStages) & 1, a.wait_cycles);
       }
       return false;
     }
@@ -316,9 +316,9 @@ __device__ __forceinline__ bool band_loop(int NT, uint32_t stages, uint64_t* bar
 
 // Thread 0 waits out the first stages' loads after the CTA's own tiles timed
 // out (nothing may land in shared memory after the CTA has left).
-__device__ __forceinline__ void band_drain(uint64_t* bars, int NT) {
+__device__ __forceinline__ void band_drain(uint64_t* bars, int NT, const AttnArgs& a) {
   if (threadIdx.x == 0)
-    for (int s = 0; s < kBStages && s < NT; ++s) mbar_wait_bounded(smem_u32(&bars[s]), 0);
+    for (int s = 0; s < kBStages && s < NT; ++s) mbar_wait_bounded(smem_u32(&bars[s]), 0, a.wait_cycles);
 }
 
 // Online softmax over N keys of a tile for rows gid (x = 0) and gid + 8 of a
@@ -459,8 +459,8 @@ __global__ void __launch_bounds__(kBThreads, 4)
   const float2* rope = static_cast<const float2*>(a.rope);
   float4 rp[2][4];
   if (rope) band_rope_pairs(rope, q.pos, rp);  // while the Q tile is in flight
-  if (!band_wait(&bars[kBStages], 0, a.status)) {
-    band_drain(bars, NT);
+  if (!band_wait(&bars[kBStages], 0, a)) {
+    band_drain(bars, NT, a);
     return;
   }
   // q~ = q'/8 rounded exactly as the backward rounds it, log2(e) applied to
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kBThreads, 4)
   QWalk cw{0, 0, 0, 0, 0};
   qwalk_seek(P, q.r, q.u0, q.ul, cw);
 
-  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
+  const bool ok = band_loop(NT, stages, bars, a, issue, [&](int, uint32_t kst) {
     // every warp computes the whole tile (skipping the n-tiles outside its
     // rows' bands measured slower: it breaks up the load and product batches
     // the scheduler overlaps), in two halves of 32 keys with one softmax step
@@ -603,8 +603,8 @@ __global__ void __launch_bounds__(kBThreads, 3)
   for (int x = 0; x < 2; ++x) lse2[x] = a.lse[(int64_t)(q.qplane + q.hh[x]) * a.T + q.pos[x]] * kLog2e;
   float4 rp[2][4];
   if (rope) band_rope_pairs(rope, q.pos, rp);  // while the query tiles are in flight
-  if (!band_wait(&bars[kBStages], 0, a.status)) {
-    band_drain(bars, NT);
+  if (!band_wait(&bars[kBStages], 0, a)) {
+    band_drain(bars, NT, a);
     return;
   }
   uint32_t qa[4][4], da[4][4];
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
   int umin, umax;
   q.warp_span(umin, umax);
 
-  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t kst) {
+  const bool ok = band_loop(NT, stages, bars, a, issue, [&](int, uint32_t kst) {
     const uint32_t vst = kst + kBTileB;
     int lo[2], hi[2];
     q.cols(P, cw, lo, hi);
@@ -780,8 +780,8 @@ __global__ void __launch_bounds__(kBThreads, 3)
     kwalk_seek(P, rho, v0, vl, Uc, iw);
     for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
   }
-  if (!band_wait(&bars[kBStages], 0, a.status)) {
-    band_drain(bars, NT);
+  if (!band_wait(&bars[kBStages], 0, a)) {
+    band_drain(bars, NT, a);
     return;
   }
   float dk[8][4], dv[8][4];
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
   // keys of this warp's 16 rows (none past the sequence)
   const int vmin = v0 + 16 * warp, vmax = min(vmin + 15, Uc - 1);
 
-  const bool ok = band_loop(NT, stages, bars, a.status, issue, [&](int, uint32_t qst) {
+  const bool ok = band_loop(NT, stages, bars, a, issue, [&](int, uint32_t qst) {
     const uint32_t dst = qst + kBTileB;
     const int len = P.len[cw.m];
     // query u of column n reaches key v of row x iff t = u - v + e is in [0, len)

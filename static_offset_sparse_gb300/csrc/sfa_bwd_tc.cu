@@ -79,8 +79,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   const uint32_t qtile = sbase, dotile = sbase + kTcQTileB, otile = sbase + 2 * kTcQTileB;
   const uint32_t stages = sbase + 3 * kTcQTileB;
   const int qplane = b * a.Hq + g * 4;
+  const int skip_grp = (blockIdx.x | blockIdx.y) == 0 ? a.debug_skip : -1;  // test injection
   const CUtensorMap* qmaps[3] = {&mq, &mdo, &mo};
-  tc_start(&mk, &mv, qmaps, 3, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+  tc_start(&mk, &mv, qmaps, 3, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars, skip_grp);
 
   uint32_t qa[4][4], da[4][4];
   float delta[2], lse2[2];
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   lse2[1] = a.lse[rowB] * kLog2e;
   float4 rp[4];
   if (rope) load_frag_rope(rope, ic, rp);  // while the query tiles are in flight
-  if (!tc_wait_qtiles(bars, a.status)) return;
+  if (!tc_wait_qtiles(bars, a)) return;
   tile_frags(qtile, warp, rope ? rp : nullptr, 0.125f, true, qa);
   tile_frags(dotile, warp, nullptr, 1.0f, false, da);
   {  // delta = dO . O per row, from the dO and O fragments of this lane (16 dims), then the quad
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
   const int colrow2 = 4 * warp + ((((lane & 7) >> 1) + 2) & 3) + (lane & 1);
 
-  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a.status,
+  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a, skip_grp,
                               [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t sa[4];
     if (grp < nwc) {
@@ -416,12 +417,12 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   for (int gt = 0; gt < NGt; ++gt) {
     const int grp = MULTI ? grpm : gt;
     const int st = gt % kKvStages;
-    const bool okw = mbar_wait_bounded(smem_u32(&bars[st]), (gt / kKvStages) & 1);
+    const bool okw = mbar_wait_bounded(smem_u32(&bars[st]), (gt / kKvStages) & 1, a.wait_cycles);
     if (__syncthreads_or(!okw)) {
       if (tid == 0) {
         record_status(a.status, SFA_ERR_TIMEOUT);
         for (int g2 = gt; g2 < NGt && g2 < gt + kKvStages; ++g2)
-          mbar_wait_bounded(smem_u32(&bars[g2 % kKvStages]), (g2 / kKvStages) & 1);
+          mbar_wait_bounded(smem_u32(&bars[g2 % kKvStages]), (g2 / kKvStages) & 1, a.wait_cycles);
       }
       return;
     }

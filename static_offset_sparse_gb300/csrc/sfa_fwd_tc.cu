@@ -103,11 +103,12 @@ __global__ void __launch_bounds__(kTcThreads, 5)
   const int NG = nwc + (nr + 1) / 2;
   const uint32_t qtile = sbase, stages = sbase + kTcQTileB;
   const int qplane = b * a.Hq + g * 4;
+  const int skip_grp = (blockIdx.x | blockIdx.y) == 0 ? a.debug_skip : -1;  // test injection
   const CUtensorMap* qmaps[1] = {&mq};
-  tc_start(&mk, &mv, qmaps, 1, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars);
+  tc_start(&mk, &mv, qmaps, 1, qtile, qplane, P, bg, i0, nwc, nr, NG, stages, bars, skip_grp);
   float4 rp[4];
   if (rope) load_frag_rope(rope, min(i, T - 1), rp);  // while the Q tile is in flight
-  if (!tc_wait_qtiles(bars, a.status)) return;
+  if (!tc_wait_qtiles(bars, a)) return;
   uint32_t qa[4][4];
   // q~ = q'/8 rounded exactly as the query-side backward rounds it, log2(e)
   // applied to the fp32 logits: the backward's P = exp(S - LSE) recomputes
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, 5)
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
 
-  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a.status,
+  const bool ok = tc_run(&mk, &mv, P, bg, i0, nwc, nr, NG, stages, bars, a, skip_grp,
                               [&](int grp, uint32_t kst, uint32_t vst) {
     uint32_t pa[4];
     if (grp < nwc) {

@@ -6,6 +6,8 @@
 
 #include "sfa.h"
 
+struct CUctx_st;  // CUcontext
+
 namespace sfa {
 
 constexpr int kD = 64;          // head dimension (the only one supported)
@@ -62,7 +64,13 @@ struct AttnArgs {
   const int32_t* pos;  // decode: device [B] query positions
   int32_t B, T, Hq, Hkv, lgG;  // G = 1 << lgG query heads per KV head
   int* status;         // device status word
+  long long wait_cycles;  // limit of every bounded mbarrier wait, in SM clock cycles
+  int32_t debug_skip;     // test injection: group whose loads CTA (0, 0) never issues, or -1
 };
+
+// Default limit of a bounded mbarrier wait: ~1 s at the GB300's 2.07 GHz
+// maximum SM clock.
+constexpr long long kDefaultWaitCycles = 2000000000LL;
 
 // Kernel launchers (stream is a cudaStream_t).
 // The rung tensor-core kernels serve bf16 I/O with G = 4m (m = 1, 2, 4: groups
@@ -96,6 +104,8 @@ int launch_band_backward(const AttnArgs& a, const BandPlan& p, const void* kr, v
                          void* stat, void* stream);
 
 // Optional launch timing (sfa_api.cu): returns a record id or -1 when off.
+// The CUDA context current on the calling thread, nullptr if none (sfa_api.cu).
+::CUctx_st* current_context();
 int timing_start(int kind, void* stream);
 void timing_stop(int id, void* stream);
 

@@ -19,7 +19,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte async global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
+// ldmatrix: four 8x8 b16 tiles from shared memory (lanes 8t..8t+7 give tile t's row addresses).
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"

@@ -8,6 +8,7 @@
 // kernel) in a file-scope device array of SFA_STATIC_WS_BYTES that every GPU
 // loading the library holds until the process exits.  The caller still
 // provides q, k, v, o and lse.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -20,18 +21,24 @@ namespace {
 // symbol: its device address comes from cudaGetSymbolAddress below.
 __device__ __align__(256) unsigned char g_static_ws[SFA_STATIC_WS_BYTES];
 
-// Device address of g_static_ws on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of g_static_ws on the current device.  It is looked up with
+// that device current on the first call there and cached together with the
+// context it belongs to; a call from another context of the same device (for
+// instance after cudaDeviceReset made a fresh primary context) looks it up
+// again, so a cached address never outlives its context.
 int static_ws_address(void** out) {
   static std::mutex mu;
   static void* cache[64] = {nullptr};
+  static CUcontext owner[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SFA_ERR_CUDA;
+  const CUcontext ctx = sfa::current_context();  // nullptr before the first runtime call
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* p = nullptr;
+  if (!ctx || !cache[dev] || owner[dev] != ctx) {
+    void* p = nullptr;  // the lookup makes the device's primary context current if none was
     if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return SFA_ERR_CUDA;
     cache[dev] = p;
+    owner[dev] = sfa::current_context();
   }
   *out = cache[dev];
   return SFA_OK;

@@ -59,9 +59,14 @@ __device__ __forceinline__ void pv_tile(const uint32_t* pa, uint32_t region, int
 // Issue the TMA loads of group `grp` (a window chunk, then rung pairs) into
 // a stage (thread 0 only).  An unpaired rung reloads its partner's slab: its
 // probabilities are zero, and the rows stay finite.
+//
+// skip (test injection only, AttnArgs::debug_skip): issue neither the
+// expect_tx nor the loads, so the stage's barrier never completes and its
+// consumers' bounded wait runs out with nothing in flight.
 __device__ __forceinline__ void tc_issue_group(const CUtensorMap* mk, const CUtensorMap* mv,
                                                const Plan& P, int bg, int i0, int nwc, int nr,
-                                               int grp, uint32_t st, uint32_t bar) {
+                                               int grp, uint32_t st, uint32_t bar, bool skip) {
+  if (skip) return;
   int y0, y1;
   if (grp < nwc) {
     y0 = i0 - kTcWC - kTcWC * grp;
@@ -93,10 +98,13 @@ constexpr size_t kBwdQTcSmem = (size_t)3 * kTcQTileB + (size_t)kTcStages * kTcSt
 // Barriers: one per stage, then one for the query tiles.  Thread 0 issues
 // the query-tile loads (nq boxes from the maps in qmaps, at coordinates
 // (0, i0, plane)) and the first stages.
+//
+// skip_grp: the group whose loads this CTA never issues (test injection
+// through AttnArgs::debug_skip, for CTA (0, 0) only), or -1.
 __device__ __forceinline__ void tc_start(const CUtensorMap* mk, const CUtensorMap* mv,
                                          const CUtensorMap* const* qmaps, int nq, uint32_t qtile,
                                          int qplane, const Plan& P, int bg, int i0, int nwc, int nr,
-                                         int NG, uint32_t sbase, uint64_t* bars) {
+                                         int NG, uint32_t sbase, uint64_t* bars, int skip_grp) {
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s <= kTcStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
@@ -109,15 +117,16 @@ __device__ __forceinline__ void tc_start(const CUtensorMap* mk, const CUtensorMa
     mbar_expect_tx(qb, nq * kTcQTileB);
     for (int x = 0; x < nq; ++x) tma_load_3d(qtile + x * kTcQTileB, qmaps[x], 0, i0, qplane, qb);
     for (int s = 0; s < kTcStages && s < NG; ++s)
-      tc_issue_group(mk, mv, P, bg, i0, nwc, nr, s, sbase + s * kTcStageB, smem_u32(&bars[s]));
+      tc_issue_group(mk, mv, P, bg, i0, nwc, nr, s, sbase + s * kTcStageB, smem_u32(&bars[s]),
+                     s == skip_grp);
   }
 }
 
 // Wait (bounded) for the query tiles; uniform across the CTA.
-__device__ __forceinline__ bool tc_wait_qtiles(uint64_t* bars, int* status) {
-  const bool ok = mbar_wait_bounded(smem_u32(&bars[kTcStages]), 0);
+__device__ __forceinline__ bool tc_wait_qtiles(uint64_t* bars, const AttnArgs& a) {
+  const bool ok = mbar_wait_bounded(smem_u32(&bars[kTcStages]), 0, a.wait_cycles);
   if (__syncthreads_or(!ok)) {
-    if (threadIdx.x == 0) record_status(status, SFA_ERR_TIMEOUT);
+    if (threadIdx.x == 0) record_status(a.status, SFA_ERR_TIMEOUT);
     return false;
   }
   return true;
@@ -130,25 +139,26 @@ __device__ __forceinline__ bool tc_wait_qtiles(uint64_t* bars, int* status) {
 template <typename ComputeFn>
 __device__ __forceinline__ bool tc_run(const CUtensorMap* mk, const CUtensorMap* mv, const Plan& P,
                                        int bg, int i0, int nwc, int nr, int NG, uint32_t sbase,
-                                       uint64_t* bars, int* status, ComputeFn compute) {
+                                       uint64_t* bars, const AttnArgs& a, int skip_grp,
+                                       ComputeFn compute) {
   const int tid = threadIdx.x;
   for (int grp = 0; grp < NG; ++grp) {
     const int s = grp % kTcStages;
-    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (grp / kTcStages) & 1);
+    const bool ok = mbar_wait_bounded(smem_u32(&bars[s]), (grp / kTcStages) & 1, a.wait_cycles);
     // One barrier per group: it makes the timeout decision uniform and, as
     // every thread has finished group grp - 1, frees that group's stage.
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
-        record_status(status, SFA_ERR_TIMEOUT);
+        record_status(a.status, SFA_ERR_TIMEOUT);
         for (int g2 = grp; g2 < NG && g2 < grp + kTcStages - 1; ++g2)  // loads still in flight
-          mbar_wait_bounded(smem_u32(&bars[g2 % kTcStages]), (g2 / kTcStages) & 1);
+          mbar_wait_bounded(smem_u32(&bars[g2 % kTcStages]), (g2 / kTcStages) & 1, a.wait_cycles);
       }
       return false;
     }
     if (tid == 0 && grp > 0 && grp - 1 + kTcStages < NG) {
       const int sp = (grp - 1) % kTcStages;
       tc_issue_group(mk, mv, P, bg, i0, nwc, nr, grp - 1 + kTcStages, sbase + sp * kTcStageB,
-                     smem_u32(&bars[sp]));
+                     smem_u32(&bars[sp]), grp - 1 + kTcStages == skip_grp);
     }
     const uint32_t kst = sbase + s * kTcStageB;
     compute(grp, kst, kst + kTcRegionB);

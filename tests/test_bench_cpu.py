@@ -50,9 +50,13 @@ def test_unique_bytes_per_token():
 
 
 def test_reference_arm_json_line():
+    import time
+
+    t0 = time.perf_counter()
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600,
                        cwd=ROOT)
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -62,3 +66,8 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["seq_len"] == 1024 and d["config"]["global_batch"] == 32
+    # the timed steps fit in the run that printed them; the scale to the
+    # workload's step (32 sequences x 16 layers) is a separate field
+    assert d["steps"] * d["ms_per_step"] * 1e-3 <= wall
+    assert d["sample_scale"]["factor"] == 32 * 16
+    assert abs(d["value"] - 32 * 1024 / (d["sample_scale"]["workload_ms_per_step"] * 1e-3)) <= 1e-2 * d["value"]

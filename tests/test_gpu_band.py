@@ -10,6 +10,7 @@ import pytest
 
 import oracle as o
 import sfa_inputs as si
+from tolerances import check_close
 
 pytestmark = pytest.mark.gpu
 
@@ -26,10 +27,7 @@ def sfa(sfa_lib):
 
 
 def _check(name, got, want):
-    lim = 2e-2 + 2.0 ** -8 * np.abs(want)
-    err = np.abs(got - want)
-    assert np.isfinite(got).all(), f"{name}: non-finite"
-    assert (err <= lim).all(), f"{name}: max err {err.max():.3g}"
+    check_close(name, got, want, True)
 
 
 SETS = {

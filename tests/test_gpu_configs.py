@@ -11,7 +11,7 @@ import pytest
 
 import oracle as o
 import sfa_inputs as si
-from tolerances import check_dalpha_dtheta
+from tolerances import check_close, check_dalpha_dtheta
 
 pytestmark = pytest.mark.gpu
 
@@ -36,11 +36,7 @@ def _np(t):
 
 
 def _close(name, got, want, bf16, tol=None):
-    tol = tol if tol is not None else (2e-2 if bf16 else 1e-5)
-    lim = tol + (2.0 ** -8) * np.abs(want) if bf16 else tol
-    err = np.abs(got - want)
-    assert np.isfinite(got).all(), f"{name}: non-finite"
-    assert (err <= lim).all(), f"{name}: max err {err.max():.3g} (bound {np.max(lim):.3g})"
+    check_close(name, got, want, bf16, tol=tol)
 
 
 def _sampled(sfa, x, pairs, slots, theta, fwd, bwd, bf16, check_bwd=True):
@@ -73,13 +69,17 @@ def test_config1_fp32_full(sfa):
     _, _, g = _sampled(sfa, x, [(0, 0), (0, 1)], slots, 1e4, fwd, bwd, False)
     gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4, alpha=1.0)
     da, dt = _np(g[3])
+    # at alpha = 1 (theta = 0) dtheta = dalpha (1 - 0.5)(1.5 - 1) = dalpha / 4, not zero
+    assert abs(gw["dtheta"] - 0.25 * gw["dalpha"]) <= 1e-12 * abs(gw["dalpha"])
     assert abs(da - gw["dalpha"]) <= 1e-3 * abs(gw["dalpha"])
-    assert dt == 0.0 or abs(dt - gw["dtheta"]) <= 1e-3 * abs(gw["dtheta"])
+    assert abs(dt - gw["dtheta"]) <= 1e-3 * abs(gw["dtheta"])
 
 
 @pytest.mark.parametrize("W,alpha,full_dtheta", [
     (8, 0.5 + 5 / 15, True),          # linear layer 5: fl64(alpha * 144) just below 120
+    (8, 0.5 + (7 * 6 % 16) / 15, True),   # coprime layer 6 (alpha index 10)
     (6, 0.5 + (7 * 3 % 16) / 15, False),  # coprime layer 3
+    (10, 0.5 + 11 / 15, False),       # linear layer 11
     (12, 1.5, False),                 # last linear layer
 ])
 def test_config2_bf16_interp(sfa, W, alpha, full_dtheta):
@@ -104,7 +104,7 @@ def test_config3_pow2(sfa, alpha):
     _sampled(sfa, x, [(5, 1), (30, 0)], slots, 1e4, fwd, bwd, True)
 
 
-@pytest.mark.parametrize("T,alpha", [(2048, 0.5), (16384, 1.5), (4096, 1.0)])
+@pytest.mark.parametrize("T,alpha", [(2048, 0.5), (4096, 1.0), (8192, 1.0), (16384, 1.5)])
 def test_config4_int_forward_long(sfa, T, alpha):
     dist = o.int_distances(FIB, alpha, 8)
     x = si.make_qkvdo(4, T, 8, 2, 64, "bf16", seed=si.mix_seed(0, 4), layer=T, with_do=False)

@@ -8,6 +8,7 @@ import pytest
 
 import oracle as o
 import sfa_inputs as si
+from tolerances import check_close
 
 pytestmark = pytest.mark.gpu
 
@@ -24,10 +25,7 @@ def sfa(sfa_lib):
 
 
 def _check(name, got, want, bf16):
-    lim = 2e-2 + 2.0 ** -8 * np.abs(want) if bf16 else 1e-5
-    err = np.abs(got - want)
-    assert np.isfinite(got).all(), f"{name}: non-finite"
-    assert (err <= lim).all(), f"{name}: max err {err.max():.3g}"
+    check_close(name, got, want, bf16)
 
 
 SETS = {
