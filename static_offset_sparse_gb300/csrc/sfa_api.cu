@@ -26,7 +26,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h) {
+int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h,
+                  bool swizzle) {
   auto fn = encode_fn();
   if (!fn) return SFA_ERR_CUDA;
   const cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)planes};
@@ -34,7 +35,8 @@ int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int b
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_h};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
              ? SFA_OK
              : SFA_ERR_CUDA;
@@ -238,9 +240,9 @@ static int forward_common(const sfa_desc* d, int interp, const void* q, const vo
 }
 
 static size_t backward_bytes(const sfa_desc* d, const Plan& p, const BandPlan& bp) {
-  size_t a, b, c;
+  size_t a, b, c, e;
   if (bp.delta > 0) return band_backward_workspace_bytes(d, &a, &b, &c);
-  return tc_path(d, p) ? backward_tc_workspace_bytes(d, p, &a, &b, &c) : backward_workspace_bytes(d, p);
+  return tc_path(d, p) ? backward_tc_workspace_bytes(d, p, &a, &b, &c, &e) : backward_workspace_bytes(d, p);
 }
 
 static int backward_common(const sfa_desc* d, int interp, const void* q, const void* k,
@@ -280,8 +282,9 @@ static int backward_common(const sfa_desc* d, int interp, const void* q, const v
     return launch_band_backward(a, bp, kr, w + oqt, w + ost, stream);
   }
   if (tc_path(d, p)) {
-    size_t okr, oqt, oco;
-    backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco);
+    size_t okr, oqt, oco, ocr;
+    backward_tc_workspace_bytes(d, p, &okr, &oqt, &oco, &ocr);
+    a.dcorr = ocr ? reinterpret_cast<float*>(w + ocr) : nullptr;
     const void* kr = nullptr;
     if ((rc = rotated_keys(d, k, w + okr, stream, &kr)) != SFA_OK) return rc;
     return launch_backward_tc(a, p, kr, w + oqt, w + oco, stream);

@@ -39,7 +39,9 @@ __device__ __forceinline__ void write_coef_half(uint4* dst, float wt, float ds0,
   *dst = make_uint4(dh, pack_bf16(a0 - dhf.x, a1 - dhf.y), ph, pack_bf16(b0 - phf.x, b1 - phf.y));
 }
 
-template <bool INTERP>
+// PSI (G > 4): also sum psi = sum_j P_ij dP_ij per row and write delta - psi
+// for the key side's correction (a.dcorr).
+template <bool INTERP, bool PSI>
 __global__ void __launch_bounds__(kTcThreads, 4)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
@@ -125,6 +127,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) dq[nd][0] = dq[nd][1] = dq[nd][2] = dq[nd][3] = 0.0f;
   float dacc = 0.0f;
+  // psi = sum_j P_ij dP_ij per row (this lane's keys), equal to dO . O for the
+  // exact O: the key side of G > 4 corrects its dS by P (delta - psi)
+  float psi[2] = {0.0f, 0.0f};
   // records of query i: [slot][2 x uint4]; this lane's rows gid, gid + 8 are
   // heads hA, hA + 2 of position p, i.e. half gid >> 2 of each record
   uint4* crow = coef + ((int64_t)qy * T + ic) * NS * 2 + (gid >> 2);
@@ -155,6 +160,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
           const float pr = v ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[r])) : 0.0f;
           ds[r][2 * nt + (e & 1)] = pr * (dp[nt][e] - delta[r]);
           pp[r][2 * nt + (e & 1)] = pr;
+          if (PSI) psi[r] = fmaf(pr, dp[nt][e], psi[r]);
         }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -196,6 +202,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
         const float d = pr * (dpi - delta[r]);
         ds[r] = d;
         prr[r] = pr;
+        if (PSI) psi[r] = fmaf(pr, dpi, psi[r]);
         if (INTERP && v) dacc = fmaf(f, fmaf(d, a0 - a1, pr * (b0 - b1)), dacc);
       }
       if (v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
@@ -212,6 +219,18 @@ __global__ void __launch_bounds__(kTcThreads, 4)
     }
   });
   if (!ok) return;
+
+  if (PSI) {  // delta - psi per (row, head), for the key side's correction
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      psi[r] += __shfl_xor_sync(0xffffffffu, psi[r], 1);
+      psi[r] += __shfl_xor_sync(0xffffffffu, psi[r], 2);
+    }
+    if (tig == 0 && act) {
+      a.dcorr[rowA] = delta[0] - psi[0];
+      a.dcorr[rowB] = delta[1] - psi[1];
+    }
+  }
 
   if (INTERP && a.dalpha_out) {
     // per-CTA partial of dL/dalpha; the key-side kernel, which runs after this
@@ -281,11 +300,17 @@ constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 
 // One group's products for a warp: NKS k-steps of 16 (query, head) pairs.
 // dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
-template <int NKS>
+// FOLD (G > 4): corr points at delta - psi of the group's 4 query heads
+// ([4][T], written by the query side), and each dS coefficient becomes
+// wt dS + (wt P)(delta - psi) = wt P (dP - psi): the dS of the exact
+// delta = sum_j P_ij dP_ij instead of dO . O from the bf16-rounded O, whose
+// error the key side would otherwise sum over G heads.  The correction is
+// folded into the lo word.
+template <int NKS, bool FOLD>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int nsl,
                                          bool win, int s_lo, int s_hi, int c, int qw, int kq,
-                                         int qoff, int j, int T, int dh, float (*dk)[4],
-                                         float (*dv)[4]) {
+                                         int qoff, int j, int T, int dh, const float* corr,
+                                         float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
@@ -313,6 +338,12 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
         bkl[hb] = rec.y;
         bvv[hb] = rec.z;
         bvl[hb] = rec.w;
+        if (FOLD) {  // heads tig & 1 (low half) and (tig & 1) + 2 (high half)
+          const float c0 = __ldg(corr + (int64_t)(tig & 1) * T + qi);
+          const float c1 = __ldg(corr + (int64_t)((tig & 1) + 2) * T + qi);
+          const float2 lo = unpack_bf16(rec.y), pw = unpack_bf16(rec.z);
+          bkl[hb] = pack_bf16(fmaf(pw.x, c0, lo.x), fmaf(pw.y, c1, lo.y));
+        }
       } else {
         bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
       }
@@ -428,14 +459,16 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     }
     const uint32_t qst = sbase + st * kKvStageB;
     const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
+    // MULTI: query-head group gt / NG; its delta - psi rows for the correction
+    const float* corr = MULTI ? a.dcorr + (int64_t)hplane_of(gt / NG) * T : nullptr;
     if (grp < nwc) {
       const int s_lo = kKvWC * grp;
-      kv_group<4>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0,
-                  qb_of(grp) + 8 * kw, kKvQ, 8 * kw, j, T, dh, dk, dv);
+      kv_group<4, MULTI>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0,
+                         qb_of(grp) + 8 * kw, kKvQ, 8 * kw, j, T, dh, corr, dk, dv);
     } else {
       const int qoff = min(8 * kw, kKvQR - 12);
-      kv_group<3>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qb_of(grp) + qoff,
-                  kKvQR, qoff, j, T, dh, dk, dv);
+      kv_group<3, MULTI>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qb_of(grp) + qoff,
+                         kKvQR, qoff, j, T, dh, corr, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
@@ -501,9 +534,14 @@ __global__ void __launch_bounds__(kKvThreads, 2)
 }
 
 size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
-                                   size_t* off_coef) {
+                                   size_t* off_coef, size_t* off_corr) {
   const size_t nparts = (size_t)((d->T + kTcTQ - 1) / kTcTQ) * d->B * (d->Hq / 4);
   size_t o = align256(nparts * sizeof(double));  // per-CTA dL/dalpha partials
+  *off_corr = 0;
+  if (d->Hq / d->Hkv > 4) {  // delta - psi per query row, for the key side's correction
+    *off_corr = o;
+    o += align256((size_t)d->B * d->Hq * d->T * sizeof(float));
+  }
   *off_kr = o;
   o += kr_bytes(d);
   *off_qt = o;
@@ -537,7 +575,9 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
       make_coef_map(&mcr, coef, qplanes / 4, a.T, NS, 2, kKvQR) != SFA_OK)
     return SFA_ERR_CUDA;
-  auto kq = p.interp ? bwd_q_tc_kernel<true> : bwd_q_tc_kernel<false>;
+  const bool psi = a.dcorr != nullptr;
+  auto kq = p.interp ? (psi ? bwd_q_tc_kernel<true, true> : bwd_q_tc_kernel<true, false>)
+                     : (psi ? bwd_q_tc_kernel<false, true> : bwd_q_tc_kernel<false, false>);
   const bool multi = a.lgG > 2;
   auto kkv = p.interp ? (multi ? bwd_kv_tc_kernel<true, true> : bwd_kv_tc_kernel<true, false>)
                       : (multi ? bwd_kv_tc_kernel<false, true> : bwd_kv_tc_kernel<false, false>);

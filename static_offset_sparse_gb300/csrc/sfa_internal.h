@@ -59,6 +59,7 @@ struct AttnArgs {
   void* dv;
   float* delta;        // workspace [B, Hq, T]
   double* dalpha_part; // workspace, one per backward key-side CTA
+  float* dcorr;        // rung backward, G > 4: delta - sum_j P dP per query row (workspace [B, Hq, T])
   double* dalpha_out;  // device [2]: dL/dalpha, dL/dtheta (or nullptr)
   double alpha;
   const int32_t* pos;  // decode: device [B] query positions
@@ -89,7 +90,7 @@ inline size_t kr_bytes(const sfa_desc* d) {
 int launch_rope_prep(const void* k, const void* rope, void* kr, int64_t rows, int T, void* stream);
 int launch_forward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* stream);
 size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off_kr, size_t* off_qt,
-                                   size_t* off_coef);
+                                   size_t* off_coef, size_t* off_corr);
 int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* qt, void* coef,
                        void* stream);
 int launch_forward(const AttnArgs& a, const Plan& p, int dtype, void* stream);

@@ -243,8 +243,9 @@ __device__ __forceinline__ void tc_store_tile(const CUtensorMap* map, uint32_t t
 }
 
 // Host: tensor map over [B*H, T, 64] bf16 rows with a (64, box_rows, box_h)
-// box and 128B swizzle (sfa_api.cu).
-int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h);
+// box, 128B swizzle unless swizzle is false (sfa_api.cu).
+int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int box_rows, int box_h,
+                  bool swizzle = true);
 // Host: tensor map over [planes, T, 64] bf16 rows viewed as [planes][T /
 // delta][delta][64] (delta divides T): coordinates (dim, residue class,
 // compressed index, plane), box (64, 1, box_rows, box_planes), 128B swizzle.
