@@ -57,13 +57,14 @@ int make_band_map(CUtensorMap* m, const void* base, int64_t planes, int T, int d
              : SFA_ERR_CUDA;
 }
 
-int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int box_slots,
-                  int box_q) {
+int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int words,
+                  int box_slots, int box_q) {
   auto fn = encode_fn();
   if (!fn) return SFA_ERR_CUDA;
-  const cuuint64_t dims[4] = {8, (cuuint64_t)NS, (cuuint64_t)T, (cuuint64_t)planes};
-  const cuuint64_t strides[3] = {32, (cuuint64_t)NS * 32, (cuuint64_t)T * NS * 32};
-  const cuuint32_t box[4] = {8, (cuuint32_t)box_slots, (cuuint32_t)box_q, 1};
+  const cuuint64_t rb = (cuuint64_t)words * 4;  // record bytes
+  const cuuint64_t dims[4] = {(cuuint64_t)words, (cuuint64_t)NS, (cuuint64_t)T, (cuuint64_t)planes};
+  const cuuint64_t strides[3] = {rb, (cuuint64_t)NS * rb, (cuuint64_t)T * NS * rb};
+  const cuuint32_t box[4] = {(cuuint32_t)words, (cuuint32_t)box_slots, (cuuint32_t)box_q, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -21,16 +21,27 @@
 //   warp: no atomics.
 #include <math.h>
 
+#include <type_traits>
+
 #include "sfa_tc.cuh"
 
 namespace sfa {
 
-// One 32-byte record of key-side coefficients for a (query, slot) is two
-// 16-byte halves, one per head pair (0, 2) and (1, 3): the pair's wt * dS and
-// wt * P as bf16 hi + lo (hi = bf16(x), lo = bf16(x - hi)), each word
-// holding the pair's two heads (lower head in the low half).  Words:
-// dS hi, dS lo, P hi, P lo.  The lane whose fragment rows are the pair's two
-// heads writes its half directly.
+// A record of key-side coefficients for a (query, slot) is two halves, one
+// per head pair (0, 2) and (1, 3), each word holding the pair's two heads
+// (lower head in the low half).  With G = 4 a half is 8 bytes, the pair's
+// wt * dS and wt * P in bf16 (words: dS, P).  With G > 4 (LO) a key sums G
+// heads' coefficients, and a half is 16 bytes, both as bf16 hi + lo
+// (hi = bf16(x), lo = bf16(x - hi); words: dS hi, dS lo, P hi, P lo).  The
+// lane whose fragment rows are the pair's two heads writes its half
+// directly.
+template <bool LO>
+struct CoefFmt {
+  using Half = typename std::conditional<LO, uint4, uint2>::type;
+  static constexpr int kHalfWords = LO ? 4 : 2;
+  static constexpr int kRecWords = 2 * kHalfWords;
+  static constexpr int kRecBytes = 4 * kRecWords;
+};
 __device__ __forceinline__ void write_coef_half(uint4* dst, float wt, float ds0, float ds1, float p0,
                                                 float p1) {
   const float a0 = wt * ds0, a1 = wt * ds1, b0 = wt * p0, b1 = wt * p1;
@@ -38,16 +49,20 @@ __device__ __forceinline__ void write_coef_half(uint4* dst, float wt, float ds0,
   const float2 dhf = unpack_bf16(dh), phf = unpack_bf16(ph);
   *dst = make_uint4(dh, pack_bf16(a0 - dhf.x, a1 - dhf.y), ph, pack_bf16(b0 - phf.x, b1 - phf.y));
 }
+__device__ __forceinline__ void write_coef_half(uint2* dst, float wt, float ds0, float ds1, float p0,
+                                                float p1) {
+  *dst = make_uint2(pack_bf16(wt * ds0, wt * ds1), pack_bf16(wt * p0, wt * p1));
+}
 
 // PSI (G > 4): also sum psi = sum_j P_ij dP_ij per row and write delta - psi
-// for the key side's correction (a.dcorr).
+// for the key side's correction (a.dcorr); records carry hi + lo words.
 template <bool INTERP, bool PSI>
 __global__ void __launch_bounds__(kTcThreads, 4)
     bwd_q_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mdo, const __grid_constant__ CUtensorMap mo,
                     const __grid_constant__ CUtensorMap mqt,
-                    const __grid_constant__ CUtensorMap mdq, uint4* coef, int NS,
+                    const __grid_constant__ CUtensorMap mdq, uint32_t* coef, int NS,
                     const __grid_constant__ Plan P) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t bars[kTcStages + 1];
@@ -130,9 +145,10 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   // psi = sum_j P_ij dP_ij per row (this lane's keys), equal to dO . O for the
   // exact O: the key side of G > 4 corrects its dS by P (delta - psi)
   float psi[2] = {0.0f, 0.0f};
-  // records of query i: [slot][2 x uint4]; this lane's rows gid, gid + 8 are
+  // records of query i: [slot][2 halves]; this lane's rows gid, gid + 8 are
   // heads hA, hA + 2 of position p, i.e. half gid >> 2 of each record
-  uint4* crow = coef + ((int64_t)qy * T + ic) * NS * 2 + (gid >> 2);
+  using Half = typename CoefFmt<PSI>::Half;
+  Half* crow = reinterpret_cast<Half*>(coef) + ((int64_t)qy * T + ic) * NS * 2 + (gid >> 2);
 
   const int colrow = 4 * warp + ((lane & 7) >> 1) + (lane & 1);
   const int colrow2 = 4 * warp + ((((lane & 7) >> 1) + 2) & 3) + (lane & 1);
@@ -293,19 +309,19 @@ constexpr int kKvQ = kKvTK + 10;
 constexpr int kKvQR = kKvTK + 2;
 constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
 constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][42 queries][128 B]
-constexpr int kKvCoefB = kKvQ * kKvWC * 32;   // records box: [42 queries][9 slots][32 B]
+// records box: [42 queries][9 slots][16 or 32 B] (at most 12 KB)
 constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
 constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 
 // One group's products for a warp: NKS k-steps of 16 (query, head) pairs.
 // dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
-// FOLD (G > 4): corr points at delta - psi of the group's 4 query heads
-// ([4][T], written by the query side), and each dS coefficient becomes
-// wt dS + (wt P)(delta - psi) = wt P (dP - psi): the dS of the exact
-// delta = sum_j P_ij dP_ij instead of dO . O from the bf16-rounded O, whose
-// error the key side would otherwise sum over G heads.  The correction is
-// folded into the lo word.
+// FOLD (G > 4): records carry hi + lo words; corr points at delta - psi of
+// the group's 4 query heads ([4][T], written by the query side), and each dS
+// coefficient becomes wt dS + (wt P)(delta - psi) = wt P (dP - psi): the dS of
+// the exact delta = sum_j P_ij dP_ij instead of dO . O from the bf16-rounded
+// O, whose error the key side would otherwise sum over G heads.  The
+// correction is folded into the lo word.
 template <int NKS, bool FOLD>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int nsl,
                                          bool win, int s_lo, int s_hi, int c, int qw, int kq,
@@ -318,7 +334,8 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
     // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
     // (q - j = c - 1).  Within a query the k order of the heads is 0, 2, 1, 3,
     // so the pair of lane tig is record half tig & 1 (heads tig & 1 and
-    // (tig & 1) + 2): words dS hi, dS lo, P hi, P lo
+    // (tig & 1) + 2): words dS, P, or with FOLD dS hi, dS lo, P hi, P lo
+    using Fmt = CoefFmt<FOLD>;
     uint32_t bk[2], bvv[2], bkl[2], bvl[2];
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
@@ -333,7 +350,14 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
         else if (qi - j == c - 1) sl = 1;
       }
       if (sl >= 0 && qi < T && j < T) {
-        const uint4 rec = *reinterpret_cast<const uint4*>(csm + ((qoff + ql) * nsl + sl) * 8 + 4 * (tig & 1));
+        const uint32_t* half = csm + ((qoff + ql) * nsl + sl) * Fmt::kRecWords + Fmt::kHalfWords * (tig & 1);
+        uint4 rec;
+        if (FOLD) {
+          rec = *reinterpret_cast<const uint4*>(half);
+        } else {
+          const uint2 r2 = *reinterpret_cast<const uint2*>(half);
+          rec = make_uint4(r2.x, 0u, r2.y, 0u);
+        }
         bk[hb] = rec.x;
         bkl[hb] = rec.y;
         bvv[hb] = rec.z;
@@ -362,8 +386,10 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
       ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
       mma_bf16(dk[x], aq, bk[0], bk[1]);
       mma_bf16(dv[x], ad, bvv[0], bvv[1]);
-      mma_bf16(dk[x], aq, bkl[0], bkl[1]);
-      mma_bf16(dv[x], ad, bvl[0], bvl[1]);
+      if (FOLD) {
+        mma_bf16(dk[x], aq, bkl[0], bkl[1]);
+        mma_bf16(dv[x], ad, bvl[0], bvl[1]);
+      }
     }
   }
 }
@@ -412,12 +438,12 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     const bool win = grp < nwc;
     const int qb = qb_of(grp);
     if (win) {
-      mbar_expect_tx(bar, 2 * kKvPlaneB + kKvCoefB);
+      mbar_expect_tx(bar, 2 * kKvPlaneB + kKvQ * kKvWC * CoefFmt<MULTI>::kRecBytes);
       tma_load_3d(st, &mq, 0, qb, hplane, bar);
       tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
       tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, rp, bar);
     } else {
-      mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * 32);
+      mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * CoefFmt<MULTI>::kRecBytes);
       tma_load_3d(st, &mqr, 0, qb, hplane, bar);
       tma_load_3d(st + kKvPlaneB, &mdr, 0, qb, hplane, bar);
       tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, rp, bar);
@@ -548,7 +574,8 @@ size_t backward_tc_workspace_bytes(const sfa_desc* d, const Plan& p, size_t* off
   o += align256((size_t)d->B * d->Hq * d->T * kD * 2);
   *off_coef = o;
   const size_t NS = (size_t)p.W + 1 + 2 * p.n;  // records per query: window slots, 2 per rung
-  o += align256((size_t)d->B * (d->Hq / 4) * d->T * NS * 32);  // one plane per group of 4 heads
+  const size_t rec_bytes = d->Hq / d->Hkv > 4 ? CoefFmt<true>::kRecBytes : CoefFmt<false>::kRecBytes;
+  o += align256((size_t)d->B * (d->Hq / 4) * d->T * NS * rec_bytes);  // one plane per group of 4 heads
   return o;
 }
 
@@ -560,6 +587,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   // query side: Q / dO / O tile loads (20-row boxes), q~ and dQ tile stores
   // (16-row boxes); key side: q~ and dO slabs (42 rows for a window chunk,
   // 34 for a rung) and the record boxes
+  const int rec_words = a.lgG > 2 ? CoefFmt<true>::kRecWords : CoefFmt<false>::kRecWords;
   CUtensorMap mk, mv, mq, md, mqr, mdr, mcw, mcr, tq, tdo, to, sqt, sdq;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
@@ -572,8 +600,8 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
       make_rows_map(&mqr, qt, qplanes, a.T, kKvQR, 4) != SFA_OK ||
       make_rows_map(&mdr, a.dO, qplanes, a.T, kKvQR, 4) != SFA_OK ||
-      make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, kKvWC, kKvQ) != SFA_OK ||
-      make_coef_map(&mcr, coef, qplanes / 4, a.T, NS, 2, kKvQR) != SFA_OK)
+      make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, rec_words, kKvWC, kKvQ) != SFA_OK ||
+      make_coef_map(&mcr, coef, qplanes / 4, a.T, NS, rec_words, 2, kKvQR) != SFA_OK)
     return SFA_ERR_CUDA;
   const bool psi = a.dcorr != nullptr;
   auto kq = p.interp ? (psi ? bwd_q_tc_kernel<true, true> : bwd_q_tc_kernel<true, false>)
@@ -590,7 +618,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   {
     LaunchTimer tm(SFA_KERNEL_BWD_Q, stream);
     if (launch_pdl(kq, gq, dim3(kTcThreads), kBwdQTcSmem, s, a, mk, mv, tq, tdo, to, sqt, sdq,
-                   static_cast<uint4*>(coef), NS, p) != cudaSuccess)
+                   static_cast<uint32_t*>(coef), NS, p) != cudaSuccess)
       return SFA_ERR_CUDA;
   }
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));

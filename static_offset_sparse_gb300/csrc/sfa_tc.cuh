@@ -251,9 +251,9 @@ int make_rows_map(CUtensorMap* m, const void* base, int64_t planes, int T, int b
 // compressed index, plane), box (64, 1, box_rows, box_planes), 128B swizzle.
 int make_band_map(CUtensorMap* m, const void* base, int64_t planes, int T, int delta, int box_rows,
                   int box_planes);
-// Host: tensor map over the key-side coefficient records [B*Hkv, T, NS, 8
-// words], box (8, box_slots, box_q, 1), no swizzle.
-int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int box_slots,
-                  int box_q);
+// Host: tensor map over the key-side coefficient records [planes, T, NS,
+// words] (uint32 words), box (words, box_slots, box_q, 1), no swizzle.
+int make_coef_map(CUtensorMap* m, const void* base, int64_t planes, int T, int NS, int words,
+                  int box_slots, int box_q);
 
 }  // namespace sfa
