@@ -314,62 +314,62 @@ constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
 constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
 
+// Bits m of the query offsets ql = m + t1 (t1 = tig >> 1) with lo <= ql <= hi.
+__device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
+  lo = max(lo - t1, 0);
+  hi = min(hi - t1, 31);
+  return lo > hi ? 0u : (0xffffffffu >> (31 - hi)) & (0xffffffffu << lo);
+}
+
 // One group's products for a warp: NKS k-steps of 16 (query, head) pairs.
 // dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
+//
+// B: the records of the (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
+// reach the lane's key j.  Within a query the k order of the heads is 0, 2,
+// 1, 3, so the pair of lane tig is record half tig & 1 (heads tig & 1 and
+// (tig & 1) + 2), and k-step ks, half hb reads query offset
+// ql = 4 ks + 2 hb + (tig >> 1) from qw.  Which slot of that query reaches
+// key j depends only on ql - (j - qw): bit m = ql - (tig >> 1) of `mask` says
+// whether it is a slot of this group at all (and inside the sequence), and
+// its record half sits at word rec + m * STEP of the staged records.
+//
 // FOLD (G > 4): records carry hi + lo words; corr points at delta - psi of
 // the group's 4 query heads ([4][T], written by the query side), and each dS
 // coefficient becomes wt dS + (wt P)(delta - psi) = wt P (dP - psi): the dS of
 // the exact delta = sum_j P_ij dP_ij instead of dO . O from the bf16-rounded
 // O, whose error the key side would otherwise sum over G heads.  The
 // correction is folded into the lo word.
-template <int NKS, bool FOLD>
-__device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int nsl,
-                                         bool win, int s_lo, int s_hi, int c, int qw, int kq,
-                                         int qoff, int j, int T, int dh, const float* corr,
-                                         float (*dk)[4], float (*dv)[4]) {
+template <int NKS, int STEP, bool FOLD>
+__device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int rec,
+                                         uint32_t mask, int qw, int kq, int qoff, int T, int dh,
+                                         const float* corr, float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
+  using Fmt = CoefFmt<FOLD>;
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
-    // B: the records of (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
-    // reach key j: window slot s = q - j, or rung role 0 (q - j = c) / 1
-    // (q - j = c - 1).  Within a query the k order of the heads is 0, 2, 1, 3,
-    // so the pair of lane tig is record half tig & 1 (heads tig & 1 and
-    // (tig & 1) + 2): words dS, P, or with FOLD dS hi, dS lo, P hi, P lo
-    using Fmt = CoefFmt<FOLD>;
     uint32_t bk[2], bvv[2], bkl[2], bvl[2];
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
-      const int ql = 4 * ks + 2 * hb + (tig >> 1);  // query offset from qw
-      const int qi = qw + ql;
-      int sl = -1;
-      if (win) {
-        const int s = qi - j;
-        if (s >= s_lo && s <= s_hi) sl = s - s_lo;
-      } else if (qi >= c) {
-        if (qi - j == c) sl = 0;
-        else if (qi - j == c - 1) sl = 1;
-      }
-      if (sl >= 0 && qi < T && j < T) {
-        const uint32_t* half = csm + ((qoff + ql) * nsl + sl) * Fmt::kRecWords + Fmt::kHalfWords * (tig & 1);
-        uint4 rec;
-        if (FOLD) {
-          rec = *reinterpret_cast<const uint4*>(half);
-        } else {
-          const uint2 r2 = *reinterpret_cast<const uint2*>(half);
-          rec = make_uint4(r2.x, 0u, r2.y, 0u);
-        }
-        bk[hb] = rec.x;
-        bkl[hb] = rec.y;
-        bvv[hb] = rec.z;
-        bvl[hb] = rec.w;
-        if (FOLD) {  // heads tig & 1 (low half) and (tig & 1) + 2 (high half)
+      const int m = 4 * ks + 2 * hb;
+      bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
+      if ((mask >> m) & 1u) {
+        const uint32_t* half = csm + rec + m * STEP;
+        if (FOLD) {  // words dS hi, dS lo, P hi, P lo
+          const uint4 r4 = *reinterpret_cast<const uint4*>(half);
+          const int qi = qw + m + (tig >> 1);
+          // heads tig & 1 (low half) and (tig & 1) + 2 (high half)
           const float c0 = __ldg(corr + (int64_t)(tig & 1) * T + qi);
           const float c1 = __ldg(corr + (int64_t)((tig & 1) + 2) * T + qi);
-          const float2 lo = unpack_bf16(rec.y), pw = unpack_bf16(rec.z);
+          const float2 lo = unpack_bf16(r4.y), pw = unpack_bf16(r4.z);
+          bk[hb] = r4.x;
           bkl[hb] = pack_bf16(fmaf(pw.x, c0, lo.x), fmaf(pw.y, c1, lo.y));
+          bvv[hb] = r4.z;
+          bvl[hb] = r4.w;
+        } else {  // words dS, P
+          const uint2 r2 = *reinterpret_cast<const uint2*>(half);
+          bk[hb] = r2.x;
+          bvv[hb] = r2.y;
         }
-      } else {
-        bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
       }
     }
     // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
@@ -487,14 +487,28 @@ __global__ void __launch_bounds__(kKvThreads, 2)
     const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
     // MULTI: query-head group gt / NG; its delta - psi rows for the correction
     const float* corr = MULTI ? a.dcorr + (int64_t)hplane_of(gt / NG) * T : nullptr;
+    constexpr int RW = CoefFmt<MULTI>::kRecWords, HW = CoefFmt<MULTI>::kHalfWords;
+    const int t1 = tig >> 1;
     if (grp < nwc) {
-      const int s_lo = kKvWC * grp;
-      kv_group<4, MULTI>(qst, qst + kKvPlaneB, csm, kKvWC, true, s_lo, min(s_lo + kKvWC - 1, P.W), 0,
-                         qb_of(grp) + 8 * kw, kKvQ, 8 * kw, j, T, dh, corr, dk, dv);
+      // window chunk: query qw + ql reaches key j through slot s = ql + rel of
+      // the chunk (s in 0 .. s_hi - s_lo), record (qoff + ql) * 9 + s
+      const int s_lo = kKvWC * grp, qw = qb_of(grp) + 8 * kw, rel = qw - j - s_lo;
+      const uint32_t mask =
+          j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + kKvWC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
+      const int rec = (8 * kw * kKvWC + rel) * RW + HW * (tig & 1) + t1 * (kKvWC + 1) * RW;
+      kv_group<4, (kKvWC + 1) * RW, MULTI>(qst, qst + kKvPlaneB, csm, rec, mask, qw, kKvQ, 8 * kw, T,
+                                           dh, corr, dk, dv);
     } else {
-      const int qoff = min(8 * kw, kKvQR - 12);
-      kv_group<3, MULTI>(qst, qst + kKvPlaneB, csm, 2, false, 0, 0, P.c[grp - nwc], qb_of(grp) + qoff,
-                         kKvQR, qoff, j, T, dh, corr, dk, dv);
+      // rung: query qw + ql reaches key j as role 1 (key i - c + 1) when
+      // ql + rel = 0 and as role 0 (key i - c) when ql + rel = 1, and only if
+      // it reads the rung at all (qw + ql >= c); record (qoff + ql) * 2 + role
+      const int c = P.c[grp - nwc], qoff = min(8 * kw, kKvQR - 12), qw = qb_of(grp) + qoff;
+      const int rel = qw - j - c + 1;
+      const uint32_t mask =
+          j < T ? ql_mask(max(-rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
+      const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
+      kv_group<3, RW, MULTI>(qst, qst + kKvPlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh, corr, dk,
+                             dv);
     }
     __syncthreads();
     if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
