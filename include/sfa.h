@@ -306,6 +306,17 @@ int sfa_timing_read(double* ms, int64_t* launches, int n);
  * last call, SFA_OK if none) and clear it. */
 int sfa_get_device_status(void* stream, int32_t* out);
 
+/* Kernel selection options (process-wide; read by every later call).
+ * SFA_OPT_BAND_FWD_TC05: the band forward (integer sets with a band plan,
+ * bf16) runs on the fifth-generation tensor cores with TMEM accumulators and
+ * 128 query rows per CTA (1) or on the mma.sync kernel with 64 rows per CTA
+ * (0, the default: faster on the Christoffel configuration, 42 against 56 us
+ * per call on a GB300).  Both compute the same keys and are checked against
+ * the same bounds; the option exists to compare them.  Returns
+ * SFA_ERR_INVALID_ARG for an unknown option or value. */
+typedef enum { SFA_OPT_BAND_FWD_TC05 = 0 } sfa_option;
+int sfa_set_option(int32_t option, int32_t value);
+
 /* Test injection for the bounded waits (no counterpart on the pages; for
  * tests of the failure path only).  Every mbarrier wait of the TMA-staged
  * kernels gives up after `wait_cycles` SM clock cycles (0 restores the

@@ -82,6 +82,7 @@ def _lib():
                 "sfa_offsets_powerlaw": [C.POINTER(C.c_double), C.c_int32, C.c_double, C.c_int32,
                                          _I32P, C.c_int32, _I32P],
                 "sfa_debug_inject": [C.c_int64, C.c_int32],
+                "sfa_set_option": [C.c_int32, C.c_int32],
                 "sfa_timing_enable": [C.c_int],
                 "sfa_timing_read": [C.POINTER(C.c_double), C.POINTER(C.c_int64), C.c_int],
             }

@@ -150,6 +150,8 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 static std::mutex g_dbg_mu;
 static long long g_dbg_wait = 0;  // 0: kDefaultWaitCycles
 static int g_dbg_skip = -1;
+// sfa_set_option values
+static int g_opt_band_tc05 = 0;
 
 static int fill_args(const sfa_desc* d, AttnArgs* a) {
   *a = AttnArgs{};
@@ -164,6 +166,7 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
     std::lock_guard<std::mutex> lock(g_dbg_mu);
     a->wait_cycles = g_dbg_wait > 0 ? g_dbg_wait : kDefaultWaitCycles;
     a->debug_skip = g_dbg_skip;
+    a->band_tc05 = g_opt_band_tc05;
   }
   if (d->rope && !aligned16(d->rope)) return SFA_ERR_INVALID_ARG;
   if (d->k_rot && !aligned16(d->k_rot)) return SFA_ERR_INVALID_ARG;
@@ -386,6 +389,18 @@ int sfa_debug_inject(int64_t wait_cycles, int32_t skip_group) {
   g_dbg_wait = wait_cycles;
   g_dbg_skip = skip_group;
   return SFA_OK;
+}
+
+int sfa_set_option(int32_t option, int32_t value) {
+  std::lock_guard<std::mutex> lock(g_dbg_mu);
+  switch (option) {
+    case SFA_OPT_BAND_FWD_TC05:
+      if (value != 0 && value != 1) return SFA_ERR_INVALID_ARG;
+      g_opt_band_tc05 = value;
+      return SFA_OK;
+    default:
+      return SFA_ERR_INVALID_ARG;
+  }
 }
 
 int sfa_timing_enable(int on) {

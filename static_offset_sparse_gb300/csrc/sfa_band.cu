@@ -31,6 +31,7 @@
 #include <math.h>
 
 #include "sfa_tc.cuh"
+#include "sfa_umma.cuh"
 
 namespace sfa {
 
@@ -890,10 +891,315 @@ __global__ void __launch_bounds__(kBThreads, 3)
   }
 }
 
+// ---- forward on the fifth-generation tensor cores (tcgen05, TMEM) -------------
+//
+// The same band walk with 128 query rows per CTA (G heads x 128 / G
+// positions), one row per thread, and both products issued by one thread as
+// tcgen05.mma with the accumulators in tensor memory:
+//  * S = q~ . K'^T (M = 128, N = 64 keys, K = 64): A is the CTA's query tile,
+//    rotated and scaled in shared memory once, B the staged K' tile (both
+//    K-major, 128B swizzle as the TMA unit writes them); S lands in TMEM
+//    columns 0..63.
+//  * Each thread reads its row of S (tcgen05.ld), masks it to its band,
+//    takes the online-softmax step in base 2 (the running maximum refreshed
+//    only when the row's maximum exceeds it by more than 8, as in the mma.sync
+//    forward), and writes its row of P in bf16 to a shared-memory tile (K-major,
+//    128B swizzle).  A refresh rescales the warp's rows of O in TMEM (ld,
+//    scale, st: warp-collective instructions, so every lane of the warp takes
+//    part, the rows without a refresh scaled by 1).
+//  * O += P . V (M = 128, N = 64 dims, K = 64 keys): B is the staged V tile,
+//    MN-major; O stays in TMEM columns 64..127 until the epilogue.
+// Two K'/V stages (three CTAs per SM: 65 KB of shared memory and 128 TMEM
+// columns each); a stage is refilled once the P . V product that last read it
+// has completed.  All waits are bounded.
+
+constexpr int kUR = 128;                 // query rows per CTA: the TMEM lanes of M = 128
+constexpr int kUStages = 2;
+constexpr int kUTileB = kUR * 128;       // 16 KB: the query (then output) tile, the P tile
+constexpr size_t kBandFwdTc05Smem = (size_t)2 * kUTileB + (size_t)kUStages * kBStageB + 1024;
+constexpr uint32_t kUColS = 0, kUColO = 64, kUCols = 128;
+
+template <int G>
+__global__ void __launch_bounds__(kBThreads, 3)
+    band_fwd_tc05_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
+                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
+                         const __grid_constant__ CUtensorMap mo, const __grid_constant__ BandPlan P) {
+  constexpr int BU = kUR / G;  // positions per head in the tile
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[kUStages + 3];  // stages, query tile, S done, P.V done
+  __shared__ uint32_t tmem_base;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  const uint32_t qtile = sbase, ptile = sbase + kUTileB, stages = sbase + 2 * kUTileB;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint64_t* const qbar = &bars[kUStages];
+  uint64_t* const sbar = &bars[kUStages + 1];
+  uint64_t* const pvbar = &bars[kUStages + 2];
+
+  // tile geometry: class r, compressed positions u0 .. ul; this thread's row
+  const int delta = P.delta, Uc = a.T / delta, nqt = (Uc + BU - 1) / BU;
+  const int r = blockIdx.x / nqt, u0 = (blockIdx.x - r * nqt) * BU, ul = min(u0 + BU - 1, Uc - 1);
+  const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv, qplane = b * a.Hq + g * G;
+  const int hrow = tid / BU, urow = u0 + tid % BU;
+  const bool live = urow < Uc;
+  const int pos = r + delta * min(urow, Uc - 1);
+  int NT = 0;
+  {
+    QWalk w{0, 0, 0, 0, 0};
+    if (qwalk_seek(P, r, u0, ul, w)) do ++NT; while (qwalk_next(P, r, u0, ul, w));
+  }
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int x = 0; x < kUStages + 3; ++x) mbar_init(smem_u32(&bars[x]), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), kUCols);
+    tmem_relinquish();
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  const uint32_t tm = tmem_base;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lanes
+  pdl_wait();  // the previous kernel's outputs are complete from here on
+
+  QWalk iw{0, 0, 0, 0, 0};
+  // thread 0's bookkeeping for a clean exit after a timeout: tiles issued and
+  // consumed, and the last S and P . V products committed (-1: none)
+  int n_issued = 0, n_consumed = 0, last_s = -1, last_pv = -1;
+  auto issue = [&](int st) {
+    const uint32_t sa = stages + st * kBStageB, bar = smem_u32(&bars[st]);
+    mbar_expect_tx(bar, kBStageB);
+    tma_load_4d(sa, &mk, 0, iw.rho, iw.vs, bg, bar);
+    tma_load_4d(sa + kBTileB, &mv, 0, iw.rho, iw.vs, bg, bar);
+    qwalk_next(P, r, u0, ul, iw);
+    ++n_issued;
+  };
+  if (tid == 0) {
+    mbar_expect_tx(smem_u32(qbar), kUTileB);
+    tma_load_4d(qtile, &mq, 0, r, u0, qplane, smem_u32(qbar));
+    qwalk_seek(P, r, u0, ul, iw);
+    for (int st = 0; st < kUStages && st < NT; ++st) issue(st);
+  }
+  bool ok = true;
+  // the query row: RoPE at its position, times 1/8, rounded to bf16 in place
+  // (the rounding the backward uses for q~)
+  const float2* rope = static_cast<const float2*>(a.rope);
+  ok = mbar_wait_bounded(smem_u32(qbar), 0, a.wait_cycles);
+  if (ok) {
+    unsigned char* row = sgen + (size_t)tid * 128;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+      uint4* plo = reinterpret_cast<uint4*>(row + ((ch ^ (tid & 7)) << 4));
+      uint4* phi = reinterpret_cast<uint4*>(row + (((ch + 4) ^ (tid & 7)) << 4));
+      uint4 lo = *plo, hi = *phi;
+      uint32_t* l4 = reinterpret_cast<uint32_t*>(&lo);
+      uint32_t* h4 = reinterpret_cast<uint32_t*>(&hi);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 x = unpack_bf16(l4[e]), y = unpack_bf16(h4[e]);
+        if (rope) {
+          const float4 cs = __ldg(reinterpret_cast<const float4*>(rope + (int64_t)pos * 32 + 8 * ch + 2 * e));
+          const float x0 = x.x * cs.x - y.x * cs.y, y0 = x.x * cs.y + y.x * cs.x;
+          const float x1 = x.y * cs.z - y.y * cs.w, y1 = x.y * cs.w + y.y * cs.z;
+          x = make_float2(x0, x1);
+          y = make_float2(y0, y1);
+        }
+        l4[e] = pack_bf16(x.x * 0.125f, x.y * 0.125f);
+        h4[e] = pack_bf16(y.x * 0.125f, y.y * 0.125f);
+      }
+      *plo = lo;
+      *phi = hi;
+    }
+  }
+  fence_async_smem();
+  tc05_fence_before();
+  ok = !__syncthreads_or(!ok);
+  tc05_fence_after();
+
+  constexpr uint32_t idS = idesc_bf16(kUR, 64, false, false);
+  constexpr uint32_t idPV = idesc_bf16(kUR, 64, false, true);
+  float m = -INFINITY, l = 0.0f;
+  QWalk cw{0, 0, 0, 0, 0};
+  qwalk_seek(P, r, u0, ul, cw);
+  // S_t = q~ . K'_t^T into TMEM columns 0..63 (thread 0).  S_{t+1} is issued
+  // right after P_t . V_t: every thread holds S_t in registers by then, and
+  // the tensor cores run both products while the threads go on.
+  auto issue_s = [&](int t) {
+    const int st = t % kUStages;
+    const uint32_t kst = stages + st * kBStageB;
+    if (!mbar_wait_bounded(smem_u32(&bars[st]), (t / kUStages) & 1, a.wait_cycles)) {
+      record_status(a.status, SFA_ERR_TIMEOUT);  // the S wait of every thread then runs out
+      return;
+    }
+    n_consumed = t + 1;
+    tc05_fence_after();
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      umma_bf16(tm + kUColS, smem_desc_sw128(qtile + 32 * k, 16, 1024),
+                smem_desc_sw128(kst + 32 * k, 16, 1024), idS, k > 0);
+    umma_commit(smem_u32(sbar));
+    last_s = t;
+  };
+  if (tid == 0 && ok && NT > 0) issue_s(0);
+  for (int t = 0; t < NT && ok; ++t) {
+    const uint32_t vst = stages + (t % kUStages) * kBStageB + kBTileB;
+    bool okw = mbar_wait_bounded(smem_u32(sbar), t & 1, a.wait_cycles);
+    tc05_fence_after();
+    // this row's keys in the tile: columns lo .. hi of the current run; a
+    // 16-column chunk no row of the warp reads is neither loaded nor
+    // exponentiated (warp-uniform: the TMEM loads are warp-collective)
+    const int len = P.len[cw.m];
+    const int lo = urow + cw.e - len + 1 - cw.vs, hi = live ? urow + cw.e - cw.vs : -1;
+    bool chunk[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) chunk[q] = __any_sync(0xffffffffu, lo <= 16 * q + 15 && hi >= 16 * q);
+    float sv[64];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (chunk[q]) tmem_ld16(tm + lane_base + kUColS + 16 * q, sv + 16 * q);
+    tmem_wait_ld();
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      sv[c] = (chunk[c >> 4] && c >= lo && c <= hi) ? sv[c] * kLog2e : -INFINITY;
+      mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+    }
+    const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    // the previous P . V has finished: O is stable and the P tile is free
+    if (t > 0) {
+      okw &= mbar_wait_bounded(smem_u32(pvbar), (t - 1) & 1, a.wait_cycles);
+      tc05_fence_after();
+      // its K'/V stage is free: refill it with tile t - 1 + kUStages
+      if (tid == 0 && t - 1 + kUStages < NT) issue((t - 1) % kUStages);
+    }
+    // refresh the running maximum (m = -inf: any valid logit); the TMEM
+    // moves are warp-collective, so a warp rescales its rows of O when any of
+    // them refreshes (by 1 for the others)
+    const bool refresh = mx > m + 8.0f;
+    float corr = 1.0f;
+    if (refresh) {
+      corr = ex2(m - mx);  // 0 while the row had no key
+      l *= corr;
+      m = mx;
+    }
+    if (t > 0 && __any_sync(0xffffffffu, refresh)) {
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float ov[16];
+        tmem_ld16(tm + lane_base + kUColO + c, ov);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ov[e] *= corr;
+        tmem_st16(tm + lane_base + kUColO + c, ov);
+      }
+      tmem_wait_st();
+    }
+    const float mm = m == -INFINITY ? 0.0f : m;
+    unsigned char* prow = sgen + kUTileB + (size_t)tid * 128;
+    float lt[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t w4[4] = {0u, 0u, 0u, 0u};
+      if (chunk[ch >> 1]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = ex2(sv[8 * ch + 2 * e] - mm), p1 = ex2(sv[8 * ch + 2 * e + 1] - mm);
+          lt[e & 1] += p0 + p1;
+          w4[e] = pack_bf16(p0, p1);
+        }
+      }
+      *reinterpret_cast<uint4*>(prow + ((ch ^ (tid & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    l += lt[0] + lt[1];
+    fence_async_smem();
+    tc05_fence_before();
+    ok = !__syncthreads_or(!okw);
+    if (!ok) {
+      if (tid == 0) record_status(a.status, SFA_ERR_TIMEOUT);
+      break;
+    }
+    // O += P . V into TMEM columns 64..127 (V MN-major: 16 keys = two 8-row
+    // groups), then S_{t+1}
+    if (tid == 0) {
+      tc05_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_bf16(tm + kUColO, smem_desc_sw128(ptile + 32 * k, 16, 1024),
+                  smem_desc_sw128(vst + 2048 * k, 8192, 1024), idPV, t > 0 || k > 0);
+      umma_commit(smem_u32(pvbar));
+      last_pv = t;
+      if (t + 1 < NT) issue_s(t + 1);
+    }
+    qwalk_next(P, r, u0, ul, cw);
+  }
+  if (ok && NT > 0) ok = mbar_wait_bounded(smem_u32(pvbar), (NT - 1) & 1, a.wait_cycles);
+  ok = !__syncthreads_or(!ok);
+  tc05_fence_after();
+  if (ok) {
+    // O = acc / l and LSE; the row goes out through the query tile's space
+    float ov[64];
+#pragma unroll
+    for (int c = 0; c < 64; c += 16) tmem_ld16(tm + lane_base + kUColO + c, ov + c);
+    tmem_wait_ld();
+    const float inv = NT > 0 ? 1.0f / l : 0.0f;
+    if (live)
+      a.out_lse[(int64_t)(qplane + hrow) * a.T + pos] = NT > 0 ? (m + log2f(l)) * kLn2 : -INFINITY;
+    unsigned char* orow = sgen + (size_t)tid * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w4[e] = pack_bf16(ov[8 * ch + 2 * e] * inv, ov[8 * ch + 2 * e + 1] * inv);
+      *reinterpret_cast<uint4*>(orow + ((ch ^ (tid & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    fence_async_smem();
+  } else if (tid == 0) {
+    record_status(a.status, SFA_ERR_TIMEOUT);
+    // wait (bounded) for the loads still in flight (at most one per stage) and
+    // the last products committed, before the TMEM and the CTA go away
+    for (int x = n_consumed; x < n_issued; ++x)
+      mbar_wait_bounded(smem_u32(&bars[x % kUStages]), (x / kUStages) & 1, a.wait_cycles);
+    if (last_s >= 0) mbar_wait_bounded(smem_u32(sbar), last_s & 1, a.wait_cycles);
+    if (last_pv >= 0) mbar_wait_bounded(smem_u32(pvbar), last_pv & 1, a.wait_cycles);
+  }
+  tc05_fence_before();
+  __syncthreads();
+  tc05_fence_after();
+  if (warp == 0) tmem_dealloc(tm, kUCols);
+  if (ok && tid == 0) {
+    tma_store_4d(&mo, 0, r, u0, qplane, qtile);
+    bulk_commit();
+    bulk_wait_read();
+  }
+}
+
 // ---- launchers ---------------------------------------------------------------
 
 template <int G>
 static int band_fwd_launch(const AttnArgs& a, const BandPlan& p, const void* kr, cudaStream_t s) {
+  if (a.band_tc05) {  // tcgen05 forward: 128 query rows per CTA
+    constexpr int BU = kUR / G;
+    CUtensorMap mk, mv, mq, mo;
+    const int64_t planes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
+    if (make_band_map(&mk, kr, planes, a.T, p.delta, kBR, 1) != SFA_OK ||
+        make_band_map(&mv, a.v, planes, a.T, p.delta, kBR, 1) != SFA_OK ||
+        make_band_map(&mq, a.q, qplanes, a.T, p.delta, BU, G) != SFA_OK ||
+        make_band_map(&mo, a.out_o, qplanes, a.T, p.delta, BU, G) != SFA_OK)
+      return SFA_ERR_CUDA;
+    if (cudaFuncSetAttribute(band_fwd_tc05_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kBandFwdTc05Smem) != cudaSuccess)
+      return SFA_ERR_CUDA;
+    const int Uc = a.T / p.delta;
+    dim3 grid((unsigned)(p.delta * ((Uc + BU - 1) / BU)), (unsigned)(a.B * a.Hkv));
+    LaunchTimer tm(SFA_KERNEL_FWD, s);
+    return launch_pdl(band_fwd_tc05_kernel<G>, grid, dim3(kBThreads), kBandFwdTc05Smem, s, a, mk, mv,
+                      mq, mo, p) == cudaSuccess
+               ? SFA_OK
+               : SFA_ERR_CUDA;
+  }
   constexpr int BU = kBR / G;
   CUtensorMap mk, mv, mq, mo;
   const int64_t planes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;

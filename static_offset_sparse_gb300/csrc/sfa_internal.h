@@ -67,6 +67,7 @@ struct AttnArgs {
   int* status;         // device status word
   long long wait_cycles;  // limit of every bounded mbarrier wait, in SM clock cycles
   int32_t debug_skip;     // test injection: group whose loads CTA (0, 0) never issues, or -1
+  int32_t band_tc05;      // band forward on tcgen05 (1) or mma.sync (0): sfa_set_option
 };
 
 // Default limit of a bounded mbarrier wait: ~1 s at the GB300's 2.07 GHz

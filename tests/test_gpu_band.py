@@ -255,3 +255,35 @@ def test_band_random_run_sets(sfa, case):
     _check("dQ", _f64(dq), gw["dq"])
     _check("dK", _f64(dk), gw["dk"])
     _check("dV", _f64(dv), gw["dv"])
+
+
+@pytest.mark.parametrize("name,shape", [("christoffel32_256", (1, 200, 2, 2)),
+                                        ("christoffel128_1024", (2, 2048, 4, 4)),
+                                        ("window64", (2, 456, 4, 2)),
+                                        ("window_stride4", (1, 1000, 8, 2)),
+                                        ("christoffel32_256", (1, 456, 8, 1))])
+def test_band_forward_both_kernels(sfa, sfa_lib, name, shape):
+    """The band forward on the fifth-generation tensor cores (tcgen05, TMEM
+    accumulators, 128 query rows per CTA) and on mma.sync (64 rows per CTA):
+    each against the oracle, and against each other."""
+    import torch
+
+    B, T, Hq, Hkv = shape
+    dist = SETS[name]
+    x = si.make_qkvdo(B, T, Hq, Hkv, 64, "bf16", seed=1700 + T + len(dist))
+    dev = {n: t.cuda() for n, t in x.items()}
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], o.dist_slots(dist), 1e4)
+    outs = {}
+    try:
+        for opt in (1, 0):
+            assert sfa_lib.sfa_set_option(0, opt) == 0
+            O, L = sfa.forward_int(dev["q"], dev["k"], dev["v"], dist=dist)
+            torch.cuda.synchronize()
+            assert sfa.get_device_status() == 0
+            _check(f"O (tcgen05={opt})", _f64(O), Ow)
+            assert np.abs(_f64(L) - Lw).max() <= 2e-2
+            outs[opt] = (_f64(O), _f64(L))
+    finally:
+        assert sfa_lib.sfa_set_option(0, 0) == 0  # the default
+    assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-4  # LSE: same keys, fp32 logits
+    assert np.abs(outs[0][0] - outs[1][0]).max() <= 2e-2
