@@ -18,9 +18,15 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsfa.so")
 
+DEBUG_LIB = os.path.join(PKG, "libsfa_debug.so")
+
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["sfa_host.cpp", "sfa_api.cu", "sfa_fwd.cu", "sfa_bwd.cu", "sfa_fwd_tc.cu", "sfa_bwd_tc.cu",
            "sfa_noalloc.cu", "sfa_decode.cu", "sfa_schedule.cpp", "sfa_band.cu"]
+# The bounds-checked build (libsfa_debug.so) recompiles the SIMT kernels with
+# SFA_DEBUG_BOUNDS: every row index they form is range-checked, a bad one is
+# recorded as SFA_ERR_DEVICE_BOUNDS and its access skipped.
+DEBUG_SOURCES = ["sfa_fwd.cu", "sfa_bwd.cu"]
 
 
 def _nvcc() -> str:
@@ -30,10 +36,12 @@ def _nvcc() -> str:
     return p
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OUT, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose: bool, debug_bounds: bool = False) -> str:
+    obj = os.path.join(OUT, ("dbg_" if debug_bounds else "") + os.path.splitext(src)[0] + ".o")
     cmd = [_nvcc(), "-std=c++17", "-O3", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC,-O2",
            "-I", os.path.join(ROOT, "include"), "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
+    if debug_bounds:
+        cmd.insert(1, "-DSFA_DEBUG_BOUNDS")
     if src.endswith(".cpp"):
         cmd[1:1] = ["-x", "c++"]
     if verbose:
@@ -46,17 +54,27 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    """Compile every source for sm_103a and link libsfa.so; returns its path."""
-    os.makedirs(OUT, exist_ok=True)
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + ".tmp"
+def _link(objs, lib: str) -> None:
+    tmp = lib + ".tmp"
     cmd = [_nvcc(), "-shared", *ARCH, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(verbose: bool = False, debug_bounds: bool = True) -> str:
+    """Compile every source for sm_103a and link libsfa.so (and, with
+    debug_bounds, the bounds-checked libsfa_debug.so); returns libsfa.so's path."""
+    os.makedirs(OUT, exist_ok=True)
+    jobs = [(s, False) for s in SOURCES] + ([(s, True) for s in DEBUG_SOURCES] if debug_bounds else [])
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], verbose, j[1]), jobs))
+    main = objs[:len(SOURCES)]
+    _link(main, LIB)
+    if debug_bounds:
+        dbg = dict(zip(DEBUG_SOURCES, objs[len(SOURCES):]))
+        _link([dbg.get(s, o) for s, o in zip(SOURCES, main)], DEBUG_LIB)
     return LIB
 
 

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const AttnArgs a,
   const int pl = qh >> a.lgG, hl = qh & (G - 1);
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int i0 = blockIdx.x * TQ, i = i0 + pl, h = g * G + hl;
-  const bool active = i < a.T;
+  const bool active = i < a.T && dbg_in((int64_t)(b * a.Hq + h) * a.T + i, (int64_t)a.B * a.Hq * a.T, a.status);
   const int ic = active ? i : 0;
   const int imax = min(a.T - 1, i0 + TQ - 1);
   const int64_t rowidx = (int64_t)(b * a.Hq + h) * a.T + ic;
@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const AttnArgs a,
 
   // One slot: P, dS and the dq update.  `ok` is uniform across the lane pair.
   auto slot_update = [&](bool ok, int row) {
+    ok = ok && dbg_in(row, kSlab, a.status);
     const int r = ok ? row : 0;
     const float s = pair_dot(qr, sK + r * kRowPad + half * 32);
     const float dp = pair_dot(dor, sV + r * kRowPad + half * 32);
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const AttnArgs a,
     const int s_hi = min(wmax, s_lo + kWinChunk - 1);
     const int pos_lo = i0 - s_hi;
     __syncthreads();
-    stage_rows<TIO>(Kb, Vb, rope, pos_lo, imax - s_lo - pos_lo + 1, sK, sV);
+    stage_rows<TIO>(Kb, Vb, rope, pos_lo, imax - s_lo - pos_lo + 1, sK, sV, a.T, a.status);
     __syncthreads();
     for (int s = s_lo; s <= s_hi; ++s) slot_update(active && i >= s, pl + (s_hi - s));
   }
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_q_kernel(const AttnArgs a,
   for (int r0 = 0; r0 < nr; r0 += RB) {
     const int nb = min(RB, nr - r0);
     __syncthreads();
-    stage_rungs<TIO, INTERP>(Kb, Vb, rope, P, r0, nb, i0, TQ, a.T, sK, sV);
+    stage_rungs<TIO, INTERP>(Kb, Vb, rope, P, r0, nb, i0, TQ, a.T, sK, sV, a.status);
     __syncthreads();
     for (int x = 0; x < nb; ++x)
       slot_update(active && i >= P.c[r0 + x] && i - P.c[r0 + x] < a.T, x * TQ + pl);
@@ -171,7 +172,7 @@ __device__ __forceinline__ float pair_dot_ss(const float* x, const float* y) {
 template <typename TIO>
 __device__ __forceinline__ void stage_queries(const AttnArgs& a, int b, int g, int G, int pos_lo,
                                               int nrows, float* sQ, float* sD, float* sLse,
-                                              float* sDel) {
+                                              float* sDel, int rows_cap) {
   const float2* rope = static_cast<const float2*>(a.rope);
   for (int it = threadIdx.x; it < nrows * G * 4; it += kThreads) {
     const int pc = it & 3, rh = it >> 2;
@@ -179,6 +180,9 @@ __device__ __forceinline__ void stage_queries(const AttnArgs& a, int b, int g, i
     const int pos = pos_lo + r;
     if (pos < 0 || pos >= a.T) continue;
     const int64_t ridx = (int64_t)(b * a.Hq + g * G + hh) * a.T + pos;
+    if (!dbg_in(r * G + hh, (int64_t)rows_cap * G, a.status) ||
+        !dbg_in(ridx, (int64_t)a.B * a.Hq * a.T, a.status))
+      continue;
     float lo[8], hi[8];
     load_pair_chunk(static_cast<const TIO*>(a.q) + ridx * kD, pc, rope, pos, lo, hi);
 #pragma unroll
@@ -251,10 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kv_kernel(const AttnArgs a,
     const int pos_lo = j0 + s_lo;
     __syncthreads();
     stage_queries<TIO>(a, b, g, G, pos_lo, min(a.T - 1, jmax + s_hi) - pos_lo + 1, sQ, sD, sLse,
-                       sDel);
+                       sDel, QR);
     __syncthreads();
     for (int s = s_lo; s <= s_hi; ++s) {
-      const bool ok = active && j + s < a.T;
+      const bool ok = active && j + s < a.T && dbg_in((jl + s - s_lo) * G + hl, (int64_t)QR * G, a.status);
       const int r = ok ? (jl + s - s_lo) * G + hl : hl;
       const float* q = sQ + r * kRowPad + hoff;
       const float* d = sD + r * kRowPad + hoff;
@@ -279,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kv_kernel(const AttnArgs a,
     const int pos_lo = j0 + c - 1;
     __syncthreads();
     stage_queries<TIO>(a, b, g, G, pos_lo, min(a.T - 1, jmax + c) - pos_lo + 1, sQ, sD, sLse,
-                       sDel);
+                       sDel, QR);
     __syncthreads();
     // query j + c: interpolates rows j (weight u) and j + 1 (weight w)
     {
-      const bool ok = active && j + c >= 0 && j + c < a.T;
+      const bool ok = active && j + c >= 0 && j + c < a.T && dbg_in((jl + 1) * G + hl, (int64_t)QR * G, a.status);
       const int r = (ok ? jl + 1 : 0) * G + hl;
       const float* q = sQ + r * kRowPad + hoff;
       const float* d = sD + r * kRowPad + hoff;
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kv_kernel(const AttnArgs a,
     }
     // query j + c - 1: interpolates rows j - 1 (weight u) and j (weight w)
     if (INTERP && w != 0.0f) {
-      const bool ok = active && j >= 1 && j + c - 1 < a.T;
+      const bool ok = active && j >= 1 && j + c - 1 < a.T && dbg_in(jl * G + hl, (int64_t)QR * G, a.status);
       const int r = (ok ? jl : 0) * G + hl;
       const float* q = sQ + r * kRowPad + hoff;
       const float* d = sD + r * kRowPad + hoff;
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kv_kernel(const AttnArgs a,
   float other[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e) other[e] = __shfl_xor_sync(0xffffffffu, dk[e], 1);
-  if (active && hl == 0) {
+  if (active && hl == 0 && dbg_in((int64_t)bg * a.T + j, (int64_t)a.B * a.Hkv * a.T, a.status)) {
     const int64_t krow = ((int64_t)bg * a.T + j) * kD + hoff;
     float out[32];
     if (rope) {

@@ -345,6 +345,22 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
                                          const float* corr, float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
   using Fmt = CoefFmt<FOLD>;
+  // FOLD: the delta - psi values of every (k-step, half) this lane reads, loaded
+  // before the products so their latency overlaps (heads tig & 1 and
+  // (tig & 1) + 2 of query qw + m + (tig >> 1); 0 where the lane reads nothing)
+  float cf[FOLD ? NKS : 1][2][2];
+  if (FOLD) {
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks)
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int m = 4 * ks + 2 * hb;
+        const bool on = (mask >> m) & 1u;
+        const int qi = on ? qw + m + (tig >> 1) : 0;
+        cf[ks][hb][0] = on ? __ldg(corr + (int64_t)(tig & 1) * T + qi) : 0.0f;
+        cf[ks][hb][1] = on ? __ldg(corr + (int64_t)((tig & 1) + 2) * T + qi) : 0.0f;
+      }
+  }
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
     uint32_t bk[2], bvv[2], bkl[2], bvl[2];
@@ -356,10 +372,7 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
         const uint32_t* half = csm + rec + m * STEP;
         if (FOLD) {  // words dS hi, dS lo, P hi, P lo
           const uint4 r4 = *reinterpret_cast<const uint4*>(half);
-          const int qi = qw + m + (tig >> 1);
-          // heads tig & 1 (low half) and (tig & 1) + 2 (high half)
-          const float c0 = __ldg(corr + (int64_t)(tig & 1) * T + qi);
-          const float c1 = __ldg(corr + (int64_t)((tig & 1) + 2) * T + qi);
+          const float c0 = cf[FOLD ? ks : 0][hb][0], c1 = cf[FOLD ? ks : 0][hb][1];
           const float2 lo = unpack_bf16(r4.y), pw = unpack_bf16(r4.z);
           bk[hb] = r4.x;
           bkl[hb] = pack_bf16(fmaf(pw.x, c0, lo.x), fmaf(pw.y, c1, lo.y));

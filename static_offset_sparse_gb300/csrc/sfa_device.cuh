@@ -15,6 +15,21 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 using bf16 = __nv_bfloat16;
 
+// Bounds checks of the SIMT kernels' indices, compiled in by SFA_DEBUG_BOUNDS
+// (the bounds-checked build, libsfa_debug.so): an index outside [0, n) is
+// recorded as SFA_ERR_DEVICE_BOUNDS in the status word and the access it
+// guards is skipped; nothing traps.  In the release build the check is
+// constant true and compiles away.
+#ifdef SFA_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_in(int64_t i, int64_t n, int* status) {
+  if (i >= 0 && i < n) return true;
+  if (status) atomicCAS(status, 0, SFA_ERR_DEVICE_BOUNDS);
+  return false;
+}
+#else
+__device__ __forceinline__ bool dbg_in(int64_t, int64_t, int*) { return true; }
+#endif
+
 // Eight consecutive elements -> fp32.  p must be 16-byte aligned.
 __device__ __forceinline__ void load8(const float* p, float* x) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p));

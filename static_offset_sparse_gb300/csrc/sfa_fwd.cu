@@ -104,14 +104,14 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const AttnArgs a,
     const int s_hi = min(wmax, s_lo + kWinChunk - 1);
     const int pos_lo = i0 - s_hi;
     __syncthreads();
-    stage_rows<TIO>(Kb, Vb, rope, pos_lo, imax - s_lo - pos_lo + 1, sK, sV);
+    stage_rows<TIO>(Kb, Vb, rope, pos_lo, imax - s_lo - pos_lo + 1, sK, sV, a.T, a.status);
     __syncthreads();
     softmax_batch(
         s_hi - s_lo + 1,
         [&](int x, int& row) {
           const int s = s_lo + x;
           row = pl + (s_hi - s);
-          return active && i >= s;
+          return active && i >= s && dbg_in(row, kSlab, a.status);
         },
         qr, sK, sV, sL, m, l, acc);
   }
@@ -123,18 +123,18 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const AttnArgs a,
   for (int r0 = 0; r0 < nr; r0 += RB) {
     const int nb = min(RB, nr - r0);
     __syncthreads();
-    stage_rungs<TIO, INTERP>(Kb, Vb, rope, P, r0, nb, i0, TQ, a.T, sK, sV);
+    stage_rungs<TIO, INTERP>(Kb, Vb, rope, P, r0, nb, i0, TQ, a.T, sK, sV, a.status);
     __syncthreads();
     softmax_batch(
         nb,
         [&](int x, int& row) {
           row = x * TQ + pl;
-          return active && i >= P.c[r0 + x] && i - P.c[r0 + x] < a.T;
+          return active && i >= P.c[r0 + x] && i - P.c[r0 + x] < a.T && dbg_in(row, kSlab, a.status);
         },
         qr, sK, sV, sL, m, l, acc);
   }
 
-  if (active) {
+  if (active && dbg_in((int64_t)(b * a.Hq + h) * a.T + i, (int64_t)a.B * a.Hq * a.T, a.status)) {
     const float inv = 1.0f / l;
     TIO* op = static_cast<TIO*>(a.out_o) + qrow + half * 32;
 #pragma unroll

@@ -16,13 +16,16 @@ constexpr int kWinChunk = 16;   // window distances per batch
 constexpr int kMaxBatch = 16;   // slots per batch
 
 // Stage rows [pos_lo, pos_lo + nrows) of K (rotated) and V into sK / sV.
+// T and status serve the bounds-checked build only.
 template <typename TIO>
 __device__ __forceinline__ void stage_rows(const TIO* Kb, const TIO* Vb, const float2* rope,
-                                           int pos_lo, int nrows, float* sK, float* sV) {
+                                           int pos_lo, int nrows, float* sK, float* sV, int T,
+                                           int* status) {
   for (int it = threadIdx.x; it < nrows * 4; it += kThreads) {
     const int r = it >> 2, pc = it & 3;
     const int pos = pos_lo + r;
     if (pos < 0) continue;  // never read: a slot needs i - s >= 0
+    if (!dbg_in(pos, T, status) || !dbg_in(r, kSlab, status)) continue;
     float lo[8], hi[8];
     load_pair_chunk(Kb + (int64_t)pos * kD, pc, rope, pos, lo, hi);
     st_smem8(sK + r * kRowPad + 8 * pc, lo);
@@ -39,7 +42,7 @@ __device__ __forceinline__ void stage_rows(const TIO* Kb, const TIO* Vb, const f
 template <typename TIO, bool INTERP>
 __device__ __forceinline__ void stage_rungs(const TIO* Kb, const TIO* Vb, const float2* rope,
                                             const Plan& P, int r0, int nb, int i0, int TQ, int T,
-                                            float* sK, float* sV) {
+                                            float* sK, float* sV, int* status) {
   const int per = TQ * 4;
   for (int it = threadIdx.x; it < nb * per; it += kThreads) {
     const int a = it / per, rem = it - a * per;
@@ -47,6 +50,7 @@ __device__ __forceinline__ void stage_rungs(const TIO* Kb, const TIO* Vb, const 
     const int iq = i0 + rr;
     const int p0 = iq - P.c[r0 + a];
     if (iq >= T || p0 < 0 || p0 >= T) continue;  // rung absent for this query
+    if (!dbg_in(a * TQ + rr, kSlab, status)) continue;
     float* dk = sK + (a * TQ + rr) * kRowPad;
     float* dv = sV + (a * TQ + rr) * kRowPad;
     float klo[8], khi[8], vlo[8], vhi[8];
@@ -54,7 +58,7 @@ __device__ __forceinline__ void stage_rungs(const TIO* Kb, const TIO* Vb, const 
     load_pair_chunk<TIO>(Vb + (int64_t)p0 * kD, pc, nullptr, p0, vlo, vhi);
     if (INTERP) {
       const float w = P.w[r0 + a];
-      if (w != 0.0f) {  // p0 + 1 <= iq: always inside the sequence
+      if (w != 0.0f && dbg_in(p0 + 1, T, status)) {  // p0 + 1 <= iq: inside the sequence
         float k2l[8], k2h[8], v2l[8], v2h[8];
         load_pair_chunk(Kb + (int64_t)(p0 + 1) * kD, pc, rope, p0 + 1, k2l, k2h);
         load_pair_chunk<TIO>(Vb + (int64_t)(p0 + 1) * kD, pc, nullptr, p0 + 1, v2l, v2h);

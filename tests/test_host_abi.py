@@ -28,6 +28,20 @@ def test_exports_every_declared_symbol(sfa_lib):
         assert hasattr(sfa_lib, n), n
 
 
+def test_bounds_checked_build_exports_the_same_symbols(sfa_lib):
+    """libsfa_debug.so (SIMT kernels with index checks) is a drop-in build of
+    the same C ABI; loading it binds every declared entry point."""
+    from static_offset_sparse_gb300 import _lib, build
+
+    if not os.path.exists(_lib.DEBUG_LIB_PATH):
+        build.build()
+    dbg = _lib.bind(_lib.DEBUG_LIB_PATH)
+    for n in _declared():
+        assert hasattr(dbg, n), n
+    out = (C.c_int32 * 15)()
+    assert dbg.sfa_offsets_fib(15, out) == 0 and out[14] == 987
+
+
 def test_offsets_match_oracle(sfa_lib):
     import static_offset_sparse_gb300 as s
 
