@@ -430,7 +430,7 @@ struct QTile {
 };
 
 template <int G>
-__global__ void __launch_bounds__(kBThreads, 4)
+__global__ void __launch_bounds__(kBThreads, 5)
     band_fwd_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mq,
                     const __grid_constant__ CUtensorMap mo, const __grid_constant__ BandPlan P) {
