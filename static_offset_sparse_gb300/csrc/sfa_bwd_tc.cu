@@ -90,8 +90,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 
   const int wmax = min(P.W, imax);
   const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
-  int nr = 0;
-  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int nr = rungs_upto(P, imax);
   const int NG = nwc + (nr + 1) / 2;
   const uint32_t qtile = sbase, dotile = sbase + kTcQTileB, otile = sbase + 2 * kTcQTileB;
   const uint32_t stages = sbase + 3 * kTcQTileB;
@@ -439,8 +438,7 @@ __global__ void __launch_bounds__(kKvThreads, 2)
 
   const int wmax = min(P.W, T - 1 - j0);
   const int nwc = wmax >= 0 ? wmax / kKvWC + 1 : 0;
-  int nr = 0;
-  while (nr < P.n && P.c[nr] <= T - j0) ++nr;
+  const int nr = rungs_upto(P, T - j0);
   const int NG = nwc + nr;       // groups per query-head group
   const int NGt = MULTI ? NG * msub : NG;  // all groups: query-head group gt / NG, group gt % NG
   // group -> first staged query: window chunk s_lo = 9 grp, or rung grp - nwc

@@ -98,8 +98,7 @@ __global__ void __launch_bounds__(kTcThreads, 5)
 
   const int wmax = min(P.W, imax);
   const int nwc = wmax >= 0 ? wmax / kTcWC + 1 : 0;
-  int nr = 0;
-  while (nr < P.n && P.c[nr] <= imax) ++nr;
+  const int nr = rungs_upto(P, imax);
   const int NG = nwc + (nr + 1) / 2;
   const uint32_t qtile = sbase, stages = sbase + kTcQTileB;
   const int qplane = b * a.Hq + g * 4;

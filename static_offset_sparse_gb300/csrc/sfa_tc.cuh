@@ -30,6 +30,17 @@ constexpr int kTcStageB = 2 * kTcRegionB;
 constexpr int kTcStages = 2;
 constexpr int kTcWC = 12;                     // window distances per chunk
 
+// Number of rungs with c <= x (the plan's c are ascending): binary search.
+__device__ __forceinline__ int rungs_upto(const Plan& P, int x) {
+  int lo = 0, hi = P.n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (P.c[mid] <= x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // S[16 x 8] += q' . K'^T for the 8 key rows of a region; lane l supplies
 // row `row` (its key column l & 7).
 __device__ __forceinline__ void qk_tile(const uint32_t (*qa)[4], uint32_t region, int row, float* s) {
@@ -200,11 +211,14 @@ __device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float4
     x[0][kk][0] = a0.x; x[0][kk][1] = a0.y; x[0][kk][2] = a2.x; x[0][kk][3] = a2.y;
     x[1][kk][0] = a1.x; x[1][kk][1] = a1.y; x[1][kk][2] = a3.x; x[1][kk][3] = a3.y;
   }
+  // scale is a power of two (1/8 or 1), so folding it into cos and sin gives
+  // the same bits as scaling the rotated values
   if (rp) {
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const float4 a = rp[2 * kk], b = rp[2 * kk + 1];
-      const float cs[4] = {a.x, a.z, b.x, b.z}, sn[4] = {a.y, a.w, b.y, b.w};
+      const float cs[4] = {a.x * scale, a.z * scale, b.x * scale, b.z * scale};
+      const float sn[4] = {a.y * scale, a.w * scale, b.y * scale, b.w * scale};
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
@@ -214,13 +228,20 @@ __device__ __forceinline__ void tile_frags(uint32_t tile, int warp, const float4
           x[rr][kk + 2][e] = lo * sn[e] + hi * cs[e];
         }
     }
+  } else {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[rr][kk][e] *= scale;
   }
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
-    qa[kk][0] = pack_bf16(x[0][kk][0] * scale, x[0][kk][1] * scale);
-    qa[kk][1] = pack_bf16(x[1][kk][0] * scale, x[1][kk][1] * scale);
-    qa[kk][2] = pack_bf16(x[0][kk][2] * scale, x[0][kk][3] * scale);
-    qa[kk][3] = pack_bf16(x[1][kk][2] * scale, x[1][kk][3] * scale);
+    qa[kk][0] = pack_bf16(x[0][kk][0], x[0][kk][1]);
+    qa[kk][1] = pack_bf16(x[1][kk][0], x[1][kk][1]);
+    qa[kk][2] = pack_bf16(x[0][kk][2], x[0][kk][3]);
+    qa[kk][3] = pack_bf16(x[1][kk][2], x[1][kk][3]);
   }
 }
 
