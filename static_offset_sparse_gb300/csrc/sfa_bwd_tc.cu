@@ -108,31 +108,27 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   if (!tc_wait_qtiles(bars, a)) return;
   tile_frags(qtile, warp, rope ? rp : nullptr, 0.125f, true, qa);
   tile_frags(dotile, warp, nullptr, 1.0f, false, da);
-  {  // delta = dO . O per row, from the dO and O fragments of this lane (16 dims), then the quad
-    uint32_t oa[4][4];
-    tile_frags(otile, warp, nullptr, 1.0f, false, oa);
-    float acc[2] = {0.0f, 0.0f};
+  {  // delta = dO . O per row: the diagonal of dO . O^T over the warp's 16 rows, by
+     // two tensor-core tiles (columns = rows 0..7 and 8..15 of the O tile); the
+     // diagonal element of row gid (gid + 8) sits in lane 4 gid + gid / 2, column
+     // gid & 1 of the first (second) tile
+    float dd[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float2 u = unpack_bf16(da[kk][x]), v = unpack_bf16(oa[kk][x]);
-        acc[x & 1] = fmaf(u.x, v.x, fmaf(u.y, v.y, acc[x & 1]));  // x even: row gid, odd: gid + 8
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 1);
-      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
-      delta[r] = acc[r];
+    for (int nt = 0; nt < 2; ++nt) {
+      const int r = 8 * nt + (lane & 7);
+      qk_tile(da, otile, (r >> 2) * kTcQRows + 4 * warp + (r & 3), dd[nt]);
     }
+    const float mine0 = (gid & 1) ? dd[0][1] : dd[0][0], mine1 = (gid & 1) ? dd[1][3] : dd[1][2];
+    const int src = 4 * gid + (gid >> 1);
+    delta[0] = __shfl_sync(0xffffffffu, mine0, src);
+    delta[1] = __shfl_sync(0xffffffffu, mine1, src);
   }
   __syncthreads();  // the dO tile is read: it now carries q~ = q'/8 out for the key side
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    st_shared_u32(otile_addr(dotile, warp, gid, 16 * kk + 2 * tig), qa[kk][0]);
-    st_shared_u32(otile_addr(dotile, warp, gid + 8, 16 * kk + 2 * tig), qa[kk][1]);
-    st_shared_u32(otile_addr(dotile, warp, gid, 16 * kk + 2 * tig + 8), qa[kk][2]);
-    st_shared_u32(otile_addr(dotile, warp, gid + 8, 16 * kk + 2 * tig + 8), qa[kk][3]);
+  {  // the A fragments are the output layout: k-step kk holds dims 16 kk .. 16 kk + 15
+    const uint32_t pk[8][2] = {{qa[0][0], qa[0][1]}, {qa[0][2], qa[0][3]}, {qa[1][0], qa[1][1]},
+                               {qa[1][2], qa[1][3]}, {qa[2][0], qa[2][1]}, {qa[2][2], qa[2][3]},
+                               {qa[3][0], qa[3][1]}, {qa[3][2], qa[3][3]}};
+    store_otile(dotile, warp, pk);
   }
   fence_async_smem();
   __syncthreads();
@@ -263,6 +259,7 @@ __global__ void __launch_bounds__(kTcThreads, 4)
   }
   // dQ = R(-phi) dq / 8 (dims d in tile nd and d + 32 in tile nd + 4 share a
   // lane), out through the Q tile's space and one TMA store
+  uint32_t pk[8][2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     float v[8][2];
@@ -285,9 +282,9 @@ __global__ void __launch_bounds__(kTcThreads, 4)
       }
     }
 #pragma unroll
-    for (int nd = 0; nd < 8; ++nd)
-      st_shared_u32(otile_addr(qtile, warp, gid + 8 * r, 8 * nd + 2 * tig), pack_bf16(v[nd][0], v[nd][1]));
+    for (int nd = 0; nd < 8; ++nd) pk[nd][r] = pack_bf16(v[nd][0], v[nd][1]);
   }
+  store_otile(qtile, warp, pk);
   fence_async_smem();
   __syncthreads();
   if (threadIdx.x == 0) {

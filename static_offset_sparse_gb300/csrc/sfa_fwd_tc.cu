@@ -225,16 +225,16 @@ __global__ void __launch_bounds__(kTcThreads, 5)
     l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
   }
   // O = acc / l through an output tile (the Q tile's space) and one TMA store
+  uint32_t pk[8][2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const float inv = 1.0f / l[r];
 #pragma unroll
-    for (int nd = 0; nd < 8; ++nd)
-      st_shared_u32(otile_addr(qtile, warp, gid + 8 * r, 8 * nd + 2 * tig),
-                    pack_bf16(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv));
+    for (int nd = 0; nd < 8; ++nd) pk[nd][r] = pack_bf16(o[nd][2 * r] * inv, o[nd][2 * r + 1] * inv);
     if (tig == 0 && i < T)
       a.out_lse[(int64_t)(b * a.Hq + (r ? hB : hA)) * T + i] = (m[r] + log2f(l[r])) * kLn2;
   }
+  store_otile(qtile, warp, pk);
   fence_async_smem();
   __syncthreads();
   if (threadIdx.x == 0) {

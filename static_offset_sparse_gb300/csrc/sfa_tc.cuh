@@ -256,6 +256,28 @@ __device__ __forceinline__ uint32_t otile_addr(uint32_t tile, int warp, int r, i
   return tile + swz(srow, d >> 3) + (d & 7) * 2;
 }
 
+// stmatrix: four 8x8 b16 tiles to shared memory (lanes 8t..8t+7 give tile
+// t's row addresses; register t holds the lane's pair of tile t, row lane / 4,
+// columns 2 (lane % 4), + 1: the mma fragment layout).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                        uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// A warp's 16 x 64 rows of an output tile (row r = 4 h + p) from packed bf16
+// pairs pk[nd][x]: row gid (x = 0) or gid + 8 (x = 1), dims 8 nd + 2 tig, + 1.
+// Four stmatrix, each two 16-row chunks nd, nd + 1.
+__device__ __forceinline__ void store_otile(uint32_t tile, int warp, const uint32_t (*pk)[2]) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3;
+  const int r = 8 * (mi & 1) + (lane & 7);
+  const int srow = (r >> 2) * kTcORows + 4 * warp + (r & 3);
+#pragma unroll
+  for (int nd = 0; nd < 8; nd += 2)
+    stsm_x4(tile + swz(srow, nd + (mi >> 1)), pk[nd][0], pk[nd][1], pk[nd + 1][0], pk[nd + 1][1]);
+}
+
 // Store an output tile (thread 0; after every thread's fence + a barrier).
 __device__ __forceinline__ void tc_store_tile(const CUtensorMap* map, uint32_t tile, int i0,
                                               int plane) {
