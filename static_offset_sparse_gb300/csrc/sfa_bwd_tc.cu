@@ -295,20 +295,37 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 
 constexpr int kKvTK = 32;                     // key rows per CTA
 constexpr int kKvThreads = 256;               // 8 warps: 4 key groups of 8 rows x 2 dim halves
-// Queries staged per group: 40 are read; 42 rows per head plane make the
-// plane stride 2 (mod 8) rows, so the 128B swizzle puts the 8 (query, head)
-// rows of one ldmatrix tile on distinct banks.
-constexpr int kKvQ = kKvTK + 10;
 // A rung group reaches queries j + c - 1 .. j + c + 31 (33 rows); 34 rows keep
-// the plane stride at 2 (mod 8).  Each warp reads 12 of them (3 k-steps), from
-// row min(8 kw, 22) on, which covers its keys' 9 queries 8 kw .. 8 kw + 8.
+// the plane stride at 2 (mod 8), so the 128B swizzle puts the 8 (query, head)
+// rows of one ldmatrix tile on distinct banks.  Each warp reads 12 of them (3
+// k-steps), from row min(8 kw, 22) on, which covers its keys' 9 queries
+// 8 kw .. 8 kw + 8.
 constexpr int kKvQR = kKvTK + 2;
-constexpr int kKvWC = 9;                      // window distances per chunk (16 queries x 4 heads)
-constexpr int kKvPlaneB = kKvQ * 4 * 128;     // q~ (or dO) box: [4 heads][42 queries][128 B]
-// records box: [42 queries][9 slots][16 or 32 B] (at most 12 KB)
-constexpr int kKvStageB = 2 * kKvPlaneB + 12288;
 constexpr int kKvStages = 2;
-constexpr size_t kBwdKvTcSmem = (size_t)kKvStages * kKvStageB + 1024;
+
+// Stage layout of the key side.  A window chunk of WC distances reaches
+// queries j0 + s_lo .. j0 + 31 + s_lo + WC - 1, staged as Q rows per head plane
+// (Q = 2 mod 8 again); a warp reads WKS k-steps of them from row
+// min(8 kw, Q - 4 WKS) on.
+//
+// G = 4 (16-byte records): chunks of 3 distances need the rung groups' 34 rows,
+// so every stage is [2 planes][4 heads][34 rows][128 B] + 2 KB of records
+// (36 KB) and three CTAs (24 warps) fit on an SM.  G > 4 (32-byte records)
+// keeps chunks of 9 distances (42 rows, 4 k-steps) in 54 KB stages, two CTAs
+// per SM.
+template <bool MULTI>
+struct KvLayout {
+  static constexpr int WC = MULTI ? 9 : 3;
+  static constexpr int Q = MULTI ? kKvTK + 10 : kKvQR;
+  static constexpr int WKS = MULTI ? 4 : 3;
+  static constexpr int PlaneB = Q * 4 * 128;             // q~ (or dO) box
+  static constexpr int RecB = MULTI ? 12288 : 2048;      // records box [Q queries][WC slots][16 or 32 B]
+  static constexpr int StageB = 2 * PlaneB + RecB;
+  static constexpr int MinBlocks = MULTI ? 2 : 3;
+  static constexpr size_t Smem = (size_t)kKvStages * StageB + 1024;
+  static_assert(Q * WC * CoefFmt<MULTI>::kRecBytes <= RecB && Q % 8 == 2, "key-side stage layout");
+  static_assert(PlaneB % 1024 == 0 && StageB % 1024 == 0, "swizzled boxes sit on 1024-byte periods");
+};
 
 // Bits m of the query offsets ql = m + t1 (t1 = tig >> 1) with lo <= ql <= hi.
 __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
@@ -405,7 +422,7 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
 
 // MULTI: G > 4, the key side loops over the G / 4 query-head groups of its KV head
 template <bool INTERP, bool MULTI>
-__global__ void __launch_bounds__(kKvThreads, 2)
+__global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
     bwd_kv_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap mq,
                      const __grid_constant__ CUtensorMap md, const __grid_constant__ CUtensorMap mqr,
                      const __grid_constant__ CUtensorMap mdr, const __grid_constant__ CUtensorMap mcw,
@@ -434,27 +451,28 @@ __global__ void __launch_bounds__(kKvThreads, 2)
       dv[x][2] = dv[x][3] = 0.0f;
 
   const int wmax = min(P.W, T - 1 - j0);
-  const int nwc = wmax >= 0 ? wmax / kKvWC + 1 : 0;
+  using L = KvLayout<MULTI>;
+  const int nwc = wmax >= 0 ? wmax / L::WC + 1 : 0;
   const int nr = rungs_upto(P, T - j0);
   const int NG = nwc + nr;       // groups per query-head group
   const int NGt = MULTI ? NG * msub : NG;  // all groups: query-head group gt / NG, group gt % NG
-  // group -> first staged query: window chunk s_lo = 9 grp, or rung grp - nwc
-  auto qb_of = [&](int grp) { return grp < nwc ? j0 + kKvWC * grp : j0 + P.c[grp - nwc] - 1; };
+  // group -> first staged query: window chunk s_lo = WC grp, or rung grp - nwc
+  auto qb_of = [&](int grp) { return grp < nwc ? j0 + L::WC * grp : j0 + P.c[grp - nwc] - 1; };
   auto issue = [&](int gt, uint32_t st, uint32_t bar) {
     const int sg = MULTI ? gt / NG : 0, grp = MULTI ? gt - sg * NG : gt;
     const int hplane = hplane_of(sg), rp = rplane_of(sg);
     const bool win = grp < nwc;
     const int qb = qb_of(grp);
     if (win) {
-      mbar_expect_tx(bar, 2 * kKvPlaneB + kKvQ * kKvWC * CoefFmt<MULTI>::kRecBytes);
+      mbar_expect_tx(bar, 2 * L::PlaneB + L::Q * L::WC * CoefFmt<MULTI>::kRecBytes);
       tma_load_3d(st, &mq, 0, qb, hplane, bar);
-      tma_load_3d(st + kKvPlaneB, &md, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * kKvPlaneB, &mcw, 0, kKvWC * grp, qb, rp, bar);
+      tma_load_3d(st + L::PlaneB, &md, 0, qb, hplane, bar);
+      tma_load_4d(st + 2 * L::PlaneB, &mcw, 0, L::WC * grp, qb, rp, bar);
     } else {
       mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * CoefFmt<MULTI>::kRecBytes);
       tma_load_3d(st, &mqr, 0, qb, hplane, bar);
-      tma_load_3d(st + kKvPlaneB, &mdr, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * kKvPlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, rp, bar);
+      tma_load_3d(st + L::PlaneB, &mdr, 0, qb, hplane, bar);
+      tma_load_4d(st + 2 * L::PlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, rp, bar);
     }
   };
 
@@ -466,7 +484,7 @@ __global__ void __launch_bounds__(kKvThreads, 2)
   __syncthreads();
   pdl_wait();  // the query side's q~, records and partials are complete from here on
   if (tid == 0)
-    for (int s = 0; s < kKvStages && s < NGt; ++s) issue(s, sbase + s * kKvStageB, smem_u32(&bars[s]));
+    for (int s = 0; s < kKvStages && s < NGt; ++s) issue(s, sbase + s * L::StageB, smem_u32(&bars[s]));
   // the RoPE pairs of the dK epilogue (keys 2 tig (+1) of the warp's group,
   // pairs 16 dh + gid (+8)), loaded now so their latency hides under the loop
   const float2* rope = static_cast<const float2*>(a.rope);
@@ -491,21 +509,22 @@ __global__ void __launch_bounds__(kKvThreads, 2)
       }
       return;
     }
-    const uint32_t qst = sbase + st * kKvStageB;
-    const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * kKvStageB + 2 * kKvPlaneB);
+    const uint32_t qst = sbase + st * L::StageB;
+    const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * L::StageB + 2 * L::PlaneB);
     // MULTI: query-head group gt / NG; its delta - psi rows for the correction
     const float* corr = MULTI ? a.dcorr + (int64_t)hplane_of(gt / NG) * T : nullptr;
     constexpr int RW = CoefFmt<MULTI>::kRecWords, HW = CoefFmt<MULTI>::kHalfWords;
     const int t1 = tig >> 1;
     if (grp < nwc) {
       // window chunk: query qw + ql reaches key j through slot s = ql + rel of
-      // the chunk (s in 0 .. s_hi - s_lo), record (qoff + ql) * 9 + s
-      const int s_lo = kKvWC * grp, qw = qb_of(grp) + 8 * kw, rel = qw - j - s_lo;
+      // the chunk (s in 0 .. s_hi - s_lo), record (qoff + ql) * WC + s
+      const int s_lo = L::WC * grp, qoff = min(8 * kw, L::Q - 4 * L::WKS), qw = qb_of(grp) + qoff;
+      const int rel = qw - j - s_lo;
       const uint32_t mask =
-          j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + kKvWC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
-      const int rec = (8 * kw * kKvWC + rel) * RW + HW * (tig & 1) + t1 * (kKvWC + 1) * RW;
-      kv_group<4, (kKvWC + 1) * RW, MULTI>(qst, qst + kKvPlaneB, csm, rec, mask, qw, kKvQ, 8 * kw, T,
-                                           dh, corr, dk, dv);
+          j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + L::WC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
+      const int rec = (qoff * L::WC + rel) * RW + HW * (tig & 1) + t1 * (L::WC + 1) * RW;
+      kv_group<L::WKS, (L::WC + 1) * RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, L::Q, qoff,
+                                                T, dh, corr, dk, dv);
     } else {
       // rung: query qw + ql reaches key j as role 1 (key i - c + 1) when
       // ql + rel = 0 and as role 0 (key i - c) when ql + rel = 1, and only if
@@ -515,7 +534,7 @@ __global__ void __launch_bounds__(kKvThreads, 2)
       const uint32_t mask =
           j < T ? ql_mask(max(-rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<3, RW, MULTI>(qst, qst + kKvPlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh, corr, dk,
+      kv_group<3, RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh, corr, dk,
                              dv);
     }
     __syncthreads();
@@ -607,9 +626,13 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   const int NS = p.W + 1 + 2 * p.n;
   const int64_t kvplanes = (int64_t)a.B * a.Hkv, qplanes = (int64_t)a.B * a.Hq;
   // query side: Q / dO / O tile loads (20-row boxes), q~ and dQ tile stores
-  // (16-row boxes); key side: q~ and dO slabs (42 rows for a window chunk,
-  // 34 for a rung) and the record boxes
-  const int rec_words = a.lgG > 2 ? CoefFmt<true>::kRecWords : CoefFmt<false>::kRecWords;
+  // (16-row boxes); key side: q~ and dO slabs (34 rows; 42 for a window chunk
+  // at G > 4) and the record boxes
+  const bool multi = a.lgG > 2;
+  const int rec_words = multi ? CoefFmt<true>::kRecWords : CoefFmt<false>::kRecWords;
+  const int wq = multi ? KvLayout<true>::Q : KvLayout<false>::Q;
+  const int wc = multi ? KvLayout<true>::WC : KvLayout<false>::WC;
+  const size_t kv_smem = multi ? KvLayout<true>::Smem : KvLayout<false>::Smem;
   CUtensorMap mk, mv, mq, md, mqr, mdr, mcw, mcr, tq, tdo, to, sqt, sdq;
   if (make_rows_map(&mk, kr, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
       make_rows_map(&mv, a.v, kvplanes, a.T, kTcBoxRows, 1) != SFA_OK ||
@@ -618,22 +641,21 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
       make_rows_map(&to, a.o, qplanes, a.T, kTcQRows, 4) != SFA_OK ||
       make_rows_map(&sqt, qt, qplanes, a.T, kTcORows, 4) != SFA_OK ||
       make_rows_map(&sdq, a.dq, qplanes, a.T, kTcORows, 4) != SFA_OK ||
-      make_rows_map(&mq, qt, qplanes, a.T, kKvQ, 4) != SFA_OK ||
-      make_rows_map(&md, a.dO, qplanes, a.T, kKvQ, 4) != SFA_OK ||
+      make_rows_map(&mq, qt, qplanes, a.T, wq, 4) != SFA_OK ||
+      make_rows_map(&md, a.dO, qplanes, a.T, wq, 4) != SFA_OK ||
       make_rows_map(&mqr, qt, qplanes, a.T, kKvQR, 4) != SFA_OK ||
       make_rows_map(&mdr, a.dO, qplanes, a.T, kKvQR, 4) != SFA_OK ||
-      make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, rec_words, kKvWC, kKvQ) != SFA_OK ||
+      make_coef_map(&mcw, coef, qplanes / 4, a.T, NS, rec_words, wc, wq) != SFA_OK ||
       make_coef_map(&mcr, coef, qplanes / 4, a.T, NS, rec_words, 2, kKvQR) != SFA_OK)
     return SFA_ERR_CUDA;
   const bool psi = a.dcorr != nullptr;
   auto kq = p.interp ? (psi ? bwd_q_tc_kernel<true, true> : bwd_q_tc_kernel<true, false>)
                      : (psi ? bwd_q_tc_kernel<false, true> : bwd_q_tc_kernel<false, false>);
-  const bool multi = a.lgG > 2;
   auto kkv = p.interp ? (multi ? bwd_kv_tc_kernel<true, true> : bwd_kv_tc_kernel<true, false>)
                       : (multi ? bwd_kv_tc_kernel<false, true> : bwd_kv_tc_kernel<false, false>);
   if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdQTcSmem) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdKvTcSmem) !=
+      cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_smem) !=
           cudaSuccess)
     return SFA_ERR_CUDA;
   dim3 gq((unsigned)((a.T + kTcTQ - 1) / kTcTQ), (unsigned)(a.B * (a.Hq / 4)));
@@ -646,7 +668,7 @@ int launch_backward_tc(const AttnArgs& a, const Plan& p, const void* kr, void* q
   dim3 gkv((unsigned)((a.T + kKvTK - 1) / kKvTK), (unsigned)(a.B * a.Hkv));
   {
     LaunchTimer tm(SFA_KERNEL_BWD_KV, stream);
-    if (launch_pdl(kkv, gkv, dim3(kKvThreads), kBwdKvTcSmem, s, a, mq, md, mqr, mdr, mcw, mcr, p) !=
+    if (launch_pdl(kkv, gkv, dim3(kKvThreads), kv_smem, s, a, mq, md, mqr, mdr, mcw, mcr, p) !=
         cudaSuccess)
       return SFA_ERR_CUDA;
   }
