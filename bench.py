@@ -378,7 +378,7 @@ def e2e_arm(layers, steps, world, dev):
     ev_out = [torch.cuda.Event() for _ in range(n)]
     first = [True]
 
-    def step():
+    def step(compute=True):
         for l, (L, hi) in enumerate(zip(layers, host_in)):
             with torch.cuda.stream(s_in):
                 if not first[0]:
@@ -388,7 +388,8 @@ def e2e_arm(layers, steps, world, dev):
                 ev_in[l].record(s_in)
         for l, L in enumerate(layers):
             s_cmp.wait_event(ev_in[l])
-            L.run(sp)
+            if compute:
+                L.run(sp)
             ev_done[l].record(s_cmp)
         for l, (L, ho) in enumerate(zip(layers, host_out)):
             with torch.cuda.stream(s_out):
@@ -407,14 +408,24 @@ def e2e_arm(layers, steps, world, dev):
         step()
     torch.cuda.synchronize()
     el = (time.perf_counter() - t0) / steps
+    # the same copies with the kernels left out: the host link's own time for
+    # a step's bytes, the floor of the end-to-end step
+    t0 = time.perf_counter()
+    for _ in range(3):
+        step(compute=False)
+    torch.cuda.synchronize()
+    el_copy = (time.perf_counter() - t0) / 3
     if world > 1:
-        t = torch.tensor([el], dtype=torch.float64, device=dev)
+        t = torch.tensor([el, el_copy], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
+        el, el_copy = float(t[0].item()), float(t[1].item())
     return {"value": round(world * B * T / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(el * 1e3, 3), "steps": steps,
+            "copies_only_ms_per_step": round(el_copy * 1e3, 3),
+            "host_link_gbs": round((h2d + d2h) / el_copy / 1e9, 1),
             "overlap": "host-to-device, compute and device-to-host streams, per-layer events; "
-                       "bound by the host link (2.1 GB per step)"}
+                       "bound by the host link (copies_only_ms_per_step: the same copies "
+                       "without the kernels)"}
 
 
 def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
