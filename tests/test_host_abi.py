@@ -122,6 +122,36 @@ def test_descriptor_validation_without_gpu(sfa_lib):
     assert sfa_lib.sfa_workspace_size(C.byref(d), 0, 1, C.byref(size)) == 1
 
 
+def test_empty_and_oversized_shapes_are_rejected_on_the_host(sfa_lib):
+    """Empty inputs (a zero extent) and shapes past the grid limits are
+    refused by the shape check, before any pointer or the device is touched:
+    the compute entry points return the error with null buffers on a machine
+    without a GPU.  The largest accepted shape still sizes its workspace."""
+    from static_offset_sparse_gb300._lib import Desc
+
+    size = C.c_size_t(0)
+    null = C.c_void_p(0)
+
+    def desc(B=1, T=16, Hq=8, Hkv=2):
+        d = Desc()
+        d.B, d.T, d.Hq, d.Hkv, d.D, d.dtype, d.W, d.alpha = B, T, Hq, Hkv, 64, 1, 8, 1.0
+        return d
+
+    for kw in ({"B": 0}, {"T": 0}, {"Hq": 0, "Hkv": 0}, {"Hkv": 0}, {"T": -5}):
+        d = desc(**kw)
+        assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 1, kw
+        assert sfa_lib.sfa_forward(C.byref(d), null, null, null, null, null, null, 0, null) == 1, kw
+        assert sfa_lib.sfa_backward(C.byref(d), null, null, null, null, null, null, null, null,
+                                    null, null, null, 0, null) == 1, kw
+    for kw in ({"T": (1 << 24) + 1}, {"B": 65536, "Hq": 4, "Hkv": 1}, {"B": 32768, "Hkv": 2}):
+        d = desc(**kw)
+        assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 2, kw
+        assert sfa_lib.sfa_forward(C.byref(d), null, null, null, null, null, null, 0, null) == 2, kw
+    d = desc(B=1, T=1 << 24)
+    assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 0
+    assert size.value > (1 << 24) * 8 * 8  # at least the per-query records of the key side
+
+
 def test_int_distances_accept_signed_sets(sfa_lib):
     import static_offset_sparse_gb300 as s
     from static_offset_sparse_gb300 import SfaError
