@@ -814,7 +814,14 @@ def configs_arm(args, dev):
         ("2 with 16/2 heads (G = 8)", 16, 1024, 16, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
         ("5 with 8/1 heads (G = 8)", 16, 2048, 8, 1, "bf16", "int", (chris(),), True),
     ]
-    if args.only:
+    # per-rung cost: one config-2 layer (alpha = 0.97, W = 8) with the Fibonacci list
+    # cut to its first n entries (the first five are window distances, so n - 5 rungs);
+    # selected with --only "2 rung sweep", not part of the default list
+    sweep = [(f"2 rung sweep: {max(n - 5, 0)} rungs", 32, 1024, 8, 2, "bf16", "interp",
+              (FIB[:n], 0.97, 8), True) for n in (5, 6, 8, 10, 12, 15)]
+    if args.only and args.only.startswith("2 rung sweep"):
+        cases = sweep
+    elif args.only:
         cases = [c for c in cases if c[0].startswith(args.only)]
     out = []
     for name, Bc, Tc, Hq, Hkv, dt, kind, par, bwd in cases:
