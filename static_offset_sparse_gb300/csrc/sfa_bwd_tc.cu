@@ -352,12 +352,26 @@ __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
 // the exact delta = sum_j P_ij dP_ij instead of dO . O from the bf16-rounded
 // O, whose error the key side would otherwise sum over G heads.  The
 // correction is folded into the lo word.
-template <int NKS, int STEP, bool FOLD>
+//
+// ONEHOT (a rung group without FOLD): the lane's two query offsets that reach
+// its key are consecutive, so at most one of the (k-step, half) entries it
+// reads (query offsets of one parity) is set: one record load, then selects.
+template <int NKS, int STEP, bool FOLD, bool ONEHOT = false>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int rec,
                                          uint32_t mask, int qw, int kq, int qoff, int T, int dh,
                                          const float* corr, float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
   using Fmt = CoefFmt<FOLD>;
+  static_assert(!(ONEHOT && FOLD), "one-hot records are the 8-byte format");
+  int m1 = -1;
+  uint2 one = make_uint2(0u, 0u);
+  if (ONEHOT) {
+    const uint32_t me = mask & (0x55555555u >> (32 - 2 * 2 * NKS));  // the even bits read below
+    if (me) {
+      m1 = __ffs(me) - 1;
+      one = *reinterpret_cast<const uint2*>(csm + rec + m1 * STEP);
+    }
+  }
   // FOLD: the delta - psi values of every (k-step, half) this lane reads, loaded
   // before the products so their latency overlaps (heads tig & 1 and
   // (tig & 1) + 2 of query qw + m + (tig >> 1); 0 where the lane reads nothing)
@@ -381,7 +395,10 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
     for (int hb = 0; hb < 2; ++hb) {
       const int m = 4 * ks + 2 * hb;
       bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
-      if ((mask >> m) & 1u) {
+      if (ONEHOT) {
+        bk[hb] = m1 == m ? one.x : 0u;
+        bvv[hb] = m1 == m ? one.y : 0u;
+      } else if ((mask >> m) & 1u) {
         const uint32_t* half = csm + rec + m * STEP;
         if (FOLD) {  // words dS hi, dS lo, P hi, P lo
           const uint4 r4 = *reinterpret_cast<const uint4*>(half);
@@ -534,8 +551,8 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
       const uint32_t mask =
           j < T ? ql_mask(max(-rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<3, RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh, corr, dk,
-                             dv);
+      kv_group<3, RW, MULTI, !MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
+                                     corr, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
