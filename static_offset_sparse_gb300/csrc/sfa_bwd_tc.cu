@@ -10,8 +10,9 @@
 //   dQ = R(-phi) dQ / 8.  dL/dd_k = dS (q~.K'[i-c] - q~.K'[i-c+1])
 //   + P (dO.V[i-c] - dO.V[i-c+1]) comes from the same raw fragments.  For
 //   the key side it writes q~ = q'/8 (bf16) and, per (query, slot, head),
-//   the pair (P, dS) as a key-side-ready record (bf16 hi + lo; a rung gets
-//   one record per role: weight 1 - w for key i - c, w for key i - c + 1).
+//   the pair (P, dS) as a key-side-ready record (bf16 at G = 4, bf16 hi + lo
+//   at G > 4; a rung gets one record per role: weight 1 - w for key i - c, w
+//   for key i - c + 1).
 // bwd_kv_tc (per key tile): dK^T and dV^T accumulate as [64 dims x 8 keys]
 //   mma tiles per warp: A = q~^T or dO^T (TMA-staged slabs) of the (query,
 //   head) pairs that read the warp's 8 key rows, B = their (dS, P)
