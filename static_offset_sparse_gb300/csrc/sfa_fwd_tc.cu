@@ -31,9 +31,11 @@ namespace sfa {
 // thread owns one position and one 8-pair chunk of the rotation: it loads
 // that chunk of the cos/sin table once and rotates the position's rows in
 // kPrepPlanes consecutive (batch, KV head) planes per grid row (loads issued
-// before the arithmetic), so a layer spreads over hundreds of CTAs.
+// before the arithmetic).  One plane per grid row spreads a config-2 layer
+// (64 planes of 1024 rows) over 1024 CTAs, which hides the loads' latency
+// best.
 
-constexpr int kPrepPlanes = 2;
+constexpr int kPrepPlanes = 1;
 
 __global__ void __launch_bounds__(256) rope_prep_kernel(const bf16* __restrict__ k,
                                                         const float2* __restrict__ rope,
