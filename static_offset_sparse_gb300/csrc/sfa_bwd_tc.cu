@@ -354,30 +354,43 @@ __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
 // O, whose error the key side would otherwise sum over G heads.  The
 // correction is folded into the lo word.
 //
-// ONEHOT (a rung group without FOLD): the lane's two query offsets that reach
-// its key are consecutive, so at most one of the (k-step, half) entries it
-// reads (query offsets of one parity) is set: one record load, then selects.
+// ONEHOT (a rung group): the lane's two query offsets that reach its key are
+// consecutive, so at most one of the (k-step, half) entries it reads (query
+// offsets of one parity) is set: one record load (and with FOLD one pair of
+// corrections), then selects.
 template <int NKS, int STEP, bool FOLD, bool ONEHOT = false>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int rec,
                                          uint32_t mask, int qw, int kq, int qoff, int T, int dh,
                                          const float* corr, float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
   using Fmt = CoefFmt<FOLD>;
-  static_assert(!(ONEHOT && FOLD), "one-hot records are the 8-byte format");
+  // ONEHOT: the lane's one entry m1 (-1: none) as the four B words dS, dS lo,
+  // P, P lo (the lo words stay 0 without FOLD); with FOLD the correction of
+  // that entry alone is loaded
   int m1 = -1;
-  uint2 one = make_uint2(0u, 0u);
+  uint4 one = make_uint4(0u, 0u, 0u, 0u);
   if (ONEHOT) {
     const uint32_t me = mask & (0x55555555u >> (32 - 2 * 2 * NKS));  // the even bits read below
     if (me) {
       m1 = __ffs(me) - 1;
-      one = *reinterpret_cast<const uint2*>(csm + rec + m1 * STEP);
+      if (FOLD) {  // words dS hi, dS lo, P hi, P lo
+        const uint4 r4 = *reinterpret_cast<const uint4*>(csm + rec + m1 * STEP);
+        const int qi = qw + m1 + (tig >> 1);
+        const float c0 = __ldg(corr + (int64_t)(tig & 1) * T + qi);
+        const float c1 = __ldg(corr + (int64_t)((tig & 1) + 2) * T + qi);
+        const float2 lo = unpack_bf16(r4.y), pw = unpack_bf16(r4.z);
+        one = make_uint4(r4.x, pack_bf16(fmaf(pw.x, c0, lo.x), fmaf(pw.y, c1, lo.y)), r4.z, r4.w);
+      } else {  // words dS, P
+        const uint2 r2 = *reinterpret_cast<const uint2*>(csm + rec + m1 * STEP);
+        one = make_uint4(r2.x, 0u, r2.y, 0u);
+      }
     }
   }
   // FOLD: the delta - psi values of every (k-step, half) this lane reads, loaded
   // before the products so their latency overlaps (heads tig & 1 and
   // (tig & 1) + 2 of query qw + m + (tig >> 1); 0 where the lane reads nothing)
-  float cf[FOLD ? NKS : 1][2][2];
-  if (FOLD) {
+  float cf[FOLD && !ONEHOT ? NKS : 1][2][2];
+  if (FOLD && !ONEHOT) {
 #pragma unroll
     for (int ks = 0; ks < NKS; ++ks)
 #pragma unroll
@@ -398,12 +411,17 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
       bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
       if (ONEHOT) {
         bk[hb] = m1 == m ? one.x : 0u;
-        bvv[hb] = m1 == m ? one.y : 0u;
+        bvv[hb] = m1 == m ? one.z : 0u;
+        if (FOLD) {
+          bkl[hb] = m1 == m ? one.y : 0u;
+          bvl[hb] = m1 == m ? one.w : 0u;
+        }
       } else if ((mask >> m) & 1u) {
         const uint32_t* half = csm + rec + m * STEP;
         if (FOLD) {  // words dS hi, dS lo, P hi, P lo
           const uint4 r4 = *reinterpret_cast<const uint4*>(half);
-          const float c0 = cf[FOLD ? ks : 0][hb][0], c1 = cf[FOLD ? ks : 0][hb][1];
+          const float c0 = cf[FOLD && !ONEHOT ? ks : 0][hb][0];
+          const float c1 = cf[FOLD && !ONEHOT ? ks : 0][hb][1];
           const float2 lo = unpack_bf16(r4.y), pw = unpack_bf16(r4.z);
           bk[hb] = r4.x;
           bkl[hb] = pack_bf16(fmaf(pw.x, c0, lo.x), fmaf(pw.y, c1, lo.y));
@@ -552,8 +570,8 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
       const uint32_t mask =
           j < T ? ql_mask(max(-rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<3, RW, MULTI, !MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
-                                     corr, dk, dv);
+      kv_group<3, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
+                                   corr, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
