@@ -803,6 +803,10 @@ def configs_arm(args, dev):
         S = sfa.offsets_christoffel(128, 1024, True)
         return S
 
+    def chris_signed():  # bidirectional: the offsets and their negatives
+        S = sfa.offsets_christoffel(128, 1024, True)
+        return sorted(set(S) | {-x for x in S})
+
     cases = [  # name, B, T, Hq, Hkv, dtype, kind, params, backward
         ("1: fp32 interp, alpha=1", 1, 1024, 8, 2, "f32", "interp", (FIB, 1.0, 8), True),
         ("2: bf16 interp, one layer, alpha=0.9667", 32, 1024, 8, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
@@ -813,6 +817,8 @@ def configs_arm(args, dev):
         ("5 with 8/2 heads (G = 4)", 16, 2048, 8, 2, "bf16", "int", (chris(),), True),
         ("2 with 16/2 heads (G = 8)", 16, 1024, 16, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
         ("5 with 8/1 heads (G = 8)", 16, 2048, 8, 1, "bf16", "int", (chris(),), True),
+        ("signed (bidirectional) Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int",
+         (chris_signed(),), True),
     ]
     # per-rung cost: one config-2 layer (alpha = 0.97, W = 8) with the Fibonacci list
     # cut to its first n entries (the first five are window distances, so n - 5 rungs);

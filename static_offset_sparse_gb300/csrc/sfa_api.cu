@@ -173,8 +173,9 @@ static int fill_args(const sfa_desc* d, AttnArgs* a) {
   return status_ptr(&a->status);
 }
 
-// The tensor-core kernels serve causal key sets; a signed (bidirectional)
-// integer set, whose first rung distance is negative, runs the SIMT kernels.
+// The rung kernels serve causal key sets; a signed (bidirectional) integer
+// set, whose first rung distance is negative, runs the band kernels when it
+// has a band plan and the SIMT kernels otherwise.
 static bool tc_path(const sfa_desc* d, const Plan& p) {
   return use_tc(d) && (p.n == 0 || p.c[0] >= 0);
 }

@@ -52,15 +52,17 @@ __device__ __forceinline__ void run_shift(const BandPlan& P, int m, int r, int& 
 }
 
 // Key tiles of a query tile (class r, compressed positions u0 .. ul): run by
-// run, the band [u0 + e - len + 1, ul + e] clipped at 0, from its low end in
-// steps of 64.
+// run, the band [u0 + e - len + 1, ul + e] clipped to the sequence's Uc
+// compressed keys (a negative distance, e > 0, reads later keys), from its
+// low end in steps of 64.
 struct QWalk {
   int m, vs, vhi, rho, e;
 };
-__device__ __forceinline__ bool qwalk_seek(const BandPlan& P, int r, int u0, int ul, QWalk& w) {
+__device__ __forceinline__ bool qwalk_seek(const BandPlan& P, int r, int u0, int ul, int Uc,
+                                           QWalk& w) {
   for (; w.m < P.nruns; ++w.m) {
     run_shift(P, w.m, r, w.rho, w.e);
-    const int lo = max(0, u0 + w.e - P.len[w.m] + 1), hi = ul + w.e;
+    const int lo = max(0, u0 + w.e - P.len[w.m] + 1), hi = min(ul + w.e, Uc - 1);
     if (lo <= hi) {
       w.vs = lo;
       w.vhi = hi;
@@ -69,26 +71,28 @@ __device__ __forceinline__ bool qwalk_seek(const BandPlan& P, int r, int u0, int
   }
   return false;
 }
-__device__ __forceinline__ bool qwalk_next(const BandPlan& P, int r, int u0, int ul, QWalk& w) {
+__device__ __forceinline__ bool qwalk_next(const BandPlan& P, int r, int u0, int ul, int Uc,
+                                           QWalk& w) {
   w.vs += kBR;
   if (w.vs <= w.vhi) return true;
   ++w.m;
-  return qwalk_seek(P, r, u0, ul, w);
+  return qwalk_seek(P, r, u0, ul, Uc, w);
 }
 
 // Query tiles that reach a key tile (class rho, compressed keys v0 .. vl):
 // run by run, query class r = (rho + a) mod delta at positions
-// [v0 - e, vl - e + len - 1] (clipped to the sequence), in steps of bu.
+// [v0 - e, vl - e + len - 1] (clipped to the sequence at both ends), in steps
+// of bu.
 struct KWalk {
   int m, us, uhi, r, e;
 };
 __device__ __forceinline__ bool kwalk_seek(const BandPlan& P, int rho, int v0, int vl, int Uc,
                                            KWalk& w) {
   for (; w.m < P.nruns; ++w.m) {
-    w.r = (rho + P.a[w.m]) % P.delta;
+    w.r = ((rho + P.a[w.m]) % P.delta + P.delta) % P.delta;  // a < 0 for a signed run
     int rho2;
     run_shift(P, w.m, w.r, rho2, w.e);
-    const int lo = v0 - w.e, hi = min(Uc - 1, vl - w.e + P.len[w.m] - 1);
+    const int lo = max(0, v0 - w.e), hi = min(Uc - 1, vl - w.e + P.len[w.m] - 1);
     if (lo <= hi) {
       w.us = lo;
       w.uhi = hi;
@@ -400,7 +404,7 @@ struct QTile {
   __device__ __forceinline__ int count(const BandPlan& P) const {
     int n = 0;
     QWalk w{0, 0, 0, 0, 0};
-    if (qwalk_seek(P, r, u0, ul, w)) do ++n; while (qwalk_next(P, r, u0, ul, w));
+    if (qwalk_seek(P, r, u0, ul, Uc, w)) do ++n; while (qwalk_next(P, r, u0, ul, Uc, w));
     return n;
   }
   // Positions of this warp's 16 rows: one head's 16 consecutive positions
@@ -414,7 +418,8 @@ struct QTile {
   // some row of the warp (bit nt); warp-uniform, 0 when none does.
   __device__ __forceinline__ unsigned ntmask(const BandPlan& P, const QWalk& w, int umin,
                                              int umax) const {
-    const int cl = max(0, umin + w.e - P.len[w.m] + 1 - w.vs), ch = min(kBR - 1, umax + w.e - w.vs);
+    const int cl = max(0, umin + w.e - P.len[w.m] + 1 - w.vs);
+    const int ch = min(kBR - 1, min(umax + w.e, Uc - 1) - w.vs);
     if (umin > umax || cl > ch) return 0u;
     return ((2u << (ch >> 3)) - 1u) & ~((1u << (cl >> 3)) - 1u);
   }
@@ -424,7 +429,8 @@ struct QTile {
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       lo[x] = uu[x] + w.e - len + 1 - w.vs;
-      hi[x] = uu[x] < Uc ? uu[x] + w.e - w.vs : -1;  // rows past the sequence take no key
+      // rows past the sequence take no key; keys past it do not exist
+      hi[x] = uu[x] < Uc ? min(uu[x] + w.e, Uc - 1) - w.vs : -1;
     }
   }
 };
@@ -448,13 +454,13 @@ __global__ void __launch_bounds__(kBThreads, 5)
     mbar_expect_tx(bar, kBStageB);
     tma_load_4d(st, &mk, 0, iw.rho, iw.vs, q.bg, bar);
     tma_load_4d(st + kBTileB, &mv, 0, iw.rho, iw.vs, q.bg, bar);
-    qwalk_next(P, q.r, q.u0, q.ul, iw);
+    qwalk_next(P, q.r, q.u0, q.ul, q.Uc, iw);
   };
   if (threadIdx.x == 0) {
     const uint32_t qb = smem_u32(&bars[kBStages]);
     mbar_expect_tx(qb, kBTileB);
     tma_load_4d(qtile, &mq, 0, q.r, q.u0, q.qplane, qb);
-    qwalk_seek(P, q.r, q.u0, q.ul, iw);
+    qwalk_seek(P, q.r, q.u0, q.ul, q.Uc, iw);
     for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
   }
   const float2* rope = static_cast<const float2*>(a.rope);
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(kBThreads, 5)
   for (int nd = 0; nd < 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.0f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
   QWalk cw{0, 0, 0, 0, 0};
-  qwalk_seek(P, q.r, q.u0, q.ul, cw);
+  qwalk_seek(P, q.r, q.u0, q.ul, q.Uc, cw);
 
   const bool ok = band_loop(NT, stages, bars, a, issue, [&](int, uint32_t kst) {
     // every warp computes the whole tile (skipping the n-tiles outside its
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(kBThreads, 5)
       const int rl = 8 * nb + (lane & 7);
       pv_tile(pa0, vst, rl, rl + 8, o);
       pv_tile(pa1, vst, rl + 16, rl + 16, o);  // keys 8 nb + 24 .. are not read (zero P)
-      qwalk_next(P, q.r, q.u0, q.ul, cw);
+      qwalk_next(P, q.r, q.u0, q.ul, q.Uc, cw);
       return;
     }
 #pragma unroll
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kBThreads, 5)
         pv_tile(pa, vst, rl, rl + 8, o);
       }
     }
-    qwalk_next(P, q.r, q.u0, q.ul, cw);
+    qwalk_next(P, q.r, q.u0, q.ul, q.Uc, cw);
   });
   if (!ok) return;
 
@@ -588,7 +594,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
     mbar_expect_tx(bar, kBStageB);
     tma_load_4d(st, &mk, 0, iw.rho, iw.vs, q.bg, bar);
     tma_load_4d(st + kBTileB, &mv, 0, iw.rho, iw.vs, q.bg, bar);
-    qwalk_next(P, q.r, q.u0, q.ul, iw);
+    qwalk_next(P, q.r, q.u0, q.ul, q.Uc, iw);
   };
   if (threadIdx.x == 0) {
     const uint32_t qb = smem_u32(&bars[kBStages]);
@@ -596,7 +602,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
     tma_load_4d(qtile, &mq, 0, q.r, q.u0, q.qplane, qb);
     tma_load_4d(dotile, &mdo, 0, q.r, q.u0, q.qplane, qb);
     tma_load_4d(otile, &mo, 0, q.r, q.u0, q.qplane, qb);
-    qwalk_seek(P, q.r, q.u0, q.ul, iw);
+    qwalk_seek(P, q.r, q.u0, q.ul, q.Uc, iw);
     for (int s = 0; s < kBStages && s < NT; ++s) issue(s);
   }
   float lse2[2];
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) kbar[nd][0] = kbar[nd][1] = kbar[nd][2] = kbar[nd][3] = 0.0f;
   QWalk cw{0, 0, 0, 0, 0};
-  qwalk_seek(P, q.r, q.u0, q.ul, cw);
+  qwalk_seek(P, q.r, q.u0, q.ul, q.Uc, cw);
   int umin, umax;
   q.warp_span(umin, umax);
 
@@ -709,7 +715,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
         pv_tile2(sa, pa, kst, rl, rl + 8, dq, kbar);
       }
     }
-    qwalk_next(P, q.r, q.u0, q.ul, cw);
+    qwalk_next(P, q.r, q.u0, q.ul, q.Uc, cw);
   });
   if (!ok) {
     if (threadIdx.x == 0) bulk_wait_read();
@@ -946,7 +952,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
   int NT = 0;
   {
     QWalk w{0, 0, 0, 0, 0};
-    if (qwalk_seek(P, r, u0, ul, w)) do ++NT; while (qwalk_next(P, r, u0, ul, w));
+    if (qwalk_seek(P, r, u0, ul, Uc, w)) do ++NT; while (qwalk_next(P, r, u0, ul, Uc, w));
   }
 
   pdl_launch_dependents();
@@ -974,13 +980,13 @@ __global__ void __launch_bounds__(kBThreads, 3)
     mbar_expect_tx(bar, kBStageB);
     tma_load_4d(sa, &mk, 0, iw.rho, iw.vs, bg, bar);
     tma_load_4d(sa + kBTileB, &mv, 0, iw.rho, iw.vs, bg, bar);
-    qwalk_next(P, r, u0, ul, iw);
+    qwalk_next(P, r, u0, ul, Uc, iw);
     ++n_issued;
   };
   if (tid == 0) {
     mbar_expect_tx(smem_u32(qbar), kUTileB);
     tma_load_4d(qtile, &mq, 0, r, u0, qplane, smem_u32(qbar));
-    qwalk_seek(P, r, u0, ul, iw);
+    qwalk_seek(P, r, u0, ul, Uc, iw);
     for (int st = 0; st < kUStages && st < NT; ++st) issue(st);
   }
   bool ok = true;
@@ -1023,7 +1029,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
   constexpr uint32_t idPV = idesc_bf16(kUR, 64, false, true);
   float m = -INFINITY, l = 0.0f;
   QWalk cw{0, 0, 0, 0, 0};
-  qwalk_seek(P, r, u0, ul, cw);
+  qwalk_seek(P, r, u0, ul, Uc, cw);
   // S_t = q~ . K'_t^T into TMEM columns 0..63 (thread 0).  S_{t+1} is issued
   // right after P_t . V_t: every thread holds S_t in registers by then, and
   // the tensor cores run both products while the threads go on.
@@ -1052,7 +1058,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
     // 16-column chunk no row of the warp reads is neither loaded nor
     // exponentiated (warp-uniform: the TMEM loads are warp-collective)
     const int len = P.len[cw.m];
-    const int lo = urow + cw.e - len + 1 - cw.vs, hi = live ? urow + cw.e - cw.vs : -1;
+    const int lo = urow + cw.e - len + 1 - cw.vs, hi = live ? min(urow + cw.e, Uc - 1) - cw.vs : -1;
     bool chunk[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) chunk[q] = __any_sync(0xffffffffu, lo <= 16 * q + 15 && hi >= 16 * q);
@@ -1133,7 +1139,7 @@ __global__ void __launch_bounds__(kBThreads, 3)
       last_pv = t;
       if (t + 1 < NT) issue_s(t + 1);
     }
-    qwalk_next(P, r, u0, ul, cw);
+    qwalk_next(P, r, u0, ul, Uc, cw);
   }
   if (ok && NT > 0) ok = mbar_wait_bounded(smem_u32(pvbar), (NT - 1) & 1, a.wait_cycles);
   ok = !__syncthreads_or(!ok);

@@ -222,15 +222,20 @@ int build_int_plan(const sfa_desc* d, Plan* p) {
 // set); a query tile of 64 / G positions then meets ceil((64 / G + len - 1) /
 // 64) key tiles of 64 rows per run.  The step with the fewest tiles wins
 // (the smallest on ties); the plan is used when at least one product in
-// eight is a wanted (query, key) pair, i.e. n >= 8 x tiles.  Distances >= T
-// reach no key and are left out.
-int band_plan_of(const int32_t* s, int n, int T, int G, BandPlan* p) {
+// eight is a wanted (query, key) pair, i.e. n >= 8 x tiles.  Distances with
+// |d| >= T reach no key and are left out.  Signed (bidirectional) sets are
+// runs like any other: a negative distance reads a later key, and the
+// kernels clip every band to the sequence at both ends.
+int band_plan_of(const int32_t* s0, int n, int T, int G, BandPlan* p) {
   p->delta = 0;
   p->nruns = 0;
   if (G != 1 && G != 2 && G != 4 && G != 8) return SFA_OK;
-  if (n <= 0 || s[0] != 0) return SFA_OK;  // signed sets, or no distance 0
-  int m = n;
-  while (m > 0 && s[m - 1] >= T) --m;
+  if (n <= 0 || !std::binary_search(s0, s0 + n, 0)) return SFA_OK;  // no distance 0
+  int first = 0, m = n;
+  while (first < n && s0[first] <= -T) ++first;
+  while (m > first && s0[m - 1] >= T) --m;
+  const int32_t* s = s0 + first;
+  m -= first;
   const int BU = 64 / G;
   int64_t best = -1;
   std::vector<int32_t> ra, rl, run_of((size_t)m);
@@ -241,7 +246,7 @@ int band_plan_of(const int32_t* s, int n, int T, int G, BandPlan* p) {
     for (int x = 0; x < m; ++x) {
       const int32_t prev = s[x] - delta;
       const int32_t* it = std::lower_bound(s, s + x, prev);
-      if (prev >= 0 && it != s + x && *it == prev) {
+      if (it != s + x && *it == prev) {
         run_of[(size_t)x] = run_of[(size_t)(it - s)];
         ++rl[(size_t)run_of[(size_t)x]];
       } else {

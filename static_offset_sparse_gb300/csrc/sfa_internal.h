@@ -122,8 +122,9 @@ struct LaunchTimer {
 // Host helpers (sfa_host.cpp).
 int build_interp_plan(const sfa_desc* d, Plan* p);
 int build_int_plan(const sfa_desc* d, Plan* p);
-// Band plan of a sorted, distinct, non-negative distance set for G query heads
-// per KV head; p->delta = 0 when the band kernels would not pay.
+// Band plan of a sorted, distinct distance set (negative distances: later
+// keys) for G query heads per KV head; p->delta = 0 when the band kernels
+// would not pay.
 int band_plan_of(const int32_t* s, int n, int T, int G, BandPlan* p);
 int build_band_plan(const sfa_desc* d, BandPlan* p);
 int validate_shape(const sfa_desc* d);

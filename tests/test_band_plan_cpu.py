@@ -1,7 +1,8 @@
 """Host logic of the band layout (sfa_band_plan): the runs it returns are
 arithmetic progressions of one step delta dividing T, and together they are
-exactly the distance set below T; the chosen delta minimises the tile count,
-and sets the band kernels would serve badly get no plan."""
+exactly the distances d with |d| < T (negative ones read later keys); the
+chosen delta minimises the tile count, and sets the band kernels would serve
+badly get no plan."""
 import itertools
 import random
 
@@ -24,7 +25,7 @@ def _tiles(runs, G):
 
 def _brute_best(dist, T, G):
     """Smallest tile count over every step <= 64 dividing T, by brute force."""
-    S = sorted(d for d in set(dist) if d < T)
+    S = sorted(d for d in set(dist) if -T < d < T)
     best = None
     for delta in range(1, 65):
         if T % delta or delta > T:
@@ -56,7 +57,7 @@ def _check_plan(sfa, dist, T, G):
     for a, n in runs:
         assert n >= 1
         covered += [a + delta * t for t in range(n)]
-    assert sorted(covered) == sorted(d for d in set(dist) if d < T)
+    assert sorted(covered) == sorted(d for d in set(dist) if -T < d < T)
     assert [a for a, _ in runs] == sorted(a for a, _ in runs)
     # maximal runs: a run's start has no predecessor in the set
     for a, _ in runs:
@@ -109,8 +110,20 @@ def test_no_plan_cases(sfa):
     assert sfa.band_plan(ch, 2047, 1) == (0, [])            # 8 does not divide T
     assert sfa.band_plan(ch, 2048, 16) == (0, [])           # G outside 1, 2, 4, 8
     assert sfa.band_plan(ch, 2048, 3) == (0, [])
-    assert sfa.band_plan([-3] + ch, 2048, 1) == (0, [])     # signed set
     assert sfa.band_plan(ch[1:], 2048, 1) == (0, [])        # no distance 0
+
+
+def test_signed_sets_are_runs(sfa):
+    """Bidirectional sets: the Christoffel offsets and their negatives are
+    three runs of step k / m; distances with |d| >= T are left out."""
+    ch = o.signed_christoffel_offsets(128, 1024)
+    assert sfa.band_plan(ch, 2048, 1) == (8, [(-1023, 128), (0, 1), (7, 128)])
+    assert sfa.band_plan(ch, 512, 1) == (8, [(-511, 64), (0, 1), (7, 64)])
+    assert sfa.band_plan(list(range(-40, 41)), 1024, 4) == (1, [(-40, 81)])
+    assert sfa.band_plan([-3] + o.christoffel_offsets(128, 1024, True), 2048, 1) == \
+        (8, [(-3, 1), (0, 1), (7, 128)])
+    for G in (1, 2, 4, 8):
+        _check_plan(sfa, ch, 2048, G)
 
 
 def test_capacity(sfa):
@@ -133,15 +146,16 @@ def test_random_sets_match_brute_force(sfa):
         G = rng.choice([1, 2, 4, 8])
         step = rng.choice([1, 2, 3, 4, 8])
         dist = {0}
+        signed = rng.random() < 0.4
         for _ in range(rng.randint(1, 4)):
-            a = rng.randrange(0, T)
+            a = rng.randrange(-T if signed else 0, T)
             n = rng.randint(1, 200)
             dist |= {a + step * t for t in range(n)}
-        dist |= set(rng.sample(range(T), rng.randint(0, 5)))
+        dist |= set(rng.sample(range(-T if signed else 0, T), rng.randint(0, 5)))
         dist = sorted(dist)
         delta, runs = _check_plan(sfa, dist, T, G)
         best = _brute_best(dist, T, G)
-        m = len([d for d in dist if d < T])
+        m = len([d for d in dist if -T < d < T])
         if delta:
             assert _tiles(runs, G) == best[0] and delta == best[1]
         else:
