@@ -130,8 +130,9 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
  * m | k: 0 and k/m - 1 + t k/m; a dense window: delta = 1) makes every
  * residue class of queries (mod delta) attend a contiguous band of keys of
  * one residue class per run: the band kernels run it as dense 64 x 64
- * tiles.  Distances are those of sfa_int_distances; distances >= T are left
- * out.  For each delta <= 64 dividing T the set is split into runs
+ * tiles.  Distances are those of sfa_int_distances; distances with |d| >= T
+ * are left out.  A negative distance (a later key of a signed set) is part of
+ * a run like any other.  For each delta <= 64 dividing T the set is split into runs
  * a + delta t, 0 <= t < len (ascending a); the delta with the fewest 64-key
  * tiles per query tile of 64 / G positions, sum over runs of
  * ceil((64 / G + len - 1) / 64), is kept (smallest delta on ties), and the
@@ -139,7 +140,7 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
  * Writes *delta (0: no band plan; the set runs the rung kernels for G = 4, 8
  * or 16, the SIMT kernels otherwise), *n_runs, and run_start / run_len (cap
  * entries; SFA_ERR_CAPACITY if more runs).  G must be 1, 2, 4 or 8 for a
- * plan; a set with a negative distance or without 0 has none. */
+ * plan; a set without 0 has none. */
 int sfa_band_plan(const int32_t* dist, int32_t n_dist, int32_t T, int32_t G, int32_t* delta,
                   int32_t* run_start, int32_t* run_len, int32_t cap, int32_t* n_runs);
 
@@ -230,10 +231,10 @@ int sfa_backward(const sfa_desc* d, const void* q, const void* k, const void* v,
  * offsets as an exact gather; "Christoffel-Balanced Sparse Attention": keys
  * i - o kept when >= 0).  Keys for query i: i - s for every s in d->dist
  * with 0 <= i - s < T.  A negative s reads the future row i + |s| (signed
- * offsets for bidirectional attention, same page); sets with negative
- * distances run the fp32 SIMT kernels.  bf16 sets with a band plan
- * (sfa_band_plan) run the band kernels, other bf16 sets with G = 4, 8 or 16 the
- * rung kernels.  Same outputs as sfa_forward / sfa_backward without the alpha
+ * offsets for bidirectional attention, same page).  bf16 sets with a band plan
+ * (sfa_band_plan; signed sets included) run the band kernels, other bf16 sets
+ * without negative distances and with G = 4, 8 or 16 the rung kernels, every
+ * other set the fp32 SIMT kernels.  Same outputs as sfa_forward / sfa_backward without the alpha
  * gradient. */
 int sfa_forward_int(const sfa_desc* d, const void* q, const void* k, const void* v, void* o,
                     float* lse, void* ws, size_t ws_bytes, void* stream);
