@@ -78,7 +78,7 @@ typedef struct {
   /* Optional device [B, Hkv, T, 64] bf16: the rotated keys sfa_rope_keys wrote
    * for this k and this rope table, or NULL.  Calls that run the tensor-core
    * kernels (bf16 I/O: the rung kernels for G = 4, 8, 16 and the band kernels,
-   * no negative distance) then read it instead of
+   * signed band sets included) then read it instead of
    * rotating K into their workspace (which shrinks accordingly), so one
    * rotation serves a layer's forward and backward.  Ignored otherwise. */
   const void* k_rot;
