@@ -135,8 +135,11 @@ int sfa_int_distances(const int32_t* dist, int32_t n_dist, int32_t* out, int32_t
  * a run like any other.  For each delta <= 64 dividing T the set is split into runs
  * a + delta t, 0 <= t < len (ascending a); the delta with the fewest 64-key
  * tiles per query tile of 64 / G positions, sum over runs of
- * ceil((64 / G + len - 1) / 64), is kept (smallest delta on ties), and the
- * plan is used when the distance count is at least 8 times that tile count.
+ * ceil((64 / G + len - 1) / 64), is kept (smallest delta on ties).  Where the
+ * rung kernels could take the set (G = 4 or 8, no negative distance) the plan
+ * is used when the distance count is at least 8 times that tile count; for
+ * G = 1 or 2 and for signed sets (whose alternative is the SIMT path) any
+ * plan is used.
  * Writes *delta (0: no band plan; the set runs the rung kernels for G = 4, 8
  * or 16, the SIMT kernels otherwise), *n_runs, and run_start / run_len (cap
  * entries; SFA_ERR_CAPACITY if more runs).  G must be 1, 2, 4 or 8 for a

@@ -221,11 +221,15 @@ int build_int_plan(const sfa_desc* d, Plan* p) {
 // of step delta (a distance extends the run of s - delta when that is in the
 // set); a query tile of 64 / G positions then meets ceil((64 / G + len - 1) /
 // 64) key tiles of 64 rows per run.  The step with the fewest tiles wins
-// (the smallest on ties); the plan is used when at least one product in
-// eight is a wanted (query, key) pair, i.e. n >= 8 x tiles.  Distances with
-// |d| >= T reach no key and are left out.  Signed (bidirectional) sets are
-// runs like any other: a negative distance reads a later key, and the
-// kernels clip every band to the sequence at both ends.
+// (the smallest on ties).  Where the rung kernels could take the set (G = 4
+// or 8, no negative distance) the plan is used when at least one product in
+// eight is a wanted (query, key) pair, i.e. n >= 8 x tiles; elsewhere the
+// alternative is the fp32 SIMT path, which every plan beats (measured down to
+// the Fibonacci set at G = 1, 19 distances in 12 tiles: 0.38 against 0.75 ms),
+// so any plan is used.  Distances with |d| >= T reach no key and are left
+// out.  Signed (bidirectional) sets are runs like any other: a negative
+// distance reads a later key, and the kernels clip every band to the
+// sequence at both ends.
 int band_plan_of(const int32_t* s0, int n, int T, int G, BandPlan* p) {
   p->delta = 0;
   p->nruns = 0;
@@ -266,7 +270,8 @@ int band_plan_of(const int32_t* s0, int n, int T, int G, BandPlan* p) {
       std::copy(rl.begin(), rl.end(), p->len);
     }
   }
-  if (best < 0 || (int64_t)m < 8 * best) {
+  const bool rung_ok = (G == 4 || G == 8) && s0[0] >= 0;
+  if (best < 0 || (rung_ok && (int64_t)m < 8 * best)) {
     p->delta = 0;
     p->nruns = 0;
   }

@@ -1,8 +1,10 @@
 """Host logic of the band layout (sfa_band_plan): the runs it returns are
 arithmetic progressions of one step delta dividing T, and together they are
 exactly the distances d with |d| < T (negative ones read later keys); the
-chosen delta minimises the tile count, and sets the band kernels would serve
-badly get no plan."""
+chosen delta minimises the tile count.  Where the rung kernels could take the
+set (G = 4 or 8, no negative distance), sets the band kernels would serve
+badly (fewer than 8 distances per tile) get no plan; elsewhere every plan is
+used (the alternative is the SIMT path)."""
 import itertools
 import random
 
@@ -47,6 +49,10 @@ def _brute_best(dist, T, G):
     return best
 
 
+def _rung_ok(dist, G):
+    return G in (4, 8) and min(dist) >= 0
+
+
 def _check_plan(sfa, dist, T, G):
     delta, runs = sfa.band_plan(dist, T, G)
     if delta == 0:
@@ -76,9 +82,9 @@ def test_christoffel_is_one_run(sfa, m, k, G):
         assert delta == k // m
         assert runs == [(0, 1), (k // m - 1, m)]
         assert _tiles(runs, G) == want[0]
-        assert len(set(dist)) >= 8 * want[0]
+        assert len(set(dist)) >= 8 * want[0] or not _rung_ok(dist, G)
     else:
-        assert len(set(dist)) < 8 * want[0]
+        assert _rung_ok(dist, G) and len(set(dist)) < 8 * want[0]
 
 
 def test_config5_plan(sfa):
@@ -98,16 +104,23 @@ def test_full_causal_and_distances_past_T(sfa):
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_fibonacci_and_pow2_get_no_plan(sfa, G):
+def test_fibonacci_and_pow2(sfa, G):
+    """Singleton rungs: no plan where the rung kernels take the set (G = 4, 8);
+    at G = 1, 2 the plan of step 1 (window run + singletons) beats SIMT."""
     fib = sorted(set(range(9)) | set(sfa.offsets_fib(15)))
-    pow2 = [0] + list(range(1, 9)) + sfa.offsets_pow2(11)
-    assert sfa.band_plan(fib, 1024, G) == (0, [])
-    assert sfa.band_plan(pow2, 1024, G) == (0, [])
+    pow2 = sorted(set(range(9)) | set(sfa.offsets_pow2(11)))
+    for dist in (fib, pow2):
+        delta, runs = _check_plan(sfa, dist, 1024, G)
+        if G in (4, 8):
+            assert (delta, runs) == (0, [])
+        else:
+            assert delta == 1 and runs[0] == (0, 9)
 
 
 def test_no_plan_cases(sfa):
     ch = o.christoffel_offsets(128, 1024, include_zero=True)
-    assert sfa.band_plan(ch, 2047, 1) == (0, [])            # 8 does not divide T
+    assert sfa.band_plan(ch, 2047, 4) == (0, [])            # 8 does not divide T
+    assert _check_plan(sfa, ch, 2047, 1)[0] in (1, 23)       # G = 1: another step
     assert sfa.band_plan(ch, 2048, 16) == (0, [])           # G outside 1, 2, 4, 8
     assert sfa.band_plan(ch, 2048, 3) == (0, [])
     assert sfa.band_plan(ch[1:], 2048, 1) == (0, [])        # no distance 0
@@ -158,8 +171,10 @@ def test_random_sets_match_brute_force(sfa):
         m = len([d for d in dist if -T < d < T])
         if delta:
             assert _tiles(runs, G) == best[0] and delta == best[1]
-        else:
+        elif _rung_ok(dist, G):
             assert best is None or m < 8 * best[0]
+        else:
+            assert best is None
 
 
 def test_plan_is_order_and_duplicate_free(sfa):

@@ -1,7 +1,8 @@
 """The bounds-checked build of the SIMT kernels (libsfa_debug.so) on the GPU.
 
-libsfa_debug.so is libsfa.so with the SIMT kernels (fp32 I/O, signed
-distance sets, one or two query heads per KV head without a band plan)
+libsfa_debug.so is libsfa.so with the SIMT kernels (fp32 I/O, and bf16
+calls with one or two query heads per KV head or signed sets that have no
+band plan)
 compiled with SFA_DEBUG_BOUNDS: every row index they form, into the sequence
 and into their shared-memory slabs, is range-checked; a bad one is recorded
 as SFA_ERR_DEVICE_BOUNDS and its access skipped, with no trap.  These cases
@@ -38,7 +39,7 @@ CASES = [  # B, T, Hq, Hkv, dtype, kind
     (1, 150, 8, 2, "f32", "interp"),    # fp32 I/O: SIMT, G = 4
     (2, 97, 2, 1, "bf16", "interp"),    # G = 2 bf16: SIMT
     (1, 70, 16, 1, "f32", "int"),       # G = 16 fp32
-    (2, 90, 4, 4, "bf16", "signed"),    # signed (bidirectional) set: SIMT
+    (2, 90, 4, 4, "f32", "signed"),     # signed (bidirectional) set, fp32: SIMT
 ]
 
 
