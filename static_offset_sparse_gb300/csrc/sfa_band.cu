@@ -129,7 +129,7 @@ __device__ __forceinline__ void band_rope_pairs(const float2* rope, const int* p
 // band_rope_pairs (none if rp is nullptr), scaled and repacked.
 __device__ __forceinline__ void band_frags(uint32_t tile, int row0, const float4 (*rp)[4],
                                            float scale, bool transform, uint32_t (*qa)[4]) {
-  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
     ldsm_x4(tile + swz(row0 + (lane & 15), 2 * kk + (lane >> 4)), qa[kk][0], qa[kk][1], qa[kk][2],
