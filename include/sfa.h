@@ -17,7 +17,9 @@
  *  - Tensors are contiguous [B, H, T, D] with D fastest; D must be 64.
  *    q, o, dO, dq: H = Hq.  k, v, dk, dv: H = Hkv.  Hq % Hkv == 0 and the
  *    group size G = Hq / Hkv is a power of two <= 32; query head h reads KV
- *    head h / G.  lse and delta are fp32 [B, Hq, T].
+ *    head h / G.  lse and delta are fp32 [B, Hq, T].  Sizes: 1 <= T <= 2^24,
+ *    B * Hkv <= 65535, and for calls that run the rung kernels (bf16, G = 8
+ *    or 16) B * Hq / 4 <= 65535; larger shapes return SFA_ERR_UNSUPPORTED.
  *  - All tensor pointers are device pointers, owned by the caller, 16-byte
  *    aligned.  Host arrays (base offsets, distance lists, outputs of the
  *    host builders) are read or written during the call and not retained.

@@ -199,7 +199,12 @@ static int plan_call(const sfa_desc* d, int interp, Plan* p, BandPlan* bp) {
       return SFA_OK;
     }
   }
-  return interp ? build_interp_plan(d, p) : build_int_plan(d, p);
+  const int rc = interp ? build_interp_plan(d, p) : build_int_plan(d, p);
+  if (rc != SFA_OK) return rc;
+  // the rung kernels give each group of four query heads a grid row: B Hq / 4
+  // rows (B Hkv for G <= 4, which the shape check bounds; more for G = 8, 16)
+  if (tc_path(d, *p) && (int64_t)d->B * (d->Hq / 4) > 65535) return SFA_ERR_UNSUPPORTED;
+  return SFA_OK;
 }
 
 // Rotated keys for the tensor-core kernels: the caller's k_rot, the raw keys

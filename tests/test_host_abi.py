@@ -147,6 +147,12 @@ def test_empty_and_oversized_shapes_are_rejected_on_the_host(sfa_lib):
         d = desc(**kw)
         assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 2, kw
         assert sfa_lib.sfa_forward(C.byref(d), null, null, null, null, null, null, 0, null) == 2, kw
+    # G = 8 on the rung kernels: one grid row per group of four query heads, so
+    # B Hq / 4 <= 65535 (B Hkv alone would allow twice as many sequences)
+    for B, rc in ((16383, 0), (16384, 2)):
+        d = desc(B=B, T=16, Hq=16, Hkv=2)
+        assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == rc, B
+        assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 0, C.byref(size)) == rc, B
     d = desc(B=1, T=1 << 24)
     assert sfa_lib.sfa_workspace_size(C.byref(d), 1, 1, C.byref(size)) == 0
     assert size.value > (1 << 24) * 8 * 8  # at least the per-query records of the key side
