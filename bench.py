@@ -799,6 +799,9 @@ def configs_arm(args, dev):
     def int_set(alpha, W):
         return sorted(set(range(W + 1)) | {round(alpha * f) for f in FIB})
 
+    def int_set_p2():  # window 0..8 and the powers of two (alpha = 1: exact rows)
+        return sorted(set(range(9)) | set(pow2))
+
     def chris():
         S = sfa.offsets_christoffel(128, 1024, True)
         return S
@@ -811,6 +814,7 @@ def configs_arm(args, dev):
         ("1: fp32 interp, alpha=1", 1, 1024, 8, 2, "f32", "interp", (FIB, 1.0, 8), True),
         ("2: bf16 interp, one layer, alpha=0.9667", 32, 1024, 8, 2, "bf16", "interp", (FIB, 0.5 + 7 / 15, 8), True),
         ("3: bf16 pow2 K=11, alpha=1", 32, 1024, 8, 2, "bf16", "interp", (pow2, 1.0, 8), True),
+        ("3: bf16 pow2 K=11, alpha=1, integer path", 32, 1024, 8, 2, "bf16", "int", (int_set_p2(),), True),
         ("4: bf16 integer forward, T=2048, alpha=1", 4, 2048, 8, 2, "bf16", "int", (int_set(1.0, 8),), False),
         ("4: bf16 integer forward, T=16384, alpha=1.5", 4, 16384, 8, 2, "bf16", "int", (int_set(1.5, 8),), False),
         ("5: bf16 Christoffel 128/1024, 4/4 heads", 16, 2048, 4, 4, "bf16", "int", (chris(),), True),

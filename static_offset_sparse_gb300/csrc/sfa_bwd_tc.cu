@@ -564,14 +564,18 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
     } else {
       // rung: query qw + ql reaches key j as role 1 (key i - c + 1) when
       // ql + rel = 0 and as role 0 (key i - c) when ql + rel = 1, and only if
-      // it reads the rung at all (qw + ql >= c); record (qoff + ql) * 2 + role
-      const int c = P.c[grp - nwc], qoff = min(8 * kw, kKvQR - 12), qw = qb_of(grp) + qoff;
+      // it reads the rung at all (qw + ql >= c); record (qoff + ql) * 2 + role.
+      // An integer rung (w = 0) has no role 1: a warp's 8 keys then read 8
+      // queries, 8 kw + 1 .. 8 kw + 8 of the slab, two k-steps instead of three
+      constexpr int RKS = INTERP ? 3 : 2;
+      const int c = P.c[grp - nwc];
+      const int qoff = INTERP ? min(8 * kw, kKvQR - 12) : 8 * kw + 1, qw = qb_of(grp) + qoff;
       const int rel = qw - j - c + 1;
       const uint32_t mask =
-          j < T ? ql_mask(max(-rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
+          j < T ? ql_mask(max(INTERP ? -rel : 1 - rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<3, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
-                                   corr, dk, dv);
+      kv_group<RKS, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
+                                     corr, dk, dv);
     }
     __syncthreads();
     if (tid == 0 && gt + kKvStages < NGt) issue(gt + kKvStages, qst, smem_u32(&bars[st]));
