@@ -185,6 +185,29 @@ __global__ void __launch_bounds__(kTcThreads, 4)
       sa[2] = pack_bf16(ds[0][2], ds[0][3]);
       sa[3] = pack_bf16(ds[1][2], ds[1][3]);
       pv_tile(sa, kst, 4 * warp + (lane & 7), 4 * warp + 8 + (lane & 7), dq);
+    } else if (!INTERP) {
+      // integer rung pair (w = 0): one tile per product, column (rung x,
+      // position p') = raw row 4w + p' of box x (the forward's layout); the
+      // lane of this row's position p holds rung tig >> 1 at column p & 1 when
+      // tig & 1 == p >> 1.  Role 0 only: the key side reads no role 1
+      const int r0 = 2 * (grp - nwc), rg = r0 + (tig >> 1), e = p & 1;
+      float sc[4] = {0, 0, 0, 0}, dpv[4] = {0, 0, 0, 0};
+      qk_tile(qa, kst, int_pair_row(warp), sc);
+      qk_tile(da, vst, int_pair_row(warp), dpv);
+      const bool v = act && (tig & 1) == (p >> 1) && rg < nr && i >= P.c[min(rg, P.n - 1)];
+      float ds[2], prr[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float a0 = e ? sc[2 * r + 1] : sc[2 * r], b0 = e ? dpv[2 * r + 1] : dpv[2 * r];
+        const float pr = v ? ex2(fmaf(a0, kLog2e, -lse2[r])) : 0.0f;
+        ds[r] = pr * (b0 - delta[r]);
+        prr[r] = pr;
+        if (PSI) psi[r] = fmaf(pr, b0, psi[r]);
+      }
+      if (v) write_coef_half(crow + 2 * (P.W + 1 + 2 * rg), 1.0f, ds[0], ds[1], prr[0], prr[1]);
+      const uint32_t sk8[2] = {pack_bf16(e ? 0.0f : ds[0], e ? ds[0] : 0.0f),
+                               pack_bf16(e ? 0.0f : ds[1], e ? ds[1] : 0.0f)};
+      pv_tile_k8(sk8, kst, int_pair_row(warp), dq);
     } else {
       // rung pair; box 1's B columns rotate positions by two, so the lane of
       // position p holding a rung's raw pair is tig == p (box 0) or
@@ -219,7 +242,8 @@ __global__ void __launch_bounds__(kTcThreads, 4)
       }
       if (v) {  // role 0: key i - c (weight 1 - w); role 1: key i - c + 1 (weight w)
         write_coef_half(crow + 2 * (P.W + 1 + 2 * rg), 1.0f - w, ds[0], ds[1], prr[0], prr[1]);
-        write_coef_half(crow + 2 * (P.W + 2 + 2 * rg), w, ds[0], ds[1], prr[0], prr[1]);
+        if (INTERP)  // an integer rung has no role 1 (w = 0); the key side does not read it
+          write_coef_half(crow + 2 * (P.W + 2 + 2 * rg), w, ds[0], ds[1], prr[0], prr[1]);
       }
       const uint32_t lo = pack_bf16(ds[0] * (1.0f - w), ds[0] * w);
       const uint32_t hi = pack_bf16(ds[1] * (1.0f - w), ds[1] * w);

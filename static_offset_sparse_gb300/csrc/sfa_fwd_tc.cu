@@ -195,6 +195,21 @@ __global__ void __launch_bounds__(kTcThreads, 5)
       pa[2] = pack_bf16(s[0][2], s[0][3]);
       pa[3] = pack_bf16(s[1][2], s[1][3]);
       pv_tile(pa, vst, 4 * warp + (lane & 7), 4 * warp + 8 + (lane & 7), o);
+    } else if (!INTERP) {
+      // integer rung pair: one tile, column (rung x, position p') = raw row
+      // 4w + p' of box x; the lane of this row's position p holds rung
+      // x = tig >> 1 at column e = p & 1 when tig & 1 == p >> 1
+      const int r0 = 2 * (grp - nwc), rg = r0 + (tig >> 1), e = p & 1;
+      float acc[4] = {0, 0, 0, 0};
+      qk_tile(qa, kst, int_pair_row(warp), acc);
+      const bool v = (tig & 1) == (p >> 1) && rg < nr && i >= P.c[min(rg, P.n - 1)];
+      float s[2][4];
+      s[0][0] = v ? (e ? acc[1] : acc[0]) * kLog2e : -INFINITY;
+      s[1][0] = v ? (e ? acc[3] : acc[2]) * kLog2e : -INFINITY;
+      softmax_step(s, std::integral_constant<int, 1>());
+      const uint32_t pk8[2] = {pack_bf16(e ? 0.0f : s[0][0], e ? s[0][0] : 0.0f),
+                               pack_bf16(e ? 0.0f : s[1][0], e ? s[1][0] : 0.0f)};
+      pv_tile_k8(pk8, vst, int_pair_row(warp), o);
     } else {
       // rung pair: box x, B column n = 2 p' + e' is row 4w + p' + e'
       const int r0 = 2 * (grp - nwc);

@@ -42,6 +42,16 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d += a * b for k = 8 (m16n8k8): a0 (row gid, k 2tig..2tig+1), a1 (row
+// gid+8, same k), b0 (k 2tig..2tig+1, n gid).
+__device__ __forceinline__ void mma_bf16_k8(float* d, const uint32_t* a, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(b0));
+}
+
 // 2^x with the hardware approximation (ex2.approx.ftz; 2^-inf = +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;

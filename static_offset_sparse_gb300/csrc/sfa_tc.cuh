@@ -67,6 +67,31 @@ __device__ __forceinline__ void pv_tile(const uint32_t* pa, uint32_t region, int
   }
 }
 
+// Integer rung pairs (w = 0: one row per position and rung): the 8 B columns
+// of one tile are (rung x, position p) = (n >> 2, n & 3), raw row 4w + p of
+// box x, so one product serves both rungs; the lane of position p's row holds
+// rung tig >> 1 at column 2 tig + (p & 1) when tig & 1 == p >> 1.
+__device__ __forceinline__ int int_pair_row(int warp) {
+  const int n = threadIdx.x & 7;
+  return (n >> 2) * kTcBoxRows + 4 * warp + (n & 3);
+}
+
+// O[16 x 64] += P[16 x 8] . V[8 keys x 64] (k = 8): P in the C-fragment
+// positions of an integer rung pair's tile, V rows as int_pair_row gives them.
+__device__ __forceinline__ void pv_tile_k8(const uint32_t* pa, uint32_t region, int row,
+                                           float (*o)[4]) {
+  const int mi = (threadIdx.x & 31) >> 3;
+#pragma unroll
+  for (int nd = 0; nd < 8; nd += 4) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(region + swz(row, nd + mi), b0, b1, b2, b3);
+    mma_bf16_k8(o[nd], pa, b0);
+    mma_bf16_k8(o[nd + 1], pa, b1);
+    mma_bf16_k8(o[nd + 2], pa, b2);
+    mma_bf16_k8(o[nd + 3], pa, b3);
+  }
+}
+
 // Issue the TMA loads of group `grp` (a window chunk, then rung pairs) into
 // a stage (thread 0 only).  An unpaired rung reloads its partner's slab: its
 // probabilities are zero, and the rows stay finite.
