@@ -168,3 +168,16 @@ def test_signed_band_forward_both_kernels(sfa, sfa_lib):
             assert np.abs(_f64(L) - Lw).max() <= 2e-2
     finally:
         assert sfa_lib.sfa_set_option(0, 0) == 0
+
+
+def test_signed_long_sequence_sampled(sfa):
+    """T = 8192 (128 key tiles per class at step 8): the signed Christoffel
+    128/1024 set, one (batch, KV head) unit against the oracle, G = 4."""
+    import torch
+
+    dist = o.signed_christoffel_offsets(128, 1024)
+    x = si.make_qkvdo(1, 8192, 8, 2, 64, "bf16", seed=3600)
+    O, L, g = _run(sfa, x, dist)
+    _compare(x, O, L, g, dist, rows=[(0, 1)])
+    for t in (O, *g):
+        assert torch.isfinite(t).all()
