@@ -104,6 +104,18 @@ def test_config3_pow2(sfa, alpha):
     _sampled(sfa, x, [(5, 1), (30, 0)], slots, 1e4, fwd, bwd, True)
 
 
+def test_config3_integer_path(sfa):
+    """Config 3 at alpha = 1 through the integer path (window 0..8 and the
+    powers of two as exact one-row gathers: the rung kernels' integer pairs,
+    one tile per pair, and the two-k-step key side); sampled units."""
+    dist = sorted(set(range(9)) | set(o.pow2_offsets(11)))
+    x = si.make_qkvdo(32, 1024, 8, 2, 64, "bf16", seed=si.mix_seed(0, 33), layer=3)
+    fwd = lambda d: sfa.forward_int(d["q"], d["k"], d["v"], dist=dist)
+    bwd = lambda d, O, L: sfa.backward_int(d["q"], d["k"], d["v"], O, L, d["do"], dist=dist)
+    assert sfa.band_plan(dist, 1024, 4)[0] == 0  # the rung kernels, not the band ones
+    _sampled(sfa, x, [(2, 0), (31, 1)], o.dist_slots(dist), 1e4, fwd, bwd, True)
+
+
 @pytest.mark.parametrize("T,alpha", [(2048, 0.5), (4096, 1.0), (8192, 1.0), (16384, 1.5)])
 def test_config4_int_forward_long(sfa, T, alpha):
     dist = o.int_distances(FIB, alpha, 8)
