@@ -353,14 +353,16 @@ def gpu_arm(args, rank, world, dev):
     return layers, ms, clk, launches, roofline
 
 
-def e2e_arm(layers, steps, world, dev):
+def e2e_arm(layers, steps, warmup, world, dev):
     """Same step through the C ABI with host buffers: every step copies each
     layer's Q, K, V, dO from pinned host memory and reads dQ, dK, dV and
     (dalpha, dtheta) back, inside the timed region.  Copies and compute run
     on three streams (host to device, compute, device to host) ordered by
     per-layer events, so one layer's copies overlap another layer's kernels;
     a layer's buffers are refilled only after its previous outputs were read
-    back, and recomputed only after its inputs arrived."""
+    back, and recomputed only after its inputs arrived.  The host's own time
+    to issue a step (copies, events and the C-ABI calls) is reported beside
+    it: when it exceeds the link's time, the host bounds the step."""
     import ctypes as C
     import torch
     import torch.distributed as dist
@@ -399,13 +401,15 @@ def e2e_arm(layers, steps, world, dev):
                 ev_out[l].record(s_out)
         first[0] = False
 
-    step()
+    for _ in range(warmup):
+        step()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(steps):
         step()
+    t_issue = (time.perf_counter() - t0) / steps
     torch.cuda.synchronize()
     el = (time.perf_counter() - t0) / steps
     # the same copies with the kernels left out: the host link's own time for
@@ -416,16 +420,22 @@ def e2e_arm(layers, steps, world, dev):
     torch.cuda.synchronize()
     el_copy = (time.perf_counter() - t0) / 3
     if world > 1:
-        t = torch.tensor([el, el_copy], dtype=torch.float64, device=dev)
+        t = torch.tensor([el, el_copy, t_issue], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el, el_copy = float(t[0].item()), float(t[1].item())
+        el, el_copy, t_issue = float(t[0].item()), float(t[1].item()), float(t[2].item())
+    # what the step waits for: the link (within 10% of the copies alone), the
+    # host issuing the work (within 10% of its issue time), or neither
+    bound = ("host link" if el <= 1.1 * el_copy else
+             "host issue" if el <= 1.1 * t_issue else "unexplained: neither link nor issue")
     return {"value": round(world * B * T / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(el * 1e3, 3), "steps": steps,
             "copies_only_ms_per_step": round(el_copy * 1e3, 3),
+            "host_issue_ms_per_step": round(t_issue * 1e3, 3),
             "host_link_gbs": round((h2d + d2h) / el_copy / 1e9, 1),
-            "overlap": "host-to-device, compute and device-to-host streams, per-layer events; "
-                       "bound by the host link (copies_only_ms_per_step: the same copies "
-                       "without the kernels)"}
+            "bound": bound,
+            "overlap": "host-to-device, compute and device-to-host streams, per-layer events "
+                       "(copies_only_ms_per_step: the same copies without the kernels; "
+                       "host_issue_ms_per_step: the host's time to issue a step)"}
 
 
 def oracle_step_sample(schedule: str, W: int, nb: int, layer: int):
@@ -1024,7 +1034,7 @@ def main():
                    "frac": round(hbm / peak, 4)},
            "gpu_launches": launches, "clocks": clk}
     if not args.no_e2e:
-        out["e2e"] = e2e_arm(layers, min(args.steps, 10), world, dev)
+        out["e2e"] = e2e_arm(layers, min(args.steps, 20), args.warmup, world, dev)
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         out["cpu_baseline"] = cpu_baseline(args.schedule, args.W, args.cpu_budget)
     if rank == 0:
