@@ -90,16 +90,17 @@ def layer_ids():
     return list(range(SCHED_L)) if LAYERS == SCHED_L else [(7 + j) % SCHED_L for j in range(LAYERS)]
 
 
-def pair_counts(alpha: float, W: int):
+def pair_counts(alpha: float, W: int, base=None):
     """(query, key) pairs per (b, query head) and how many are rung pairs.
 
     Counts the plain definition: window keys min(W, i) + 1 and a rung with
-    ceil(alpha f) = c and alpha f > W reaching queries i >= c."""
+    ceil(alpha f) = c and alpha f > W reaching queries i >= c (f over the base
+    list, Fibonacci by default)."""
     import math
 
     win = sum(min(W, i) + 1 for i in range(T))
     rung = 0
-    for f in FIB:
+    for f in (FIB if base is None else base):
         d = alpha * f
         if d <= W:
             continue
@@ -206,7 +207,7 @@ def kernel_traffic(kind: str):
 class Layer:
     """One layer's device tensors and its prebuilt C-ABI descriptor."""
 
-    def __init__(self, sfa, lib, x, alpha, W, dev):
+    def __init__(self, sfa, lib, x, alpha, W, dev, base=None):
         import ctypes as C
         import torch
 
@@ -221,7 +222,8 @@ class Layer:
         # the layer's rotated keys: one rotation per step serves forward and
         # backward (kept like a saved activation)
         self.k_rot = torch.empty_like(x["k"])
-        self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha, base=FIB, rope_theta=ROPE,
+        self.desc = sfa.make_desc(x["q"], x["k"], W=W, alpha=alpha,
+                                  base=FIB if base is None else base, rope_theta=ROPE,
                                   k_rot=self.k_rot)
         self.nws = max(1, sfa.workspace_size(self.desc, True, True),
                        sfa.workspace_size(self.desc, True, False))
@@ -899,12 +901,13 @@ def configs_arm(args, dev):
     return out
 
 
-def grid_arm(args, dev):
+def grid_arm(args, dev, staggered_pow2=False):
     """The 16-layer step of the interpolated configuration over its whole grid:
-    W in {6, 8, 10, 12} x {linear, coprime} alpha schedules.  Each point builds
-    its 16 layers (own seeded inputs, rotated keys once per layer), captures
-    the step as one CUDA graph and times K replays with CUDA events after the
-    warm-ups; one JSON object per point."""
+    W in {6, 8, 10, 12} x {linear, coprime} alpha schedules (staggered_pow2:
+    the power-of-two base list K = 11 instead, W = 8, both schedules).  Each
+    point builds its 16 layers (own seeded inputs, rotated keys once per
+    layer), captures the step as one CUDA graph and times K replays with CUDA
+    events after the warm-ups; one JSON object per point."""
     import ctypes as C
     import torch
 
@@ -915,11 +918,12 @@ def grid_arm(args, dev):
     lib = _lib()
     peak, src = hbm_peak()
     out = []
+    base = [1 << j for j in range(11)] if staggered_pow2 else None
     for schedule in ("linear", "coprime"):
         al = alphas(schedule)
-        for W in (6, 8, 10, 12):
+        for W in ((8,) if staggered_pow2 else (6, 8, 10, 12)):
             layers = [Layer(sfa, lib, si.make_qkvdo_device(B, T, HQ, HKV, D, "bf16", rank_seed(0), dev,
-                                                           layer=l), al[l], W, dev)
+                                                           layer=l), al[l], W, dev, base)
                       for l in layer_ids()]
             stream = torch.cuda.current_stream()
             sp = C.c_void_p(stream.cuda_stream)
@@ -945,8 +949,10 @@ def grid_arm(args, dev):
             assert sfa.get_device_status() == 0
             ms = ev0.elapsed_time(ev1) / n
             hbm = UNIQUE_BYTES_PER_TOKEN * B * T * len(layers) / (ms * 1e-3) / 1e9
-            keys = sum(pair_counts(L.alpha, W)[0] for L in layers) / len(layers) / T
-            out.append({"config": f"2 grid: {schedule}, W={W}", "B": B, "T": T, "heads": f"{HQ}/{HKV}",
+            keys = sum(pair_counts(L.alpha, W, base)[0] for L in layers) / len(layers) / T
+            name = (f"3 staggered: pow2 K=11, {schedule}, W={W}" if staggered_pow2
+                    else f"2 grid: {schedule}, W={W}")
+            out.append({"config": name, "B": B, "T": T, "heads": f"{HQ}/{HKV}",
                         "layers": len(layers), "dtype": "bf16", "direction": "fwd+bwd+dtheta",
                         "ms_per_step": round(ms, 4), "tokens_per_s": round(B * T / (ms * 1e-3), 1),
                         "hbm_frac": round(hbm / peak, 4), "hbm_peak_source": src,
@@ -976,7 +982,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
     ap.add_argument("--only", default="", help="configs mode: run the configurations whose name "
-                    "starts with this (e.g. '5:'; '2 grid' runs only the W x schedule grid)")
+                    "starts with this (e.g. '5:'; '2 grid' runs only the W x schedule grid, '3 staggered' "
+                    "only the 16-layer power-of-two step)")
     ap.add_argument("--mode", default="train", choices=["train", "decode", "configs"],
                     help="train: the fwd+bwd step (default); decode: one token per sequence; "
                          "configs: one line per configuration of the pages")
@@ -1016,7 +1023,10 @@ def main():
             if not args.only or args.only.startswith("2 grid"):
                 for line in grid_arm(args, dev):
                     print(json.dumps(line), flush=True)
-            if args.only != "2 grid":
+            if not args.only or args.only.startswith("3 staggered"):
+                for line in grid_arm(args, dev, staggered_pow2=True):
+                    print(json.dumps(line), flush=True)
+            if args.only not in ("2 grid", "3 staggered"):
                 for line in configs_arm(args, dev):
                     print(json.dumps(line), flush=True)
         return
