@@ -841,8 +841,14 @@ def configs_arm(args, dev):
     # selected with --only "2 rung sweep", not part of the default list
     sweep = [(f"2 rung sweep: {max(n - 5, 0)} rungs", 32, 1024, 8, 2, "bf16", "interp",
               (FIB[:n], 0.97, 8), True) for n in (5, 6, 8, 10, 12, 15)]
+    # config 4 over its whole grid: the integer forward at T in {2k, 4k, 8k, 16k}
+    # and alpha in {0.5, 1, 1.5} (rounded offsets, W = 8); selected with --only "4 grid"
+    grid4 = [(f"4 grid: T={Tg}, alpha={ag}", 4, Tg, 8, 2, "bf16", "int", (int_set(ag, 8),), False)
+             for Tg in (2048, 4096, 8192, 16384) for ag in (0.5, 1.0, 1.5)]
     if args.only and args.only.startswith("2 rung sweep"):
         cases = sweep
+    elif args.only and args.only.startswith("4 grid"):
+        cases = grid4
     elif args.only:
         cases = [c for c in cases if c[0].startswith(args.only)]
     out = []
@@ -983,7 +989,7 @@ def main():
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
     ap.add_argument("--only", default="", help="configs mode: run the configurations whose name "
                     "starts with this (e.g. '5:'; '2 grid' runs only the W x schedule grid, '3 staggered' "
-                    "only the 16-layer power-of-two step)")
+                    "only the 16-layer power-of-two step, '4 grid' the integer forward over T x alpha)")
     ap.add_argument("--mode", default="train", choices=["train", "decode", "configs"],
                     help="train: the fwd+bwd step (default); decode: one token per sequence; "
                          "configs: one line per configuration of the pages")
