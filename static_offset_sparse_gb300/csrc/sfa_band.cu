@@ -373,6 +373,13 @@ __device__ __forceinline__ void band_softmax(float (*s)[N], float* m, float* l, 
   }
 }
 
+// Whether every row of the warp reads all 32 key columns c0 .. c0 + 31 of the
+// current tile (lo, hi: this lane's two rows' column ranges; a row past the
+// sequence has hi = -1 and never qualifies).  Warp-uniform.
+__device__ __forceinline__ bool band_half_full(const int* lo, const int* hi, int c0) {
+  return __all_sync(0xffffffffu, lo[0] <= c0 && lo[1] <= c0 && hi[0] >= c0 + 31 && hi[1] >= c0 + 31);
+}
+
 // Query-tile geometry shared by the forward and the query-side backward.
 template <int G>
 struct QTile {
@@ -529,13 +536,22 @@ __global__ void __launch_bounds__(kBThreads, 5)
       for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
       qk_tiles4(qa, kst, 32 * hf, acc);
       float s[2][8];
+      // inside the band: every row of the warp reads all 32 keys of the half,
+      // so the per-element mask (which would pass them all) is skipped
+      if (band_half_full(lo, hi, 32 * hf)) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
-          s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
-        }
+          for (int e = 0; e < 4; ++e) s[e >> 1][2 * nt + (e & 1)] = acc[nt][e] * kLog2e;
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
+            s[x][2 * nt + (e & 1)] = (col >= lo[x] && col <= hi[x]) ? acc[nt][e] * kLog2e : -INFINITY;
+          }
+      }
       band_softmax<8>(s, m, l, o);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
@@ -688,17 +704,29 @@ __global__ void __launch_bounds__(kBThreads, 3)
         qk_tile(da, vst, row, dp[nt]);
       }
       float ds[4][4], pp[4][4];
+      if (mh == 15u && band_half_full(lo, hi, 32 * hf)) {  // no key of the half is masked
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pp[nt][e] = ex2(fmaf(sc[nt][e], kLog2e, -lse2[e >> 1]));
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
+            pp[nt][e] = ((mh >> nt) & 1u) && col >= lo[x] && col <= hi[x]
+                            ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x]))
+                            : 0.0f;
+          }
+      }
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int x = e >> 1, col = 32 * hf + 8 * nt + 2 * tig + (e & 1);
-          const float pr = ((mh >> nt) & 1u) && col >= lo[x] && col <= hi[x]
-                               ? ex2(fmaf(sc[nt][e], kLog2e, -lse2[x]))
-                               : 0.0f;
-          ds[nt][e] = pr * (dp[nt][e] - dlt[x]);
-          pp[nt][e] = pr;
-          psum[x] = fmaf(pr, dp[nt][e], psum[x]);
+          const int x = e >> 1;
+          ds[nt][e] = pp[nt][e] * (dp[nt][e] - dlt[x]);
+          psum[x] = fmaf(pp[nt][e], dp[nt][e], psum[x]);
         }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
@@ -852,17 +880,32 @@ __global__ void __launch_bounds__(kBThreads, 3)
         qk_tiles4(ka, qst, 32 * hq, st);
         qk_tiles4(va, dst, 32 * hq, dpt);
       }
+      // the half's query positions are ua .. ub (each head's, for G > 2); when
+      // every one of them reads every key row of the warp through the run, the
+      // per-element test (which would pass them all) is skipped
+      const int ua = cw.us + (BU >= 32 ? (32 * hq) % BU : 0), ub = ua + min(BU, 32) - 1;
+      const bool full = mh == 15u && vmin + 15 < Uc && ub < Uc && ua - (vmin + 15) + cw.e >= 0 &&
+                        ub - vmin + cw.e <= len - 1;
       float pp[4][4], ds[4][4];
+      if (full) {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pp[nt][e] = ex2(fmaf(st[nt][e], kLog2e, -sd[nt][e & 1].x));
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int x = e >> 1, c = e & 1;
+            const bool valid = (unsigned)(uq[nt][c] + tb[x]) < (unsigned)len;
+            pp[nt][e] = valid ? ex2(fmaf(st[nt][e], kLog2e, -sd[nt][c].x)) : 0.0f;
+          }
+      }
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = e >> 1, c = e & 1;
-          const bool valid = (unsigned)(uq[nt][c] + tb[x]) < (unsigned)len;
-          const float pr = valid ? ex2(fmaf(st[nt][e], kLog2e, -sd[nt][c].x)) : 0.0f;
-          pp[nt][e] = pr;
-          ds[nt][e] = pr * (dpt[nt][e] - sd[nt][c].y);
-        }
+        for (int e = 0; e < 4; ++e) ds[nt][e] = pp[nt][e] * (dpt[nt][e] - sd[nt][e & 1].y);
       // a key row sums P and dS over up to G x len (query, head) pairs, with
       // sum P above 1 for the early keys: both go in as bf16 hi + lo
 #pragma unroll
