@@ -49,6 +49,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fwd+bwd sparse-attn tokens/s at T=1024 GQA bf16; HBM GB/s vs GB300 peak"
 B, T, HQ, HKV, D = 32, 1024, 8, 2, 64
 LAYERS = 16  # --layers changes it for profiling captures of a smaller case
+ORDER = "training"  # --order: "training" (all forwards, then backwards last to first) or "layerwise"
 FIB = [1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987]
 ROPE = 1e4
 SEED = 0
@@ -237,12 +238,36 @@ class Layer:
                       self.nws)
         self.lib = lib
 
-    def run(self, stream):
+    def run_fwd(self, stream):
         rc = self.lib.sfa_rope_keys(*self.rargs, stream)
         rc = rc or self.lib.sfa_forward(*self.fargs, stream)
-        rc = rc or self.lib.sfa_backward(*self.bargs, stream)
         if rc:
             raise RuntimeError(f"libsfa status {rc}")
+
+    def run_bwd(self, stream):
+        rc = self.lib.sfa_backward(*self.bargs, stream)
+        if rc:
+            raise RuntimeError(f"libsfa status {rc}")
+
+    def run(self, stream):
+        self.run_fwd(stream)
+        self.run_bwd(stream)
+
+
+def run_layers(layers, stream):
+    """One training step's attention calls in a training step's order: every
+    layer's forward (its keys rotated once, kept like a saved activation),
+    then the backwards from the last layer to the first.  With ORDER ==
+    "layerwise" each layer's backward follows its own forward instead (then
+    the backward finds that layer's tensors still in L2)."""
+    if ORDER == "layerwise":
+        for L in layers:
+            L.run(stream)
+        return
+    for L in layers:
+        L.run_fwd(stream)
+    for L in reversed(layers):
+        L.run_bwd(stream)
 
 
 def gpu_arm(args, rank, world, dev):
@@ -265,8 +290,7 @@ def gpu_arm(args, rank, world, dev):
     dtheta = torch.zeros((LAYERS,), dtype=torch.float64, device=dev)
 
     def step():
-        for L in layers:
-            L.run(sp)
+        run_layers(layers, sp)
         if world > 1:
             allreduce_dtheta([L.dadt for L in layers], dtheta)
 
@@ -310,9 +334,7 @@ def gpu_arm(args, rank, world, dev):
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            cs = C.c_void_p(torch.cuda.current_stream().cuda_stream)
-            for L in layers:
-                L.run(cs)
+            run_layers(layers, C.c_void_p(torch.cuda.current_stream().cuda_stream))
         run = graph.replay
         for _ in range(args.warmup):
             run()
@@ -934,14 +956,11 @@ def grid_arm(args, dev, staggered_pow2=False):
             stream = torch.cuda.current_stream()
             sp = C.c_void_p(stream.cuda_stream)
             for _ in range(args.warmup):
-                for L in layers:
-                    L.run(sp)
+                run_layers(layers, sp)
             torch.cuda.synchronize()
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
-                cs = C.c_void_p(torch.cuda.current_stream().cuda_stream)
-                for L in layers:
-                    L.run(cs)
+                run_layers(layers, C.c_void_p(torch.cuda.current_stream().cuda_stream))
             for _ in range(args.warmup):
                 graph.replay()
             torch.cuda.synchronize()
@@ -973,6 +992,8 @@ def config(args):
                         f"D={D}, {LAYERS} layers, Fibonacci K=15, RoPE 1e4, fwd+bwd+dtheta",
             "global_batch": B * args.gpus, "seq_len": T, "layers": LAYERS, "W": args.W,
             "schedule": args.schedule, "parallelism": f"dp{args.gpus}",
+            "order": ("every forward, then the backwards from the last layer to the first"
+                      if args.order == "training" else "each layer's backward right after its forward"),
             "l2": "inputs exceed L2 (16 distinct layers, 2.6 GB per step); no flush"}
 
 
@@ -987,6 +1008,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=16, help="profiling captures only")
+    ap.add_argument("--order", default="training", choices=["training", "layerwise"],
+                    help="order of the step's calls: training (every forward, then the "
+                         "backwards last to first) or layerwise (each layer's backward right "
+                         "after its forward)")
     ap.add_argument("--only", default="", help="configs mode: run the configurations whose name "
                     "starts with this (e.g. '5:'; '2 grid' runs only the W x schedule grid, '3 staggered' "
                     "only the 16-layer power-of-two step, '4 grid' the integer forward over T x alpha)")
@@ -995,8 +1020,9 @@ def main():
                          "configs: one line per configuration of the pages")
     ap.add_argument("--decode-batch", type=int, default=32)
     args = ap.parse_args()
-    global LAYERS
+    global LAYERS, ORDER
     LAYERS = args.layers
+    ORDER = args.order
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
