@@ -29,6 +29,51 @@ def test_pair_counts_match_oracle_key_sets():
             assert pairs == ok.sum() and rung == ok[rung_rows].sum()
 
 
+def test_pair_counts_take_other_base_lists():
+    import bench
+
+    pow2 = [1 << j for j in range(11)]
+    slots = o.interp_slots(pow2, 0.5 + 9 / 15, 8)
+    T = bench.T
+    want = sum(max(0, T - (sl["s"] if sl["kind"] == "win" else sl["c"])) for sl in slots)
+    assert bench.pair_counts(0.5 + 9 / 15, 8, pow2)[0] == want
+
+
+def test_step_order():
+    """The timed step runs every layer's forward first, then the backwards
+    from the last layer to the first; --order layerwise pairs them per layer."""
+    import bench
+
+    calls = []
+
+    class FakeLayer:
+        def __init__(self, i):
+            self.i = i
+
+        def run_fwd(self, stream):
+            calls.append(("fwd", self.i))
+
+        def run_bwd(self, stream):
+            calls.append(("bwd", self.i))
+
+        def run(self, stream):
+            self.run_fwd(stream)
+            self.run_bwd(stream)
+
+    layers = [FakeLayer(i) for i in range(3)]
+    saved = bench.ORDER
+    try:
+        bench.ORDER = "training"
+        bench.run_layers(layers, None)
+        assert calls == [("fwd", 0), ("fwd", 1), ("fwd", 2), ("bwd", 2), ("bwd", 1), ("bwd", 0)]
+        calls.clear()
+        bench.ORDER = "layerwise"
+        bench.run_layers(layers, None)
+        assert calls == [("fwd", 0), ("bwd", 0), ("fwd", 1), ("bwd", 1), ("fwd", 2), ("bwd", 2)]
+    finally:
+        bench.ORDER = saved
+
+
 def test_schedules_match_oracle():
     import bench
 
