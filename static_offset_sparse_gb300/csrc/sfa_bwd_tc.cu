@@ -319,7 +319,8 @@ __global__ void __launch_bounds__(kTcThreads, 4)
 }
 
 constexpr int kKvTK = 32;                     // key rows per CTA
-constexpr int kKvThreads = 256;               // 8 warps: 4 key groups of 8 rows x 2 dim halves
+constexpr int kKvThreads = 128;               // 4 warps: 8 key rows each, all 64 dims
+constexpr int kKvMT = 4;                      // dK / dV m-tiles per warp (16 dims each)
 // A rung group reaches queries j + c - 1 .. j + c + 31 (33 rows); 34 rows keep
 // the plane stride at 2 (mod 8), so the 128B swizzle puts the 8 (query, head)
 // rows of one ldmatrix tile on distinct banks.  Each warp reads 12 of them (3
@@ -335,7 +336,7 @@ constexpr int kKvStages = 2;
 //
 // G = 4 (16-byte records): chunks of 3 distances need the rung groups' 34 rows,
 // so every stage is [2 planes][4 heads][34 rows][128 B] + 2 KB of records
-// (36 KB) and three CTAs (24 warps) fit on an SM.  G > 4 (32-byte records)
+// (36 KB) and three CTAs (12 warps) fit on an SM.  G > 4 (32-byte records)
 // keeps chunks of 9 distances (42 rows, 4 k-steps) in 54 KB stages, two CTAs
 // per SM.
 template <bool MULTI>
@@ -360,7 +361,8 @@ __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
 }
 
 // One group's products for a warp: NKS k-steps of 16 (query, head) pairs.
-// dk / dv hold m-tiles dh and dh + 2 (dims 16 dh .. +15 and 32 + 16 dh ..).
+// dk / dv hold the warp's 4 m-tiles (dims 16 mt .. 16 mt + 15): the record
+// selection of a lane's key is done once for all 64 dims.
 //
 // B: the records of the (query, head) pairs k = 2 tig, 2 tig + 1 (+8) that
 // reach the lane's key j.  Within a query the k order of the heads is 0, 2,
@@ -384,7 +386,7 @@ __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
 // corrections), then selects.
 template <int NKS, int STEP, bool FOLD, bool ONEHOT = false>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int rec,
-                                         uint32_t mask, int qw, int kq, int qoff, int T, int dh,
+                                         uint32_t mask, int qw, int kq, int qoff, int T,
                                          const float* corr, float (*dk)[4], float (*dv)[4]) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
   using Fmt = CoefFmt<FOLD>;
@@ -464,17 +466,16 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
     const int kx = 8 * (mi >> 1) + (lane & 7);
     const int arow = (((kx & 1) << 1) | ((kx >> 1) & 1)) * kq + qoff + 4 * ks + (kx >> 2);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int mt = dh + 2 * x;
+    for (int mt = 0; mt < kKvMT; ++mt) {
       uint32_t aq[4], ad[4];
       const uint32_t off = swz(arow, 2 * mt + (mi & 1));
       ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
       ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
-      mma_bf16(dk[x], aq, bk[0], bk[1]);
-      mma_bf16(dv[x], ad, bvv[0], bvv[1]);
+      mma_bf16(dk[mt], aq, bk[0], bk[1]);
+      mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
       if (FOLD) {
-        mma_bf16(dk[x], aq, bkl[0], bkl[1]);
-        mma_bf16(dv[x], ad, bvl[0], bvl[1]);
+        mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
+        mma_bf16(dv[mt], ad, bvl[0], bvl[1]);
       }
     }
   }
@@ -493,7 +494,7 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
   unsigned char* sgen = smem_raw + (sbase - smem_u32(smem_raw));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  const int kw = warp >> 1, dh = warp & 1;
+  const int kw = warp;  // key group: rows 8 kw .. 8 kw + 7 of the tile
   const int bg = blockIdx.y, b = bg / a.Hkv, g = bg - b * a.Hkv;
   const int T = a.T;
   const int j0 = blockIdx.x * kKvTK, j0w = j0 + 8 * kw;
@@ -505,9 +506,9 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
   auto hplane_of = [&](int sg) { return b * a.Hq + (g * msub + sg) * 4; };
   auto rplane_of = [&](int sg) { return b * (a.Hq >> 2) + g * msub + sg; };
 
-  float dk[2][4], dv[2][4];
+  float dk[kKvMT][4], dv[kKvMT][4];
 #pragma unroll
-  for (int x = 0; x < 2; ++x) dk[x][0] = dk[x][1] = dk[x][2] = dk[x][3] = dv[x][0] = dv[x][1] =
+  for (int x = 0; x < kKvMT; ++x) dk[x][0] = dk[x][1] = dk[x][2] = dk[x][3] = dv[x][0] = dv[x][1] =
       dv[x][2] = dv[x][3] = 0.0f;
 
   const int wmax = min(P.W, T - 1 - j0);
@@ -546,16 +547,20 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
   if (tid == 0)
     for (int s = 0; s < kKvStages && s < NGt; ++s) issue(s, sbase + s * L::StageB, smem_u32(&bars[s]));
   // the RoPE pairs of the dK epilogue (keys 2 tig (+1) of the warp's group,
-  // pairs 16 dh + gid (+8)), loaded now so their latency hides under the loop
+  // pairs 16 h2 + gid (+8) for h2 = 0, 1), loaded now so their latency hides
+  // under the loop
   const float2* rope = static_cast<const float2*>(a.rope);
-  float2 kcs[2][2];
+  float2 kcs[2][2][2];
   if (rope)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int jj = min(j0w + 2 * tig + e, T - 1);
+    for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) kcs[e][hh] = __ldg(rope + (int64_t)jj * 32 + 16 * dh + gid + 8 * hh);
-    }
+      for (int e = 0; e < 2; ++e) {
+        const int jj = min(j0w + 2 * tig + e, T - 1);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          kcs[h2][e][hh] = __ldg(rope + (int64_t)jj * 32 + 16 * h2 + gid + 8 * hh);
+      }
   int grpm = 0;  // with MULTI: gt mod NG, kept by a counter (no division per group)
   for (int gt = 0; gt < NGt; ++gt) {
     const int grp = MULTI ? grpm : gt;
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
           j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + L::WC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
       const int rec = (qoff * L::WC + rel) * RW + HW * (tig & 1) + t1 * (L::WC + 1) * RW;
       kv_group<L::WKS, (L::WC + 1) * RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, L::Q, qoff,
-                                                T, dh, corr, dk, dv);
+                                                T, corr, dk, dv);
     } else {
       // rung: query qw + ql reaches key j as role 1 (key i - c + 1) when
       // ql + rel = 0 and as role 0 (key i - c) when ql + rel = 1, and only if
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
       const uint32_t mask =
           j < T ? ql_mask(max(INTERP ? -rel : 1 - rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<RKS, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T, dh,
+      kv_group<RKS, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T,
                                      corr, dk, dv);
     }
     __syncthreads();
@@ -607,35 +612,38 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
   }
 
   // dK = R(-phi) dk' at key positions; transpose through shared memory for
-  // row-contiguous stores.  Lane holds dims 16 mt + gid (+8) for mt = dh,
-  // dh + 2, keys 2 tig (+1) of its key group.
+  // row-contiguous stores.  Lane holds dims 16 mt + gid (+8) for mt = 0..3,
+  // keys 2 tig (+1) of its key group.
   if (rope) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float2 cs = kcs[e][hh];
-        const float lo = dk[0][2 * hh + e], hi = dk[1][2 * hh + e];
-        dk[0][2 * hh + e] = lo * cs.x + hi * cs.y;
-        dk[1][2 * hh + e] = hi * cs.x - lo * cs.y;
+      for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // m-tiles h2 and h2 + 2 hold dims d and d + 32
+          const float2 cs = kcs[h2][e][hh];
+          const float lo = dk[h2][2 * hh + e], hi = dk[h2 + 2][2 * hh + e];
+          dk[h2][2 * hh + e] = lo * cs.x + hi * cs.y;
+          dk[h2 + 2][2 * hh + e] = hi * cs.x - lo * cs.y;
+        }
       }
-    }
   }
   bf16* tk = reinterpret_cast<bf16*>(sgen);  // [32 keys][72] for dK, then dV
   bf16* tv = tk + kKvTK * 72;
 #pragma unroll
-  for (int x = 0; x < 2; ++x)
+  for (int x = 0; x < kKvMT; ++x)
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int d = 16 * (dh + 2 * x) + gid + 8 * hh, n = 8 * kw + 2 * tig + e;
+        const int d = 16 * x + gid + 8 * hh, n = 8 * kw + 2 * tig + e;
         tk[n * 72 + d] = __float2bfloat16_rn(dk[x][2 * hh + e]);
         tv[n * 72 + d] = __float2bfloat16_rn(dv[x][2 * hh + e]);
       }
   __syncthreads();
-  {
-    const int n = tid >> 3, ch = tid & 7;  // key row n of the tile, 8 dims per thread
+  for (int it = tid; it < kKvTK * 8; it += kKvThreads) {
+    const int n = it >> 3, ch = it & 7;  // key row n of the tile, 8 dims per thread
     const int jr = j0 + n;
     if (jr < T) {
       const int64_t row = ((int64_t)bg * T + jr) * kD + 8 * ch;
