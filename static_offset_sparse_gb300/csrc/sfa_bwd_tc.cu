@@ -329,28 +329,36 @@ constexpr int kKvMT = 4;                      // dK / dV m-tiles per warp (16 di
 constexpr int kKvQR = kKvTK + 2;
 constexpr int kKvStages = 2;
 
-// Stage layout of the key side.  A window chunk of WC distances reaches
-// queries j0 + s_lo .. j0 + 31 + s_lo + WC - 1, staged as Q rows per head plane
-// (Q = 2 mod 8 again); a warp reads WKS k-steps of them from row
-// min(8 kw, Q - 4 WKS) on.
+// Stage layout of the key side.  A window chunk of WC = 9 distances reaches
+// queries j0 + s_lo .. j0 + 31 + s_lo + 8, staged as Q = 42 rows per head plane
+// (Q = 2 mod 8 again); a warp reads WKS = 4 k-steps of them from row
+// min(8 kw, Q - 4 WKS) on.  A rung group stages 34 rows ([4 heads][34][128 B]
+// for q~ and for dO) and its records.
 //
-// G = 4 (16-byte records): chunks of 3 distances need the rung groups' 34 rows,
-// so every stage is [2 planes][4 heads][34 rows][128 B] + 2 KB of records
-// (36 KB) and three CTAs (12 warps) fit on an SM.  G > 4 (32-byte records)
-// keeps chunks of 9 distances (42 rows, 4 k-steps) in 54 KB stages, two CTAs
-// per SM.
+// G = 4 (16-byte records, SPLIT): a window chunk runs as two pipeline groups,
+// its q~ slab with the records (the dK products; the lane's dV coefficients
+// are kept in registers) and then its dO slab (the dV products), so every
+// stage fits in 36 KB (a rung group: 2 x 17 KB + 1 KB of records) and three
+// CTAs (12 warps) stay on an SM, while the window's rows are staged once.
+// G > 4 (32-byte records) stages a window chunk's two slabs and records
+// together in 54 KB stages, two CTAs per SM.
 template <bool MULTI>
 struct KvLayout {
-  static constexpr int WC = MULTI ? 9 : 3;
-  static constexpr int Q = MULTI ? kKvTK + 10 : kKvQR;
-  static constexpr int WKS = MULTI ? 4 : 3;
-  static constexpr int PlaneB = Q * 4 * 128;             // q~ (or dO) box
-  static constexpr int RecB = MULTI ? 12288 : 2048;      // records box [Q queries][WC slots][16 or 32 B]
-  static constexpr int StageB = 2 * PlaneB + RecB;
+  static constexpr bool SPLIT = !MULTI;
+  static constexpr int WC = 9;
+  static constexpr int Q = kKvTK + 10;
+  static constexpr int WKS = 4;
+  static constexpr int PlaneB = Q * 4 * 128;                       // a window slab (q~ or dO)
+  static constexpr int WRecB = Q * WC * CoefFmt<MULTI>::kRecBytes;  // a window chunk's records
+  static constexpr int RDoff = MULTI ? PlaneB : kKvQR * 4 * 128;   // a rung group's dO slab
+  static constexpr int StageB = MULTI ? 2 * PlaneB + 12288 : 36864;
   static constexpr int MinBlocks = MULTI ? 2 : 3;
   static constexpr size_t Smem = (size_t)kKvStages * StageB + 1024;
-  static_assert(Q * WC * CoefFmt<MULTI>::kRecBytes <= RecB && Q % 8 == 2, "key-side stage layout");
-  static_assert(PlaneB % 1024 == 0 && StageB % 1024 == 0, "swizzled boxes sit on 1024-byte periods");
+  static_assert(Q % 8 == 2 && kKvQR % 8 == 2, "slab strides 2 (mod 8)");
+  static_assert((SPLIT ? PlaneB : 2 * PlaneB) + WRecB <= StageB, "window chunk fits a stage");
+  static_assert(2 * RDoff + kKvQR * 2 * CoefFmt<MULTI>::kRecBytes <= StageB, "rung group fits a stage");
+  static_assert(PlaneB % 1024 == 0 && RDoff % 1024 == 0 && StageB % 1024 == 0,
+                "swizzled boxes sit on 1024-byte periods");
 };
 
 // Bits m of the query offsets ql = m + t1 (t1 = tig >> 1) with lo <= ql <= hi.
@@ -384,10 +392,15 @@ __device__ __forceinline__ uint32_t ql_mask(int lo, int hi, int t1) {
 // consecutive, so at most one of the (k-step, half) entries it reads (query
 // offsets of one parity) is set: one record load (and with FOLD one pair of
 // corrections), then selects.
-template <int NKS, int STEP, bool FOLD, bool ONEHOT = false>
+//
+// PASS 0 runs both products; PASS 1 (a split window chunk's q~ slab) runs the
+// dK products and keeps the lane's dV coefficients in bsave; PASS 2 (its dO
+// slab, in dst) runs the dV products from bsave.
+template <int NKS, int STEP, bool FOLD, bool ONEHOT = false, int PASS = 0>
 __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint32_t* csm, int rec,
                                          uint32_t mask, int qw, int kq, int qoff, int T,
-                                         const float* corr, float (*dk)[4], float (*dv)[4]) {
+                                         const float* corr, float (*dk)[4], float (*dv)[4],
+                                         uint32_t (*bsave)[2] = nullptr) {
   const int lane = threadIdx.x & 31, tig = lane & 3, mi = lane >> 3;
   using Fmt = CoefFmt<FOLD>;
   // ONEHOT: the lane's one entry m1 (-1: none) as the four B words dS, dS lo,
@@ -435,7 +448,9 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
     for (int hb = 0; hb < 2; ++hb) {
       const int m = 4 * ks + 2 * hb;
       bk[hb] = bkl[hb] = bvv[hb] = bvl[hb] = 0u;
-      if (ONEHOT) {
+      if (PASS == 2) {
+        bvv[hb] = bsave[ks][hb];
+      } else if (ONEHOT) {
         bk[hb] = m1 == m ? one.x : 0u;
         bvv[hb] = m1 == m ? one.z : 0u;
         if (FOLD) {
@@ -463,19 +478,25 @@ __device__ __forceinline__ void kv_group(uint32_t qst, uint32_t dst, const uint3
     // A: q~^T and dO^T [16 dims x 16 (query, head)] by transposed ldmatrix;
     // k index kx = 4 (query offset) + hs (head slot; head 2 (hs & 1) + (hs >> 1)
     // by the order 0, 2, 1, 3) lives in slab row head * kq + query
+    if (PASS == 1) {
+      bsave[ks][0] = bvv[0];
+      bsave[ks][1] = bvv[1];
+    }
     const int kx = 8 * (mi >> 1) + (lane & 7);
     const int arow = (((kx & 1) << 1) | ((kx >> 1) & 1)) * kq + qoff + 4 * ks + (kx >> 2);
 #pragma unroll
     for (int mt = 0; mt < kKvMT; ++mt) {
       uint32_t aq[4], ad[4];
       const uint32_t off = swz(arow, 2 * mt + (mi & 1));
-      ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
-      ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
-      mma_bf16(dk[mt], aq, bk[0], bk[1]);
-      mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
-      if (FOLD) {
-        mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
-        mma_bf16(dv[mt], ad, bvl[0], bvl[1]);
+      if (PASS != 2) {
+        ldsm_x4_t(qst + off, aq[0], aq[1], aq[2], aq[3]);
+        mma_bf16(dk[mt], aq, bk[0], bk[1]);
+        if (FOLD) mma_bf16(dk[mt], aq, bkl[0], bkl[1]);
+      }
+      if (PASS != 1) {
+        ldsm_x4_t(dst + off, ad[0], ad[1], ad[2], ad[3]);
+        mma_bf16(dv[mt], ad, bvv[0], bvv[1]);
+        if (FOLD) mma_bf16(dv[mt], ad, bvl[0], bvl[1]);
       }
     }
   }
@@ -514,26 +535,38 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
   const int wmax = min(P.W, T - 1 - j0);
   using L = KvLayout<MULTI>;
   const int nwc = wmax >= 0 ? wmax / L::WC + 1 : 0;
+  const int nwg = L::SPLIT ? 2 * nwc : nwc;  // window groups (SPLIT: q~ pass, then dO pass)
   const int nr = rungs_upto(P, T - j0);
-  const int NG = nwc + nr;       // groups per query-head group
+  const int NG = nwg + nr;       // groups per query-head group
   const int NGt = MULTI ? NG * msub : NG;  // all groups: query-head group gt / NG, group gt % NG
-  // group -> first staged query: window chunk s_lo = WC grp, or rung grp - nwc
-  auto qb_of = [&](int grp) { return grp < nwc ? j0 + L::WC * grp : j0 + P.c[grp - nwc] - 1; };
+  // window group -> its chunk; group -> first staged query: window chunk
+  // s_lo = WC chunk, or rung grp - nwg
+  auto chunk_of = [&](int grp) { return L::SPLIT ? grp >> 1 : grp; };
+  auto qb_of = [&](int grp) { return grp < nwg ? j0 + L::WC * chunk_of(grp) : j0 + P.c[grp - nwg] - 1; };
   auto issue = [&](int gt, uint32_t st, uint32_t bar) {
     const int sg = MULTI ? gt / NG : 0, grp = MULTI ? gt - sg * NG : gt;
     const int hplane = hplane_of(sg), rp = rplane_of(sg);
-    const bool win = grp < nwc;
     const int qb = qb_of(grp);
-    if (win) {
-      mbar_expect_tx(bar, 2 * L::PlaneB + L::Q * L::WC * CoefFmt<MULTI>::kRecBytes);
-      tma_load_3d(st, &mq, 0, qb, hplane, bar);
-      tma_load_3d(st + L::PlaneB, &md, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * L::PlaneB, &mcw, 0, L::WC * grp, qb, rp, bar);
+    if (grp < nwg) {
+      const int ch = chunk_of(grp);
+      if (!L::SPLIT) {
+        mbar_expect_tx(bar, 2 * L::PlaneB + L::WRecB);
+        tma_load_3d(st, &mq, 0, qb, hplane, bar);
+        tma_load_3d(st + L::PlaneB, &md, 0, qb, hplane, bar);
+        tma_load_4d(st + 2 * L::PlaneB, &mcw, 0, L::WC * ch, qb, rp, bar);
+      } else if ((grp & 1) == 0) {  // q~ slab and records
+        mbar_expect_tx(bar, L::PlaneB + L::WRecB);
+        tma_load_3d(st, &mq, 0, qb, hplane, bar);
+        tma_load_4d(st + L::PlaneB, &mcw, 0, L::WC * ch, qb, rp, bar);
+      } else {  // dO slab
+        mbar_expect_tx(bar, L::PlaneB);
+        tma_load_3d(st, &md, 0, qb, hplane, bar);
+      }
     } else {
       mbar_expect_tx(bar, 2 * kKvQR * 4 * 128 + kKvQR * 2 * CoefFmt<MULTI>::kRecBytes);
       tma_load_3d(st, &mqr, 0, qb, hplane, bar);
-      tma_load_3d(st + L::PlaneB, &mdr, 0, qb, hplane, bar);
-      tma_load_4d(st + 2 * L::PlaneB, &mcr, 0, P.W + 1 + 2 * (grp - nwc), qb, rp, bar);
+      tma_load_3d(st + L::RDoff, &mdr, 0, qb, hplane, bar);
+      tma_load_4d(st + 2 * L::RDoff, &mcr, 0, P.W + 1 + 2 * (grp - nwg), qb, rp, bar);
     }
   };
 
@@ -561,6 +594,7 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
         for (int hh = 0; hh < 2; ++hh)
           kcs[h2][e][hh] = __ldg(rope + (int64_t)jj * 32 + 16 * h2 + gid + 8 * hh);
       }
+  uint32_t wsave[L::WKS][2];  // SPLIT: a window chunk's dV coefficients between its two groups
   int grpm = 0;  // with MULTI: gt mod NG, kept by a counter (no division per group)
   for (int gt = 0; gt < NGt; ++gt) {
     const int grp = MULTI ? grpm : gt;
@@ -575,21 +609,33 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
       return;
     }
     const uint32_t qst = sbase + st * L::StageB;
-    const uint32_t* csm = reinterpret_cast<const uint32_t*>(sgen + st * L::StageB + 2 * L::PlaneB);
+    const unsigned char* stg = sgen + st * L::StageB;
     // MULTI: query-head group gt / NG; its delta - psi rows for the correction
     const float* corr = MULTI ? a.dcorr + (int64_t)hplane_of(gt / NG) * T : nullptr;
     constexpr int RW = CoefFmt<MULTI>::kRecWords, HW = CoefFmt<MULTI>::kHalfWords;
     const int t1 = tig >> 1;
-    if (grp < nwc) {
+    if (grp < nwg) {
       // window chunk: query qw + ql reaches key j through slot s = ql + rel of
       // the chunk (s in 0 .. s_hi - s_lo), record (qoff + ql) * WC + s
-      const int s_lo = L::WC * grp, qoff = min(8 * kw, L::Q - 4 * L::WKS), qw = qb_of(grp) + qoff;
-      const int rel = qw - j - s_lo;
-      const uint32_t mask =
-          j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + L::WC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
-      const int rec = (qoff * L::WC + rel) * RW + HW * (tig & 1) + t1 * (L::WC + 1) * RW;
-      kv_group<L::WKS, (L::WC + 1) * RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, L::Q, qoff,
-                                                T, corr, dk, dv);
+      const int s_lo = L::WC * chunk_of(grp), qoff = min(8 * kw, L::Q - 4 * L::WKS);
+      const int qw = qb_of(grp) + qoff;
+      if (L::SPLIT && (grp & 1)) {  // the chunk's dO slab: dV from the kept coefficients
+        kv_group<L::WKS, (L::WC + 1) * RW, MULTI, false, 2>(qst, qst, nullptr, 0, 0u, qw, L::Q, qoff,
+                                                           T, corr, dk, dv, wsave);
+      } else {
+        const int rel = qw - j - s_lo;
+        const uint32_t mask =
+            j < T ? ql_mask(max(-rel, 0), min(min(P.W, s_lo + L::WC - 1) - s_lo - rel, T - 1 - qw), t1) : 0u;
+        const int rec = (qoff * L::WC + rel) * RW + HW * (tig & 1) + t1 * (L::WC + 1) * RW;
+        const uint32_t* csm =
+            reinterpret_cast<const uint32_t*>(stg + (L::SPLIT ? 1 : 2) * L::PlaneB);
+        if (L::SPLIT)  // the chunk's q~ slab and records: dK, and the dV coefficients kept
+          kv_group<L::WKS, (L::WC + 1) * RW, MULTI, false, 1>(qst, qst, csm, rec, mask, qw, L::Q, qoff,
+                                                             T, corr, dk, dv, wsave);
+        else
+          kv_group<L::WKS, (L::WC + 1) * RW, MULTI>(qst, qst + L::PlaneB, csm, rec, mask, qw, L::Q,
+                                                    qoff, T, corr, dk, dv);
+      }
     } else {
       // rung: query qw + ql reaches key j as role 1 (key i - c + 1) when
       // ql + rel = 0 and as role 0 (key i - c) when ql + rel = 1, and only if
@@ -597,13 +643,14 @@ __global__ void __launch_bounds__(kKvThreads, KvLayout<MULTI>::MinBlocks)
       // An integer rung (w = 0) has no role 1: a warp's 8 keys then read 8
       // queries, 8 kw + 1 .. 8 kw + 8 of the slab, two k-steps instead of three
       constexpr int RKS = INTERP ? 3 : 2;
-      const int c = P.c[grp - nwc];
+      const int c = P.c[grp - nwg];
       const int qoff = INTERP ? min(8 * kw, kKvQR - 12) : 8 * kw + 1, qw = qb_of(grp) + qoff;
       const int rel = qw - j - c + 1;
       const uint32_t mask =
           j < T ? ql_mask(max(INTERP ? -rel : 1 - rel, c - qw), min(1 - rel, T - 1 - qw), t1) : 0u;
       const int rec = (2 * qoff + 1 - rel) * RW + HW * (tig & 1) + t1 * RW;
-      kv_group<RKS, RW, MULTI, true>(qst, qst + L::PlaneB, csm, rec, mask, qw, kKvQR, qoff, T,
+      const uint32_t* csm = reinterpret_cast<const uint32_t*>(stg + 2 * L::RDoff);
+      kv_group<RKS, RW, MULTI, true>(qst, qst + L::RDoff, csm, rec, mask, qw, kKvQR, qoff, T,
                                      corr, dk, dv);
     }
     __syncthreads();
