@@ -218,3 +218,35 @@ def test_rung_kernels_groups_of_four_heads(sfa, B, T, Hq, Hkv):
     for name, got, key in (("dQ int", gi[0], "dq"), ("dK int", gi[1], "dk"), ("dV int", gi[2], "dv")):
         _check(name, got, gw[key], 2e-2)
     assert sfa.get_device_status() == 0
+
+
+@pytest.mark.parametrize("W,T,Hq", [(10, 70, 8), (12, 300, 8), (12, 129, 16), (9, 41, 4)])
+def test_rung_kernels_wide_window(sfa, W, T, Hq):
+    """Windows of 9 to 13 distances on the rung kernels: the key side stages a
+    window chunk of up to 9 distances (at G = 4 as two groups, its q~ slab with
+    the records, then its dO slab), so W = 10 and 12 take two chunks; ragged T,
+    interpolated (with dL/dalpha) and integer paths, element by element."""
+    base = o.fib_offsets(15)
+    x = si.make_qkvdo(1, T, Hq, 2 if Hq > 4 else 1, 64, "bf16", seed=400 + W + T)
+    alpha = 0.77
+    O, L, g = _run_interp(sfa, x, W, alpha, base, 1e4)
+    slots = o.interp_slots(base, alpha, W)
+    Ow, Lw = o.forward(x["q"], x["k"], x["v"], slots, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], slots, 1e4, alpha=alpha)
+    _check("O", O, Ow, 2e-2)
+    _check("LSE", L, Lw, 2e-2, bf16=False)
+    for name, got, key in (("dQ", g[0], "dq"), ("dK", g[1], "dk"), ("dV", g[2], "dv")):
+        _check(name, got, gw[key], 2e-2)
+    da, dt = _np(g[3])
+    check_dalpha_dtheta(da, dt, gw, alpha, True)
+    dist = sorted(set(range(W + 1)) | {round(alpha * f) for f in base})
+    q, k, v, do = (_dev(x[n]) for n in ("q", "k", "v", "do"))
+    Oi, Li = sfa.forward_int(q, k, v, dist=dist)
+    gi = sfa.backward_int(q, k, v, Oi, Li, do, dist=dist)
+    si_ = o.dist_slots(dist)
+    Ow, _ = o.forward(x["q"], x["k"], x["v"], si_, 1e4)
+    gw = o.backward(x["q"], x["k"], x["v"], x["do"], si_, 1e4)
+    _check("O int", Oi, Ow, 2e-2)
+    for name, got, key in (("dQ int", gi[0], "dq"), ("dK int", gi[1], "dk"), ("dV int", gi[2], "dv")):
+        _check(name, got, gw[key], 2e-2)
+    assert sfa.get_device_status() == 0
